@@ -1,0 +1,187 @@
+"""Seeded synthetic inputs for the GDN speculative transaction.
+
+This module is the one piece shared by the CUDA path's tests/bench and by the
+CPU oracle's callers.  It draws random numbers and lays them out; it holds none
+of the method's arithmetic (no convolution, normalisation, gating or delta rule).
+
+Random numbers come from SplitMix64 (Steele, Lea & Flood, "Fast splittable
+pseudorandom number generators", 2014) used as a counter-based generator:
+value i of stream (seed, name) is mix64(key(seed, name) + (i + 1) * golden),
+and normals come from the Box-Muller transform.  Everything is numpy, so the
+same seed gives the same arrays on x86 and Arm hosts (up to libm's last ulp in
+log/cos, which only matters after bf16 rounding in rare ties).
+
+Distributions follow the workloads named for this path (MTP depth-one verify
+cohorts of hybrid Qwen models):
+
+* raw pre-conv q|k|v inputs x ~ N(0, 1), rounded to bf16;
+* conv weights ~ N(0, 0.5^2) (std 0.5), rounded to bf16;
+* log-decay g = -softplus(N(0, 1)) * 0.5  (so g <= 0, alpha = e^g in (0, 1]);
+* write strength beta = sigmoid(N(0, 1));
+* recurrent state S0 ~ N(0, 0.1^2) (std 0.1), fp32;
+* primed conv window ~ N(0, 1) bf16; ring slots outside the committed window
+  hold bf16 NaN so that any read outside the window poisons the result;
+* committed offsets uniform in [3, 1000) so ring indices wrap arbitrarily;
+* keep per row uniform in {0..T}.
+"""
+from __future__ import annotations
+
+import dataclasses
+import zlib
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _key(seed: int, name: str) -> np.uint64:
+    tag = zlib.crc32(name.encode()) & 0xFFFFFFFF
+    base = np.array([(seed & 0xFFFFFFFF) << 32 | tag], dtype=np.uint64)
+    return _mix64(base)[0]
+
+
+def uniform(seed: int, name: str, n: int) -> np.ndarray:
+    """n doubles in the open interval (0, 1) from stream (seed, name)."""
+    i = np.arange(1, n + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = _mix64(_key(seed, name) + i * _GOLDEN)
+    return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
+
+
+def normal(seed: int, name: str, shape, std: float = 1.0) -> np.ndarray:
+    """fp64 normals N(0, std^2) of the given shape (Box-Muller, cosine branch)."""
+    n = int(np.prod(shape))
+    u = uniform(seed, name, 2 * n)
+    r = np.sqrt(-2.0 * np.log(u[0::2]))
+    return (std * r * np.cos(2.0 * np.pi * u[1::2])).reshape(shape)
+
+
+def integers(seed: int, name: str, shape, lo: int, hi: int) -> np.ndarray:
+    """int32 uniform in [lo, hi)."""
+    n = int(np.prod(shape))
+    u = uniform(seed, name, n)
+    return (lo + np.floor(u * (hi - lo))).astype(np.int32).reshape(shape)
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32/fp64 values to bf16 (round to nearest even); return uint16 bits."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact fp32 values of bf16 bit patterns."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclasses.dataclass(frozen=True)
+class Geometry:
+    """Shape of one GDN layer's speculative transaction.
+
+    B rows, T positions per verify, ring capacity for up to T_max positions,
+    H_k key heads, H_v value heads, head size d (= d_k = d_v), conv width 4.
+    """
+
+    B: int
+    T: int
+    H_k: int
+    H_v: int
+    d: int
+    T_max: int | None = None
+    width: int = 4
+    act: int = 1  # 1 = SiLU after the conv, 0 = none
+
+    @property
+    def tmax(self) -> int:
+        return self.T if self.T_max is None else self.T_max
+
+    @property
+    def C(self) -> int:
+        return 2 * self.H_k * self.d + self.H_v * self.d
+
+    @property
+    def R(self) -> int:
+        return self.width - 1 + self.tmax
+
+
+# Named workloads.  TINY is small enough for pure-Python checks; COHORT is the
+# depth-one MTP verify cohort (8 rows, 2 positions, Qwen-style 16/32 heads of 128).
+TINY = Geometry(B=1, T=2, H_k=2, H_v=4, d=32)
+COHORT = Geometry(B=8, T=2, H_k=16, H_v=32, d=128)
+
+
+def softplus(z: np.ndarray) -> np.ndarray:
+    return np.logaddexp(0.0, z)
+
+
+def layer_state(geom: Geometry, seed: int, n_layers: int = 1, offsets=None) -> dict:
+    """Persistent per-layer tensors: conv weights, state, ring and row offsets.
+
+    Returns numpy arrays:
+      conv_w  uint16 bf16 [n_layers][C][4]
+      state   float32     [n_layers][B][H_v][d_v][d_k]
+      ring    uint16 bf16 [n_layers][B][R][C]  (slot = absolute position mod R)
+      offsets int32       [B]  committed tokens per row (shared by all layers)
+    """
+    g = geom
+    w = bf16_bits(normal(seed, "conv_w", (n_layers, g.C, g.width), std=0.5))
+    s0 = normal(seed, "state", (n_layers, g.B, g.H_v, g.d, g.d), std=0.1).astype(np.float32)
+    if offsets is None:
+        offsets = integers(seed, "offsets", (g.B,), 3, 1000)
+    offsets = np.asarray(offsets, dtype=np.int32)
+    ring = np.full((n_layers, g.B, g.R, g.C), BF16_NAN, dtype=np.uint16)
+    win = bf16_bits(normal(seed, "window", (n_layers, g.B, g.width - 1, g.C)))
+    for b in range(g.B):
+        for i in range(g.width - 1):
+            pos = int(offsets[b]) - (g.width - 1) + i
+            ring[:, b, pos % g.R, :] = win[:, b, i, :]
+    return {"conv_w": w, "state": s0, "ring": ring, "offsets": offsets}
+
+
+def cycle_inputs(geom: Geometry, seed: int, cycle: int, n_layers: int = 1) -> dict:
+    """Per-cycle verify inputs for every layer plus the cycle's keep[] draw.
+
+      x     uint16 bf16 [n_layers][B][T][C]  raw pre-conv q|k|v
+      g     float32     [n_layers][B][T][H_v] log-decay (<= 0)
+      beta  float32     [n_layers][B][T][H_v]
+      keep  int32       [B] uniform in {0..T}
+    """
+    g = geom
+    tag = f"c{cycle}"
+    x = bf16_bits(normal(seed, "x" + tag, (n_layers, g.B, g.T, g.C)))
+    gl = (-softplus(normal(seed, "g" + tag, (n_layers, g.B, g.T, g.H_v))) * 0.5).astype(np.float32)
+    bz = normal(seed, "beta" + tag, (n_layers, g.B, g.T, g.H_v))
+    beta = (1.0 / (1.0 + np.exp(-bz))).astype(np.float32)
+    keep = integers(seed, "keep" + tag, (g.B,), 0, g.T + 1)
+    return {"x": x, "g": gl, "beta": beta, "keep": keep}
+
+
+def active_mask(B: int, inactive=()) -> np.ndarray:
+    a = np.ones(B, dtype=np.uint8)
+    for r in inactive:
+        a[r] = 0
+    return a
+
+
+def prompt_inputs(geom: Geometry, seed: int, L: int) -> dict:
+    """A prompt of L tokens for state priming (B rows, all active).
+
+      x    uint16 bf16 [B][L][C],  g, beta float32 [B][L][H_v]
+    """
+    g = geom
+    x = bf16_bits(normal(seed, "px", (g.B, L, g.C)))
+    gl = (-softplus(normal(seed, "pg", (g.B, L, g.H_v))) * 0.5).astype(np.float32)
+    bz = normal(seed, "pbeta", (g.B, L, g.H_v))
+    beta = (1.0 / (1.0 + np.exp(-bz))).astype(np.float32)
+    return {"x": x, "g": gl, "beta": beta}

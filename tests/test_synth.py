@@ -1,0 +1,46 @@
+"""The seeded input generator: determinism, distributions and bf16 rounding."""
+import numpy as np
+import torch
+
+from speculative_decode_gated_gdn_gb300 import synth
+
+
+def test_deterministic_and_stream_separated():
+    a = synth.normal(3, "x", (1000,))
+    b = synth.normal(3, "x", (1000,))
+    c = synth.normal(3, "y", (1000,))
+    d = synth.normal(4, "x", (1000,))
+    assert np.array_equal(a, b)
+    assert not np.allclose(a, c) and not np.allclose(a, d)
+
+
+def test_normal_moments():
+    z = synth.normal(0, "m", (200000,))
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1.0) < 0.01
+
+
+def test_bf16_rounding_matches_torch():
+    v = synth.normal(5, "r", (100000,)) * 37.0
+    ours = synth.bf16_bits(v)
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    back = synth.bf16_to_f32(ours)
+    assert np.array_equal(back, torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).float().numpy())
+
+
+def test_cohort_recipe():
+    g = synth.COHORT
+    assert g.C == 8192 and g.R == 5
+    st = synth.layer_state(g, 1)
+    cy = synth.cycle_inputs(g, 1, 0)
+    assert st["state"].shape == (1, 8, 32, 128, 128) and st["state"].dtype == np.float32
+    assert cy["x"].shape == (1, 8, 2, 8192) and cy["x"].dtype == np.uint16
+    assert np.all(cy["g"] <= 0) and np.all((cy["beta"] > 0) & (cy["beta"] < 1))
+    assert set(np.unique(cy["keep"])) <= {0, 1, 2}
+    # the committed window is filled, every other ring slot is poisoned with NaN
+    for b in range(g.B):
+        off = int(st["offsets"][b])
+        win_slots = {(off - 3 + i) % g.R for i in range(3)}
+        for s in range(g.R):
+            isnan = np.isnan(synth.bf16_to_f32(st["ring"][0, b, s]))
+            assert isnan.all() == (s not in win_slots)
