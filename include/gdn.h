@@ -1,0 +1,209 @@
+/*
+ * gdn.h -- C ABI of libgdn_gb300.so, the batched Gated DeltaNet (GDN)
+ * speculative transaction for MTP speculative decoding, written for GB300
+ * (sm_103a).
+ *
+ * One verify/commit cycle of a hybrid Qwen-style model, per GDN layer:
+ *
+ *   gdn_conv_verify   conv-ring read + width-4 causal depthwise conv + SiLU +
+ *                     L2 norm of q/k + gated delta rule over the T
+ *                     draft-plus-verify positions of every row, from the
+ *                     pre-verification state, which it never writes.
+ *   gdn_commit        once per cycle for all layers: keep the accepted prefix
+ *                     keep[b] of every row; keep=0 and inactive rows restore
+ *                     the pre-verification state exactly (nothing is
+ *                     written); advances the per-row committed offsets.
+ *   gdn_prefill_chunked  the same recurrence over a prompt of L tokens in
+ *                     chunked (WY/UT) form, leaving state, conv ring and
+ *                     offsets primed for the first verify.
+ *
+ * Passages this follows (page title, section):
+ *  - "MTP inference: review and commit structure", Functional commits, item 2:
+ *    GDN speculative transactions with verifier buffers, accepted-prefix state
+ *    replay, grouped copies across layers and a compiled short convolution;
+ *    item 4: the conv-cache mutation sits behind an operator boundary; Review
+ *    fixes: grouped replay checks every input before combining layers.
+ *  - "Add request-owned eight-way MTP serving for Qwen 35B", section 2 (per-row
+ *    committed offsets; inactive rows use keep=0 and keep their state) and
+ *    section 4 (the commit handles keep = 0, 1, 2; keep=0 restores the
+ *    pre-verification state; padded and finished rows are inert).
+ *  - "perf(qwen): full-context MTP draft prefill and replay-free rewind",
+ *    Summary item 4: the rewind reruns only the GDN mixer on captured
+ *    verification inputs from the pre-verification state.
+ *  - The recurrence is the gated delta rule (Yang, Kautz & Hatamizadeh, "Gated
+ *    Delta Networks", ICLR 2025): S_t = a_t S_{t-1} (I - b_t k_t k_t^T) +
+ *    b_t v_t k_t^T, a_t = exp(g_t), o_t = S_t q_t with q_t, k_t L2-normalised
+ *    and q_t scaled by 1/sqrt(d_k).
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument except `dims` and the host arrays of gdn_commit is
+ *    a DEVICE pointer on the current CUDA device, owned by the caller, 16-byte
+ *    aligned, to densely packed row-major storage in the layout stated.
+ *    The library never allocates device memory and never frees caller memory.
+ *  - bf16 tensors are passed as gdn_bf16 (the raw 16-bit pattern).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    only enqueues work; none synchronises the host except gdn_get_status.
+ *  - Arguments are validated on the host before anything is launched; on error
+ *    nothing is launched, the call returns a negative GDN_ERR_* code and
+ *    gdn_last_error() describes it.  Launch failures return GDN_ERR_CUDA.
+ *  - All verify/commit calls of one layer must be issued in stream order.
+ *
+ * Layouts (C = 2*H_k*d_k + H_v*d_v conv channels; R = width - 1 + T_max)
+ *  x        [B][T][C]           bf16  raw pre-conv inputs, channels q | k | v:
+ *                                     q [H_k][d_k], k [H_k][d_k], v [H_v][d_v]
+ *  conv_w   [C][width]          bf16  taps; conv_w[c][width-1] multiplies the
+ *                                     current token, conv_w[c][0] the oldest
+ *  g, beta  [B][T][H_v]         fp32  log-decay (a = exp(g), g <= 0 expected)
+ *                                     and write strength
+ *  state    [B][H_v][d_v][d_k]  fp32  S with v ~ S k: row j (d_v) holds a
+ *                                     contiguous d_k vector
+ *  ring     [B][R][C]           bf16  raw inputs of absolute position p in slot
+ *                                     p mod R; the committed conv window of row
+ *                                     b is positions offsets[b]-3 .. offsets[b]-1
+ *  offsets  [B]                 int32 committed tokens per row (one array shared
+ *                                     by all layers)
+ *  active   [B]                 uint8 0 = inactive/padding/finished row
+ *  out      [B][T][H_v][d_v]    bf16  o_t for each position
+ *
+ * Value head h reads key head floor(h * H_k / H_v).
+ * Supported: d_k == d_v in {32, 64, 128}; width == 4; 1 <= T <= T_max <= 8;
+ * H_v % H_k == 0; B <= 65535; H_v <= 65535.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
+
+/* return codes */
+#define GDN_OK 0
+#define GDN_ERR_INVALID_ARG (-1)   /* null pointer, bad enum, inconsistent sizes */
+#define GDN_ERR_UNSUPPORTED (-2)   /* a shape outside the supported set above */
+#define GDN_ERR_MISALIGNED (-3)    /* a device pointer not 16-byte aligned */
+#define GDN_ERR_WORKSPACE (-4)     /* workspace smaller than the size query */
+#define GDN_ERR_CUDA (-5)          /* a CUDA runtime call or launch failed */
+
+/* conv activation */
+#define GDN_ACT_NONE 0
+#define GDN_ACT_SILU 1
+
+/* commit strategies (chosen per call pair; verify and commit must agree) */
+#define GDN_COMMIT_RECOMPUTE 0 /* verify captures k, the per-row delta
+                                  coefficients and the cumulative decay; commit
+                                  rebuilds S_keep from the untouched S_0 */
+#define GDN_COMMIT_SNAPSHOT 1  /* verify writes S_1..S_T to the workspace;
+                                  commit copies S_keep back */
+
+/* sticky device status bits (gdn_get_status) */
+#define GDN_STATUS_BAD_KEEP 1u /* an active row passed keep outside [0, T];
+                                  that row was committed with keep = 0 */
+
+#define GDN_MAX_LAYERS 256     /* layers one gdn_commit call may group */
+
+typedef struct gdn_dims {
+  int32_t B;      /* rows in the cohort */
+  int32_t T;      /* positions per verify, 1..T_max */
+  int32_t T_max;  /* ring capacity parameter (R = width - 1 + T_max), <= 8 */
+  int32_t H_k;    /* key heads */
+  int32_t H_v;    /* value heads, a multiple of H_k */
+  int32_t d_k;    /* key head size */
+  int32_t d_v;    /* value head size (== d_k) */
+  int32_t width;  /* conv width, must be 4 */
+  int32_t act;    /* GDN_ACT_SILU or GDN_ACT_NONE */
+} gdn_dims;
+
+/* Library version string (static storage). */
+const char *gdn_version(void);
+
+/* Message for the last error returned on the calling host thread ("" if none;
+ * thread-local storage, valid until the next call on that thread). */
+const char *gdn_last_error(void);
+
+/*
+ * Bytes of per-layer workspace that gdn_conv_verify fills and gdn_commit reads
+ * for `mode`; 0 if dims or mode are invalid.  RECOMPUTE needs
+ * 4*B*T*(H_v*d_v + H_k*d_k + H_v) bytes (+ alignment padding); SNAPSHOT needs
+ * 4*T*B*H_v*d_v*d_k bytes.
+ */
+size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int mode);
+
+/*
+ * Verify one layer: for every active row b run the T positions from the
+ * committed window and the pre-verification state, writing o_t to `out`.
+ *  - reads  x, conv_w, g, beta, state, ring (window slots), offsets, active;
+ *  - writes out; the ring slots of positions offsets[b] .. offsets[b]+T-1 of
+ *    active rows (never the committed window); layer_ws (the captured
+ *    verification quantities the matching gdn_commit needs).
+ *  - never writes `state`; inactive rows get out = 0 and no ring or state
+ *    access.
+ * layer_ws must stay untouched until the matching gdn_commit has run.
+ * Errors: GDN_ERR_INVALID_ARG, _UNSUPPORTED, _MISALIGNED, _WORKSPACE
+ * (layer_ws_bytes < gdn_layer_workspace_bytes), _CUDA.
+ */
+int gdn_conv_verify(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w,
+                    const float *g, const float *beta, const float *state, gdn_bf16 *ring,
+                    const int32_t *offsets, const uint8_t *active, gdn_bf16 *out,
+                    void *layer_ws, size_t layer_ws_bytes, void *stream);
+
+/*
+ * Commit the accepted prefix of every row for n_layers layers in one launch
+ * (grouped across layers).  keep'[b] = keep[b] if active[b] and
+ * 0 <= keep[b] <= T, else 0 (an active row with keep outside [0, T] also sets
+ * GDN_STATUS_BAD_KEEP).  For keep' >= 1 the layer's state rows of b become the
+ * state after the first keep' positions; for keep' = 0 nothing of row b is
+ * written (exact restore).  offsets[b] += keep' (once, not per layer).  The
+ * ring is not touched: advancing the offset is what moves the committed
+ * window over the positions verify already wrote.
+ *  state    host array [n_layers] of device pointers to each layer's state
+ *  layer_ws host array [n_layers] of device pointers to each layer's workspace
+ *           (as filled by that layer's gdn_conv_verify with the same dims/mode)
+ *  keep, active, offsets  device arrays [B]; keep/active are read on the
+ *           device, so the call can be captured in a CUDA graph.
+ * Errors: GDN_ERR_INVALID_ARG (n_layers outside 1..GDN_MAX_LAYERS, null
+ * entries), _UNSUPPORTED, _MISALIGNED, _CUDA.
+ */
+int gdn_commit(const gdn_dims *dims, int mode, int n_layers, float *const *state,
+               void *const *layer_ws, const int32_t *keep, const uint8_t *active,
+               int32_t *offsets, void *stream);
+
+/*
+ * Bytes of workspace gdn_prefill_chunked needs for a prompt of L tokens;
+ * 0 if the arguments are invalid.
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L);
+
+/*
+ * Prime every row over a prompt of L tokens in chunked form (chunk = 64):
+ * conv from the committed window, L2 norm, then per chunk the UT transform of
+ * the decay-weighted strictly-lower K K^T block on tensor cores and a
+ * sequential pass of the state across chunks.  Equivalent, up to rounding, to
+ * gdn_conv_verify with T = L followed by gdn_commit with keep = L for all rows.
+ *  x [B][L][C] bf16; g, beta [B][L][H_v] fp32; state [B][H_v][d_v][d_k] fp32
+ *  in (initial) / out (final); ring and offsets updated as a commit of L
+ *  tokens would (offsets[b] += L); out [B][L][H_v][d_v] bf16.
+ * dims->T and T_max describe the ring the state is primed for (R = 3 + T_max).
+ * Errors: as gdn_conv_verify; GDN_ERR_WORKSPACE if ws_bytes is too small.
+ */
+int gdn_prefill_chunked(const gdn_dims *dims, int L, const gdn_bf16 *x, const gdn_bf16 *conv_w,
+                        const float *g, const float *beta, float *state, gdn_bf16 *ring,
+                        int32_t *offsets, gdn_bf16 *out, void *ws, size_t ws_bytes,
+                        void *stream);
+
+/*
+ * Read the sticky device status word of the current device (GDN_STATUS_*
+ * bits) into *status; clear it if `clear` is nonzero.  Synchronises the
+ * device.  Returns GDN_OK or GDN_ERR_CUDA / GDN_ERR_INVALID_ARG.
+ */
+int gdn_get_status(int clear, uint32_t *status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

@@ -1,0 +1,219 @@
+// api.cu -- the extern "C" boundary of libgdn_gb300.so: host-side validation,
+// workspace sizing, dispatch to the kernels, and error reporting.
+//
+// Every check runs before anything is launched, so a rejected call leaves all
+// device memory untouched ("Add request-owned eight-way MTP serving for Qwen
+// 35B", Clean-install public launch verification: an incomplete launch
+// contract fails before any work; "MTP inference: review and commit
+// structure", Review fixes: grouped replay checks all inputs before combining
+// layers).
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "gdn_common.cuh"
+
+using namespace gdn;
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+int ok() {
+  t_err.clear();
+  return GDN_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_dims(const gdn_dims *d) {
+  if (!d) return fail(GDN_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 0 || d->B > 65535) return fail(GDN_ERR_UNSUPPORTED, "B=%d outside [0, 65535]", d->B);
+  if (d->T < 1 || d->T > d->T_max || d->T_max > kMaxT)
+    return fail(GDN_ERR_UNSUPPORTED, "need 1 <= T (%d) <= T_max (%d) <= %d", d->T, d->T_max, kMaxT);
+  if (d->H_k < 1 || d->H_v < 1 || d->H_v % d->H_k != 0 || d->H_v > 65535)
+    return fail(GDN_ERR_UNSUPPORTED, "need H_k >= 1 and H_v (%d) a multiple of H_k (%d), H_v <= 65535",
+                d->H_v, d->H_k);
+  if (d->d_k != d->d_v || (d->d_k != 32 && d->d_k != 64 && d->d_k != 128))
+    return fail(GDN_ERR_UNSUPPORTED, "need d_k == d_v in {32, 64, 128} (got %d, %d)", d->d_k, d->d_v);
+  if (d->width != kWidth) return fail(GDN_ERR_UNSUPPORTED, "conv width must be 4 (got %d)", d->width);
+  if (d->act != GDN_ACT_NONE && d->act != GDN_ACT_SILU)
+    return fail(GDN_ERR_INVALID_ARG, "act must be GDN_ACT_NONE or GDN_ACT_SILU (got %d)", d->act);
+  const long long C = (2LL * d->H_k + d->H_v) * d->d_k;
+  if (C > (1LL << 30)) return fail(GDN_ERR_UNSUPPORTED, "too many conv channels (%lld)", C);
+  return GDN_OK;
+}
+
+int check_mode(int mode) {
+  if (mode != GDN_COMMIT_RECOMPUTE && mode != GDN_COMMIT_SNAPSHOT)
+    return fail(GDN_ERR_INVALID_ARG, "mode must be GDN_COMMIT_RECOMPUTE or GDN_COMMIT_SNAPSHOT (got %d)", mode);
+  return GDN_OK;
+}
+
+size_t layer_ws_bytes(const gdn_dims *d, int mode) {
+  if (mode == GDN_COMMIT_RECOMPUTE) return recompute_ws(d->B, d->T, d->H_k, d->H_v, d->d_k).total;
+  return snapshot_ws(d->B, d->T, d->H_v, d->d_k);
+}
+
+#define GDN_NEED_PTR(ptr, align)                                                             \
+  do {                                                                                       \
+    if (!(ptr)) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", #ptr);                        \
+    if (!aligned((ptr), (align)))                                                            \
+      return fail(GDN_ERR_MISALIGNED, "%s is not %d-byte aligned", #ptr, int(align));        \
+  } while (0)
+
+int cuda_fail(cudaError_t e, const char *what) {
+  return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+__attribute__((visibility("default"))) const char *gdn_version(void) {
+  return "gdn_gb300 1.0 (sm_103a)";
+}
+
+__attribute__((visibility("default"))) const char *gdn_last_error(void) { return t_err.c_str(); }
+
+__attribute__((visibility("default"))) size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int mode) {
+  if (check_dims(dims) != GDN_OK || check_mode(mode) != GDN_OK) return 0;
+  return layer_ws_bytes(dims, mode);
+}
+
+__attribute__((visibility("default"))) int gdn_conv_verify(
+    const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
+    const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
+    const uint8_t *active, gdn_bf16 *out, void *layer_ws, size_t layer_ws_bytes_given, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_mode(mode))) return rc;
+  if (dims->B == 0) return ok();
+  GDN_NEED_PTR(x, 16);
+  GDN_NEED_PTR(conv_w, 16);
+  GDN_NEED_PTR(g, 16);
+  GDN_NEED_PTR(beta, 16);
+  GDN_NEED_PTR(state, 16);
+  GDN_NEED_PTR(ring, 16);
+  GDN_NEED_PTR(offsets, 4);
+  GDN_NEED_PTR(active, 1);
+  GDN_NEED_PTR(out, 16);
+  GDN_NEED_PTR(layer_ws, 256);
+  const size_t need = layer_ws_bytes(dims, mode);
+  if (layer_ws_bytes_given < need)
+    return fail(GDN_ERR_WORKSPACE, "layer workspace has %zu bytes, needs %zu", layer_ws_bytes_given, need);
+
+  VerifyParams p{};
+  p.x = x;
+  p.w = conv_w;
+  p.g = g;
+  p.beta = beta;
+  p.state = state;
+  p.ring = ring;
+  p.offsets = offsets;
+  p.active = active;
+  p.out = out;
+  p.B = dims->B;
+  p.H_k = dims->H_k;
+  p.H_v = dims->H_v;
+  p.C = (2 * dims->H_k + dims->H_v) * dims->d_k;
+  p.R = kHist + dims->T_max;
+  p.act = dims->act;
+  char *ws = static_cast<char *>(layer_ws);
+  if (mode == GDN_COMMIT_RECOMPUTE) {
+    const RecomputeWs w = recompute_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);
+    p.ws_e = reinterpret_cast<float *>(ws + w.e);
+    p.ws_k = reinterpret_cast<float *>(ws + w.k);
+    p.ws_G = reinterpret_cast<float *>(ws + w.G);
+  } else {
+    p.ws_snap = reinterpret_cast<float *>(ws);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (dims->d_k) {
+    case 32: e = launch_verify_32(p, dims->T, mode, s); break;
+    case 64: e = launch_verify_64(p, dims->T, mode, s); break;
+    default: e = launch_verify_128(p, dims->T, mode, s); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_conv_verify launch");
+  return ok();
+}
+
+__attribute__((visibility("default"))) int gdn_commit(const gdn_dims *dims, int mode, int n_layers,
+                                                      float *const *state, void *const *layer_ws,
+                                                      const int32_t *keep, const uint8_t *active,
+                                                      int32_t *offsets, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_mode(mode))) return rc;
+  if (n_layers < 1 || n_layers > kMaxLayers)
+    return fail(GDN_ERR_INVALID_ARG, "n_layers=%d outside [1, %d]", n_layers, kMaxLayers);
+  if (!state || !layer_ws) return fail(GDN_ERR_INVALID_ARG, "state / layer_ws host arrays are NULL");
+  if (dims->B == 0) return ok();
+  GDN_NEED_PTR(keep, 4);
+  GDN_NEED_PTR(active, 1);
+  GDN_NEED_PTR(offsets, 4);
+  CommitParams p{};
+  for (int l = 0; l < n_layers; ++l) {
+    if (!state[l] || !layer_ws[l]) return fail(GDN_ERR_INVALID_ARG, "layer %d: NULL state or workspace", l);
+    if (!aligned(state[l], 16)) return fail(GDN_ERR_MISALIGNED, "layer %d: state not 16-byte aligned", l);
+    if (!aligned(layer_ws[l], 256))
+      return fail(GDN_ERR_MISALIGNED, "layer %d: workspace not 256-byte aligned", l);
+    p.state[l] = state[l];
+    p.ws[l] = static_cast<const float *>(layer_ws[l]);
+  }
+  p.keep = keep;
+  p.active = active;
+  p.offsets = offsets;
+  p.n_layers = n_layers;
+  p.B = dims->B;
+  p.T = dims->T;
+  p.H_k = dims->H_k;
+  p.H_v = dims->H_v;
+  cudaError_t e = launch_commit(p, dims->d_k, mode, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_commit launch");
+  return ok();
+}
+
+__attribute__((visibility("default"))) size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L) {
+  (void)dims;
+  (void)L;
+  return 0;
+}
+
+__attribute__((visibility("default"))) int gdn_prefill_chunked(
+    const gdn_dims *dims, int L, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
+    const float *beta, float *state, gdn_bf16 *ring, int32_t *offsets, gdn_bf16 *out, void *ws,
+    size_t ws_bytes, void *stream) {
+  (void)dims, (void)L, (void)x, (void)conv_w, (void)g, (void)beta, (void)state, (void)ring;
+  (void)offsets, (void)out, (void)ws, (void)ws_bytes, (void)stream;
+  return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked is not available in this build");
+}
+
+__attribute__((visibility("default"))) int gdn_get_status(int clear, uint32_t *status) {
+  if (!status) return fail(GDN_ERR_INVALID_ARG, "status is NULL");
+  uint32_t *dev = status_word_address();
+  if (!dev) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_get_status synchronize");
+  e = cudaMemcpy(status, dev, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_get_status read");
+  if (clear) {
+    e = cudaMemset(dev, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_get_status clear");
+  }
+  return ok();
+}
+
+}  // extern "C"

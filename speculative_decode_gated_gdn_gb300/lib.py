@@ -1,0 +1,196 @@
+"""Python binding of libgdn_gb300.so (ctypes; argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: it turns torch tensors into device pointers and the
+current torch stream into a cudaStream_t, calls the library, and raises
+GdnError on a nonzero return code.  There is no CPU fallback: if the library
+cannot be built or loaded, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = -1
+GDN_ERR_UNSUPPORTED = -2
+GDN_ERR_MISALIGNED = -3
+GDN_ERR_WORKSPACE = -4
+GDN_ERR_CUDA = -5
+GDN_ACT_NONE = 0
+GDN_ACT_SILU = 1
+GDN_COMMIT_RECOMPUTE = 0
+GDN_COMMIT_SNAPSHOT = 1
+GDN_STATUS_BAD_KEEP = 1
+GDN_MAX_LAYERS = 256
+
+EXPORTS = ("gdn_version", "gdn_last_error", "gdn_layer_workspace_bytes", "gdn_conv_verify",
+           "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, fn: str, msg: str):
+        super().__init__(f"{fn} returned {code}: {msg}")
+        self.code = code
+
+
+class gdn_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "T", "T_max", "H_k", "H_v", "d_k", "d_v", "width", "act")]
+
+
+def dims(B, T, H_k, H_v, d, T_max=None, width=4, act=GDN_ACT_SILU) -> gdn_dims:
+    return gdn_dims(B, T, T if T_max is None else T_max, H_k, H_v, d, d, width, act)
+
+
+def dims_of(geom) -> gdn_dims:
+    """gdn_dims from a synth.Geometry."""
+    return dims(geom.B, geom.T, geom.H_k, geom.H_v, geom.d, geom.tmax, geom.width, geom.act)
+
+
+_P = ctypes.c_void_p
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib):
+    D = ctypes.POINTER(gdn_dims)
+    lib.gdn_version.restype = ctypes.c_char_p
+    lib.gdn_version.argtypes = []
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_last_error.argtypes = []
+    lib.gdn_layer_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_layer_workspace_bytes.argtypes = [D, ctypes.c_int]
+    lib.gdn_conv_verify.restype = ctypes.c_int
+    lib.gdn_conv_verify.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
+    lib.gdn_commit.restype = ctypes.c_int
+    lib.gdn_commit.argtypes = [D, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P), ctypes.POINTER(_P),
+                               _P, _P, _P, _P]
+    lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_prefill_workspace_bytes.argtypes = [D, ctypes.c_int]
+    lib.gdn_prefill_chunked.restype = ctypes.c_int
+    lib.gdn_prefill_chunked.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
+    lib.gdn_get_status.restype = ctypes.c_int
+    lib.gdn_get_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load (building first if missing or stale) and return the ctypes library."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or _build.build()
+            if not os.path.exists(p):
+                raise RuntimeError(f"libgdn_gb300.so not found at {p}")
+            lib = ctypes.CDLL(p)
+            _declare(lib)
+            if path is not None:
+                return lib
+            _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------------ marshalling
+def _ptr(t, what, dtype=None):
+    """Device pointer of a tensor (or a raw int pointer / None)."""
+    if t is None or isinstance(t, int):
+        return t
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: expected a torch.Tensor or an int pointer")
+    if not t.is_cuda:
+        raise ValueError(f"{what}: tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: tensor must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc, fn):
+    if rc != GDN_OK:
+        raise GdnError(rc, fn, load().gdn_last_error().decode())
+
+
+def _t():
+    import torch
+    return torch
+
+
+def gdn_version() -> str:
+    return load().gdn_version().decode()
+
+
+def gdn_last_error() -> str:
+    return load().gdn_last_error().decode()
+
+
+def gdn_layer_workspace_bytes(d: gdn_dims, mode: int) -> int:
+    return int(load().gdn_layer_workspace_bytes(ctypes.byref(d), mode))
+
+
+def gdn_conv_verify(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets, active, out,
+                    layer_ws, layer_ws_bytes=None, stream=None):
+    torch = _t()
+    if layer_ws_bytes is None:
+        layer_ws_bytes = layer_ws.numel() * layer_ws.element_size()
+    rc = load().gdn_conv_verify(
+        ctypes.byref(d), mode, _ptr(x, "x", torch.bfloat16), _ptr(conv_w, "conv_w", torch.bfloat16),
+        _ptr(g, "g", torch.float32), _ptr(beta, "beta", torch.float32), _ptr(state, "state", torch.float32),
+        _ptr(ring, "ring", torch.bfloat16), _ptr(offsets, "offsets", torch.int32),
+        _ptr(active, "active", torch.uint8), _ptr(out, "out", torch.bfloat16), _ptr(layer_ws, "layer_ws"),
+        int(layer_ws_bytes), _stream(stream))
+    _check(rc, "gdn_conv_verify")
+
+
+def gdn_commit(d: gdn_dims, mode, states, layer_ws, keep, active, offsets, stream=None):
+    """states / layer_ws: sequences (one per layer) of tensors or int device pointers."""
+    torch = _t()
+    n = len(states)
+    if len(layer_ws) != n:
+        raise ValueError("states and layer_ws must have one entry per layer")
+    sp = (_P * max(n, 1))(*[_ptr(s, f"state[{i}]", torch.float32) for i, s in enumerate(states)])
+    wp = (_P * max(n, 1))(*[_ptr(w, f"layer_ws[{i}]") for i, w in enumerate(layer_ws)])
+    rc = load().gdn_commit(ctypes.byref(d), mode, n, sp, wp, _ptr(keep, "keep", torch.int32),
+                           _ptr(active, "active", torch.uint8), _ptr(offsets, "offsets", torch.int32),
+                           _stream(stream))
+    _check(rc, "gdn_commit")
+
+
+def gdn_prefill_workspace_bytes(d: gdn_dims, L: int) -> int:
+    return int(load().gdn_prefill_workspace_bytes(ctypes.byref(d), L))
+
+
+def gdn_prefill_chunked(d: gdn_dims, L, x, conv_w, g, beta, state, ring, offsets, out, ws,
+                        ws_bytes=None, stream=None):
+    torch = _t()
+    if ws_bytes is None:
+        ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().gdn_prefill_chunked(
+        ctypes.byref(d), L, _ptr(x, "x", torch.bfloat16), _ptr(conv_w, "conv_w", torch.bfloat16),
+        _ptr(g, "g", torch.float32), _ptr(beta, "beta", torch.float32), _ptr(state, "state", torch.float32),
+        _ptr(ring, "ring", torch.bfloat16), _ptr(offsets, "offsets", torch.int32),
+        _ptr(out, "out", torch.bfloat16), _ptr(ws, "ws"), int(ws_bytes), _stream(stream))
+    _check(rc, "gdn_prefill_chunked")
+
+
+def gdn_get_status(clear: bool = False) -> int:
+    v = ctypes.c_uint32(0)
+    rc = load().gdn_get_status(1 if clear else 0, ctypes.byref(v))
+    _check(rc, "gdn_get_status")
+    return int(v.value)

@@ -185,3 +185,12 @@ def prompt_inputs(geom: Geometry, seed: int, L: int) -> dict:
     bz = normal(seed, "pbeta", (g.B, L, g.H_v))
     beta = (1.0 / (1.0 + np.exp(-bz))).astype(np.float32)
     return {"x": x, "g": gl, "beta": beta}
+
+
+def keep_draws(geom: Geometry, seed: int, n_cycles: int) -> np.ndarray:
+    """keep[] for n consecutive cycles, int32 [n_cycles][B], uniform in {0..T}.
+
+    Long runs draw x/g/beta from a pool of cycle_inputs() (pool index = cycle
+    mod pool size) but re-draw keep every cycle from this stream.
+    """
+    return integers(seed, "keeps", (n_cycles, geom.B), 0, geom.T + 1)

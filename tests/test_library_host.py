@@ -1,0 +1,110 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decode_gated_gdn_gb300 import lib as L
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(gdn_\w+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return L.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"gdn_conv_verify", "gdn_commit", "gdn_prefill_chunked"} <= names
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert set(L.EXPORTS) <= names
+
+
+def test_only_gdn_symbols_exported():
+    out = os.popen(f"nm -D --defined-only {L.library_path()}").read()
+    syms = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert syms and all(s.startswith("gdn_") for s in syms), sorted(syms)[:20]
+
+
+def test_version(lib):
+    assert "sm_103a" in L.gdn_version()
+
+
+def test_workspace_sizes(lib):
+    d = L.dims(8, 2, 16, 32, 128)
+    rec = L.gdn_layer_workspace_bytes(d, L.GDN_COMMIT_RECOMPUTE)
+    snap = L.gdn_layer_workspace_bytes(d, L.GDN_COMMIT_SNAPSHOT)
+    assert rec >= 4 * 8 * 2 * (32 * 128 + 16 * 128 + 32)
+    assert snap == 4 * 2 * 8 * 32 * 128 * 128
+    assert L.gdn_layer_workspace_bytes(d, 7) == 0
+    assert L.gdn_layer_workspace_bytes(L.dims(8, 2, 16, 32, 96), 0) == 0
+
+
+BAD_DIMS = [
+    (dict(B=8, T=0, H_k=16, H_v=32, d=128), L.GDN_ERR_UNSUPPORTED),
+    (dict(B=8, T=3, H_k=16, H_v=32, d=128, T_max=2), L.GDN_ERR_UNSUPPORTED),
+    (dict(B=8, T=9, H_k=16, H_v=32, d=128), L.GDN_ERR_UNSUPPORTED),
+    (dict(B=8, T=2, H_k=3, H_v=32, d=128), L.GDN_ERR_UNSUPPORTED),
+    (dict(B=8, T=2, H_k=16, H_v=32, d=96), L.GDN_ERR_UNSUPPORTED),
+    (dict(B=8, T=2, H_k=16, H_v=32, d=128, width=3), L.GDN_ERR_UNSUPPORTED),
+    (dict(B=8, T=2, H_k=16, H_v=32, d=128, act=5), L.GDN_ERR_INVALID_ARG),
+    (dict(B=-1, T=2, H_k=16, H_v=32, d=128), L.GDN_ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("kw,code", BAD_DIMS)
+def test_bad_dims_rejected_before_launch(lib, kw, code):
+    d = L.dims(**kw)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    rc = lib.gdn_conv_verify(ctypes.byref(d), 0, *([fake] * 10), 1 << 30, None)
+    assert rc == code, L.gdn_last_error()
+    assert L.gdn_last_error()
+
+
+def test_null_and_misaligned_pointers(lib):
+    d = L.dims(8, 2, 16, 32, 128)
+    good = 1 << 20
+    ptrs = [good] * 10
+    ptrs[0] = None
+    assert lib.gdn_conv_verify(ctypes.byref(d), 0, *ptrs, 1 << 30, None) == L.GDN_ERR_INVALID_ARG
+    assert "x is NULL" in L.gdn_last_error()
+    ptrs[0] = good + 2
+    assert lib.gdn_conv_verify(ctypes.byref(d), 0, *ptrs, 1 << 30, None) == L.GDN_ERR_MISALIGNED
+    ptrs[0] = good
+    assert lib.gdn_conv_verify(ctypes.byref(d), 0, *ptrs, 16, None) == L.GDN_ERR_WORKSPACE
+    assert lib.gdn_conv_verify(ctypes.byref(d), 3, *ptrs, 1 << 30, None) == L.GDN_ERR_INVALID_ARG
+
+
+def test_commit_argument_checks(lib):
+    d = L.dims(8, 2, 16, 32, 128)
+    P = ctypes.c_void_p
+    arr = (P * 1)(1 << 20)
+    assert lib.gdn_commit(ctypes.byref(d), 0, 0, arr, arr, 1 << 20, 1 << 20, 1 << 20, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_commit(ctypes.byref(d), 0, L.GDN_MAX_LAYERS + 1, arr, arr, 1 << 20, 1 << 20, 1 << 20,
+                          None) == L.GDN_ERR_INVALID_ARG
+    bad = (P * 1)(None)
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, bad, arr, 1 << 20, 1 << 20, 1 << 20, None) == L.GDN_ERR_INVALID_ARG
+    mis = (P * 1)((1 << 20) + 8)
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, mis, arr, 1 << 20, 1 << 20, 1 << 20, None) == L.GDN_ERR_MISALIGNED
+
+
+def test_empty_batch_is_a_no_op(lib):
+    d = L.dims(0, 2, 16, 32, 128)
+    assert lib.gdn_conv_verify(ctypes.byref(d), 0, *([None] * 10), 0, None) == L.GDN_OK
+    P = ctypes.c_void_p
+    arr = (P * 1)(1 << 20)
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, arr, None, None, None, None) == L.GDN_OK
