@@ -123,7 +123,7 @@ def dist_env():
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -131,6 +131,13 @@ class ClockSampler:
         self.device_id = device_id
         self.proc = None
         self.lines: list[str] = []
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __enter__(self):
         exe = shutil.which("nvidia-smi")
@@ -163,23 +170,27 @@ class ClockSampler:
             return None
         sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if self.t0 is not None and not (self.t0 - 0.02 <= ts <= self.t1 + 0.02):
+                    continue
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
             except ValueError:
                 continue
-            for name, flag in zip(names, parts[5:9]):
+            for name, flag in zip(names, parts[6:10]):
                 if flag.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power)}
+                "samples": len(sm), "power_w_max": max(power), "window": "timed region only"}
 
 
 def measured_peak():
@@ -267,6 +278,19 @@ def run_oracle_sample(geom, inactive, n_layers, seconds, max_layer_cycles=None, 
 
 
 # ---------------------------------------------------------------- GPU arm
+def timing_event():
+    """A timing event that records as a graph node when captured."""
+    import torch
+    return torch.cuda.Event(enable_timing=True, external=True)
+
+
+def verify_mode(mode, layer):
+    """Layers after the first follow another layer's verify, which writes none of
+    their buffers, so they may stage state before that verify finishes."""
+    from speculative_decode_gated_gdn_gb300 import lib as L
+    return mode | (L.GDN_VERIFY_OVERLAP if layer > 0 else 0)
+
+
 def run_gpu(args, rank, world, local):
     import torch
     from speculative_decode_gated_gdn_gb300 import lib as L
@@ -307,8 +331,8 @@ def run_gpu(args, rank, world, local):
 
     def cycle(c, x, g, beta, keep, ev=None):
         for l in range(n_layers):
-            L.gdn_conv_verify(d, mode, x[l], conv_w[l], g[l], beta[l], state[l], ring[l], offsets, active,
-                              out[l], ws[l], ws_bytes)
+            L.gdn_conv_verify(d, verify_mode(mode, l), x[l], conv_w[l], g[l], beta[l], state[l], ring[l],
+                              offsets, active, out[l], ws[l], ws_bytes)
         if ev is not None:
             ev[0].record()
         L.gdn_commit(d, mode, states, ws, keep, active, offsets)
@@ -324,7 +348,7 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     for c in range(K + W):
         p = c % pool
-        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ev = (timing_event(), timing_event())
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=side):
             cycle(c, xs[p], gs[p], bs[p], keeps[c], ev)
@@ -349,11 +373,13 @@ def run_gpu(args, rank, world, local):
     dev_id = f"GPU-{uuid}" if uuid is not None else str(local)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev_id) as clk:
+        clk.mark_start()
         start.record()
         for c in range(W, W + K):
             graphs[c].replay()
         end.record()
         torch.cuda.synchronize()
+        clk.mark_end()
     if world > 1:
         dist.barrier()
     ms = start.elapsed_time(end)
@@ -439,8 +465,8 @@ def run_e2e(args, geom, d, mode, dev, inp, keeps_np, state, ring, conv_w, offset
         db.copy_(hb[p], non_blocking=True)
         dk.copy_(hk[c], non_blocking=True)
         for l in range(n_layers):
-            L.gdn_conv_verify(d, mode, dxb[l], conv_w[l], dg[l], db[l], state[l], ring[l], offsets, active,
-                              out[l], ws[l], ws_bytes)
+            L.gdn_conv_verify(d, verify_mode(mode, l), dxb[l], conv_w[l], dg[l], db[l], state[l], ring[l],
+                              offsets, active, out[l], ws[l], ws_bytes)
         L.gdn_commit(d, mode, states, ws, dk, active, offsets)
         hout.copy_(out, non_blocking=True)
         hoff.copy_(offsets, non_blocking=True)

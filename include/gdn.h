@@ -100,9 +100,23 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
 #define GDN_COMMIT_SNAPSHOT 1  /* verify writes S_1..S_T to the workspace;
                                   commit copies S_keep back */
 
+/* flag OR-ed into the mode argument of gdn_conv_verify.  Every kernel of
+ * the library is launched with programmatic dependent launch and waits for
+ * the preceding kernel on the stream before reading anything it may write.
+ * With GDN_VERIFY_OVERLAP the caller also guarantees that the work issued
+ * immediately before this call on the stream writes none of this call's
+ * `state`, `ring`, `active` and `conv_w`; the kernel then stages its state
+ * tiles while that work is still finishing.  Do not pass it to the first
+ * verify after gdn_commit, gdn_prefill_chunked or any other write of these
+ * buffers; it is always safe to omit. */
+#define GDN_VERIFY_OVERLAP 0x100
+
 /* sticky device status bits (gdn_get_status) */
 #define GDN_STATUS_BAD_KEEP 1u /* an active row passed keep outside [0, T];
                                   that row was committed with keep = 0 */
+#define GDN_STATUS_TIMEOUT 2u  /* a kernel gave up waiting for one of its own
+                                  bulk copies (bounded wait); its outputs for
+                                  that tile were not written */
 
 #define GDN_MAX_LAYERS 256     /* layers one gdn_commit call may group */
 

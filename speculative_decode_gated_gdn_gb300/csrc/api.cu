@@ -97,6 +97,10 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
     const uint8_t *active, gdn_bf16 *out, void *layer_ws, size_t layer_ws_bytes_given, void *stream) {
   int rc = check_dims(dims);
   if (rc) return rc;
+  if (mode & ~(GDN_VERIFY_OVERLAP | 0xff))
+    return fail(GDN_ERR_INVALID_ARG, "unknown flag bits in mode 0x%x", mode);
+  const int overlap = (mode & GDN_VERIFY_OVERLAP) != 0;
+  mode &= 0xff;
   if ((rc = check_mode(mode))) return rc;
   if (dims->B == 0) return ok();
   GDN_NEED_PTR(x, 16);
@@ -129,6 +133,9 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
   p.C = (2 * dims->H_k + dims->H_v) * dims->d_k;
   p.R = kHist + dims->T_max;
   p.act = dims->act;
+  p.overlap = overlap;
+  p.status = status_word_address();
+  if (!p.status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
   char *ws = static_cast<char *>(layer_ws);
   if (mode == GDN_COMMIT_RECOMPUTE) {
     const RecomputeWs w = recompute_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);

@@ -17,9 +17,16 @@ namespace gdn {
 
 __device__ uint32_t g_status;  // sticky GDN_STATUS_* bits of this device
 
+// Device address of g_status on the current device, looked up once per device
+// (the launchers pass it to kernels in other translation units).
 uint32_t *status_word_address() {
+  static void *cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (dev >= 0 && dev < 64 && cached[dev]) return static_cast<uint32_t *>(cached[dev]);
   void *ptr = nullptr;
   if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+  if (dev >= 0 && dev < 64) cached[dev] = ptr;
   return static_cast<uint32_t *>(ptr);
 }
 
@@ -36,6 +43,8 @@ __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
   constexpr int TILES = D / kTileRows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane % LPR, grp = lane / LPR;
+  pdl_wait();  // every state, workspace and offsets access follows the preceding kernel
+  pdl_trigger();
 
   if (blockIdx.x == 0) {
     for (int b = tid; b < p.B; b += blockDim.x) {
@@ -132,10 +141,8 @@ static cudaError_t launch_commit_d(const CommitParams &p, int mode, cudaStream_t
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
   if (mode == GDN_COMMIT_RECOMPUTE)
-    commit_kernel<D, GDN_COMMIT_RECOMPUTE><<<unsigned(grid), 128, 0, stream>>>(p);
-  else
-    commit_kernel<D, GDN_COMMIT_SNAPSHOT><<<unsigned(grid), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+    return launch_pdl(commit_kernel<D, GDN_COMMIT_RECOMPUTE>, dim3(unsigned(grid)), dim3(128), stream, p);
+  return launch_pdl(commit_kernel<D, GDN_COMMIT_SNAPSHOT>, dim3(unsigned(grid)), dim3(128), stream, p);
 }
 
 cudaError_t launch_commit(const CommitParams &p, int D, int mode, cudaStream_t stream) {

@@ -28,7 +28,9 @@ __device__ __forceinline__ int ring_slot(int pos, int R) {
   return s < 0 ? s + R : s;
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// SiLU with the fast exponential and division intrinsics (a few ulp; the
+// conv output feeds an fp32 recurrence whose tolerance is far looser).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Streaming 128-bit load that does not allocate in L1 (each state byte is
 // read once per call).
@@ -42,6 +44,81 @@ __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
 
 __device__ __forceinline__ void st_f4(float *p, float4 v) {
   *reinterpret_cast<float4 *>(p) = v;
+}
+
+// ---- shared-memory barrier + bulk-copy (TMA) helpers ------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make an initialised mbarrier visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Contiguous global -> shared copy on the bulk-copy engine; completion is
+// counted on `bar` in bytes.  dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` with an iteration limit (about a second in
+// total); false if the limit ran out.
+constexpr uint32_t kWaitLimit = 1u << 22;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= 32) __nanosleep(256);
+  }
+  return false;
+}
+
+// ---- programmatic dependent launch --------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialization.  It waits for the preceding kernel on the stream
+// (griddepcontrol.wait) before touching anything that kernel may write, and
+// only then lets the next kernel start (launch_dependents), so a kernel's
+// pre-wait section can overlap only its immediate predecessor.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename Kernel, typename Params>
+inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, cudaStream_t stream, const Params &p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
@@ -125,7 +202,9 @@ struct VerifyParams {
   float *ws_k;    // RECOMPUTE: [B][T][H_k][D]
   float *ws_G;    // RECOMPUTE: [B][T][H_v]
   float *ws_snap; // SNAPSHOT:  [T][B][H_v][D][D]
+  uint32_t *status; // sticky device status word
   int B, H_k, H_v, C, R, act;
+  int overlap;      // GDN_VERIFY_OVERLAP: stage the state tile before the PDL wait
 };
 
 constexpr int kMaxLayers = GDN_MAX_LAYERS;

@@ -1,8 +1,17 @@
 // verify.cuh -- the fused conv + L2-norm + gated-delta-rule verify kernel.
 //
-// One CTA of 128 threads owns 32 state rows (d_v) of one (row b, value head h)
-// and runs all T draft-plus-verify positions of that tile from the
-// pre-verification state S_0, which it only reads ("MTP inference: review and
+// Work decomposition.  A CTA of 4 warps owns 32 state rows (d_v) of one
+// (row b, value head h).  Its state tile (32 contiguous rows) is staged in
+// shared memory by one bulk copy on the TMA engine issued at entry.  The q/k
+// conv of the key head is split over the CTA's threads and exchanged through
+// shared memory at the kernel's one block barrier; after it every warp owns 8
+// rows and works alone.  Lane l works on the d_k segment [4*(l % LPR), +4) of
+// its rows.  Every global load (state tile, conv window, new inputs, taps,
+// gates) is issued before the barrier, so the critical path is one memory
+// round trip plus a few hundred instructions per warp, which is what a
+// one-wave kernel of a few microseconds needs.
+//
+// The pre-verification state S_0 is only read ("MTP inference: review and
 // commit structure", Functional commits item 2: speculative transactions with
 // verifier buffers; "Add request-owned eight-way MTP serving for Qwen 35B",
 // section 4: keep=0 must find the real base state).
@@ -14,13 +23,14 @@
 //            - sum_{s<t} b_t exp(G_t - G_s) (k_s.k_t) e_s[j]
 //   o_t[j] = gamma_t (S_0[j].q_t) + sum_{s<=t} exp(G_t - G_s) (k_s.q_t) e_s[j]
 // so a state row only needs its 2T dot products with S_0 (one batched warp
-// reduction) plus per-head scalars that every CTA computes once in shared
-// memory; the T sequential steps act on scalars, not on the 64 KiB state.
-// This is the chunked (WY) form of the rule with one chunk of T positions
-// (Yang et al., "Parallelizing Linear Transformers with the Delta Rule over
-// Sequence Length", 2024), which differs from the step-by-step form only in
-// rounding ("MTP inference: review and commit structure", Verification and
-// limits).
+// reduction) plus per-head scalars, and the T sequential steps act on
+// scalars, not on the 64 KiB state.  This is the chunked (WY) form of the rule
+// with one chunk of T positions (Yang et al., "Parallelizing Linear
+// Transformers with the Delta Rule over Sequence Length", 2024), equal to the
+// step-by-step form up to rounding ("MTP inference: review and commit
+// structure", Verification and limits).  The L2 norms are folded in as scale
+// factors: every dot product is taken on the raw conv outputs and multiplied
+// by 1/|k| (and 1/(|q| sqrt(d_k))) afterwards.
 //
 // Captures for the commit (the "captured verification inputs" of "perf(qwen):
 // full-context MTP draft prefill and replay-free rewind", Summary item 4):
@@ -35,204 +45,267 @@
 
 namespace gdn {
 
+// Causal conv of one channel over T new positions: window xt[0..2] (oldest
+// first) followed by the new inputs; taps w[0..3], w[3] on the current token.
+template <int T>
+__device__ __forceinline__ void conv1(const float (&w)[kWidth], const float (&xt)[kHist + T], int act,
+                                      float (&y)[T]) {
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    float acc = w[0] * xt[t];
+    acc = fmaf(w[1], xt[t + 1], acc);
+    acc = fmaf(w[2], xt[t + 2], acc);
+    acc = fmaf(w[3], xt[t + 3], acc);
+    y[t] = act ? silu_fast(acc) : acc;
+  }
+}
+
+// Load the taps, committed window and new inputs of channel c of row b and run
+// its conv; optionally copy the new raw inputs into the ring slots of their
+// positions.
+template <int T>
+__device__ __forceinline__ void conv_channel(const VerifyParams &p, int b, int c, int slot0, int wslot0,
+                                            bool write_ring, float (&y)[T]) {
+  const int C = p.C, R = p.R;
+  const uint2 wr = *reinterpret_cast<const uint2 *>(p.w + size_t(c) * kWidth);
+  const float w[kWidth] = {bf2f(uint16_t(wr.x & 0xffff)), bf2f(uint16_t(wr.x >> 16)),
+                           bf2f(uint16_t(wr.y & 0xffff)), bf2f(uint16_t(wr.y >> 16))};
+  const uint16_t *ringb = p.ring + size_t(b) * R * C + c;
+  const uint16_t *xb = p.x + size_t(b) * T * C + c;
+  float xt[kHist + T];
+  uint16_t xraw[T];
+  int slot = slot0;
+#pragma unroll
+  for (int i = 0; i < kHist; ++i) {
+    xt[i] = bf2f(ringb[size_t(slot) * C]);
+    slot = slot + 1 == R ? 0 : slot + 1;
+  }
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    xraw[t] = xb[size_t(t) * C];
+    xt[kHist + t] = bf2f(xraw[t]);
+  }
+  conv1<T>(w, xt, p.act, y);
+  if (write_ring) {
+    uint16_t *ringw = p.ring + size_t(b) * R * C + c;
+    int ws = wslot0;
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      ringw[size_t(ws) * C] = xraw[t];
+      ws = ws + 1 == R ? 0 : ws + 1;
+    }
+  }
+}
+
 template <int D, int T, int MODE>
-__global__ void __launch_bounds__(kVerifyThreads) verify_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kVerifyThreads, T <= 2 ? 6 : 1) verify_kernel(const VerifyParams p) {
   using G = RowLanes<D>;
   constexpr int RPL = G::RPL, GPW = G::GPW, LPR = G::LPR;
-  constexpr int NCH = 2 * D + kTileRows;  // q, k of the key head + this tile's v channels
+  // per-head reductions: |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t)
+  constexpr int NKK = T * (T - 1) / 2, NKQ = T * (T + 1) / 2, NV = 2 * T + NKK + NKQ;
 
+  __shared__ __align__(128) float sS[kTileRows * D];
   __shared__ __align__(16) float sq[T][D];
   __shared__ __align__(16) float sk[T][D];
-  __shared__ float sv[T][kTileRows];
-  __shared__ float s_inv[2 * T];
-  __shared__ float s_dot[2][T][T];  // [0][s][t] = k_s.k_t, [1][s][t] = k_s.q_t
-  __shared__ float sG[T], sBeta[T];
-  __shared__ float sM[T][T], sN[T][T], sBg[T], sGam[T], sAlpha[T];
+  __shared__ __align__(8) uint64_t sbar;
 
   const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane % LPR, grp = lane / LPR;
-  const int j0 = tile * kTileRows;
-  const int H_v = p.H_v, H_k = p.H_k, C = p.C, R = p.R;
+  const int H_v = p.H_v, H_k = p.H_k, R = p.R;
   const int rep = H_v / H_k;
   const int hk = h / rep;
+  const int jw = tile * kTileRows + warp * 8;  // first state row of this warp
+  const int istar = row_of_lane<D>(lane);      // row this lane holds after the reduction
+  const int jrow = jw + grp + GPW * istar;
+  const bool leader = (lane & 3) == 0;         // four lanes share a row after the reduction
 
+  // With GDN_VERIFY_OVERLAP the caller guarantees that the preceding work on
+  // the stream writes none of this call's state, ring, active mask or taps, so
+  // the state tile is staged before waiting for that work; otherwise
+  // everything waits first.
+  if (!p.overlap) {
+    pdl_wait();
+    pdl_trigger();
+  }
   if (!p.active[b]) {
     // Inactive / padding / finished rows are inert: zero output, no state,
     // ring or workspace access.
-    for (int i = tid; i < T * kTileRows; i += kVerifyThreads) {
-      const int t = i / kTileRows, jj = i % kTileRows;
-      p.out[((size_t(b) * T + t) * H_v + h) * D + j0 + jj] = 0;
+    if (p.overlap) {
+      pdl_wait();
+      pdl_trigger();
     }
+    if (leader)
+#pragma unroll
+      for (int t = 0; t < T; ++t) p.out[((size_t(b) * T + t) * H_v + h) * D + jrow] = 0;
     return;
   }
 
-  // 1. Issue the state loads first so the HBM reads overlap the conv prologue.
-  const float *Sw = p.state + ((size_t(b) * H_v + h) * D + j0 + warp * 8) * D;
+  // ---- 1. stage the state tile (bulk copy on the TMA engine) ----------------
+  constexpr uint32_t kTileBytes = kTileRows * D * sizeof(float);
+  if (tid == 0) {
+    mbar_init(&sbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&sbar, kTileBytes);
+    bulk_g2s(sS, p.state + ((size_t(b) * H_v + h) * D + size_t(tile) * kTileRows) * D, kTileBytes, &sbar);
+  }
+  if (p.overlap) {
+    pdl_wait();
+    pdl_trigger();
+  }
+
+  // ---- 2. conv + activation: q/k channels of the key head split over the CTA,
+  //         the v channel of each lane's row done by the lanes of that row ----
+  const int off = p.offsets[b];
+  const int slot0 = ring_slot(off - kHist, R);
+  const int wslot0 = ring_slot(off, R);
+  const bool qk_writer = (tile == 0) && (h % rep == 0);  // one CTA per key head writes its q/k ring slots
+  for (int c2 = tid; c2 < 2 * D; c2 += kVerifyThreads) {
+    const bool is_k = c2 >= D;
+    const int ch = is_k ? c2 - D : c2;
+    const int c = (is_k ? H_k * D : 0) + hk * D + ch;
+    float y[T];
+    conv_channel<T>(p, b, c, slot0, wslot0, qk_writer, y);
+#pragma unroll
+    for (int t = 0; t < T; ++t) (is_k ? sk : sq)[t][ch] = y[t];
+  }
+  float v[T];
+  conv_channel<T>(p, b, 2 * H_k * D + h * D + jrow, slot0, wslot0, leader, v);
+  float gt[T], bt[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
+    bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
+  }
+  __syncthreads();  // conv outputs and the initialised barrier are visible
+
+  float q[T][4], k[T][4];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const float4 qv = *reinterpret_cast<const float4 *>(&sq[t][4 * sub]);
+    const float4 kv = *reinterpret_cast<const float4 *>(&sk[t][4 * sub]);
+    q[t][0] = qv.x, q[t][1] = qv.y, q[t][2] = qv.z, q[t][3] = qv.w;
+    k[t][0] = kv.x, k[t][1] = kv.y, k[t][2] = kv.z, k[t][3] = kv.w;
+  }
+
+  // ---- 3. per-head sums over the LPR lanes of a row group ------------------
+  float red_h[NV];
+  {
+    int n = 0;
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      red_h[n++] = q[t][0] * q[t][0] + q[t][1] * q[t][1] + q[t][2] * q[t][2] + q[t][3] * q[t][3];
+      red_h[n++] = k[t][0] * k[t][0] + k[t][1] * k[t][1] + k[t][2] * k[t][2] + k[t][3] * k[t][3];
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+      for (int s0 = 0; s0 < t; ++s0)
+        red_h[n++] = k[s0][0] * k[t][0] + k[s0][1] * k[t][1] + k[s0][2] * k[t][2] + k[s0][3] * k[t][3];
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+      for (int s0 = 0; s0 <= t; ++s0)
+        red_h[n++] = k[s0][0] * q[t][0] + k[s0][1] * q[t][1] + k[s0][2] * q[t][2] + k[s0][3] * q[t][3];
+  }
+#pragma unroll
+  for (int m = LPR / 2; m >= 1; m >>= 1)
+#pragma unroll
+    for (int i = 0; i < NV; ++i) red_h[i] += __shfl_xor_sync(0xffffffffu, red_h[i], m);
+
+  // ---- 4. the 2T dot products of every state row with S_0 (raw q/k) -------
+  if (!mbar_wait_bounded(&sbar, 0)) {
+    // The staged tile never arrived: flag it, give the copy one more bounded
+    // wait so it does not land in a retired CTA's shared memory, and write
+    // nothing for this tile.
+    if (lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
+    mbar_wait_bounded(&sbar, 0);
+    return;
+  }
   float4 s[RPL];
 #pragma unroll
-  for (int i = 0; i < RPL; ++i) s[i] = ld_stream_f4(Sw + size_t(grp + GPW * i) * D + 4 * sub);
-
-  // 2. Causal conv over window ++ x for the q/k channels of key head hk and the
-  //    v channels of this tile; the raw inputs go to ring slots (off + t) mod R.
-  const int off = p.offsets[b];
-  const bool qk_writer = (tile == 0) && (h % rep == 0);
-  for (int ci = tid; ci < NCH; ci += kVerifyThreads) {
-    int c;
-    float *dst;
-    int dstride;
-    bool write_ring;
-    if (ci < D) {
-      c = hk * D + ci;
-      dst = &sq[0][ci];
-      dstride = D;
-      write_ring = qk_writer;
-    } else if (ci < 2 * D) {
-      c = H_k * D + hk * D + (ci - D);
-      dst = &sk[0][ci - D];
-      dstride = D;
-      write_ring = qk_writer;
-    } else {
-      c = 2 * H_k * D + h * D + j0 + (ci - 2 * D);
-      dst = &sv[0][ci - 2 * D];
-      dstride = kTileRows;
-      write_ring = true;
-    }
-    const uint2 wr = *reinterpret_cast<const uint2 *>(p.w + size_t(c) * kWidth);
-    const float w0 = bf2f(uint16_t(wr.x & 0xffff)), w1 = bf2f(uint16_t(wr.x >> 16));
-    const float w2 = bf2f(uint16_t(wr.y & 0xffff)), w3 = bf2f(uint16_t(wr.y >> 16));
-    float xt[kHist + T];
-    uint16_t xraw[T];
-    const uint16_t *ringb = p.ring + size_t(b) * R * C + c;
-#pragma unroll
-    for (int i = 0; i < kHist; ++i) xt[i] = bf2f(ringb[size_t(ring_slot(off - kHist + i, R)) * C]);
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      xraw[t] = p.x[(size_t(b) * T + t) * C + c];
-      xt[kHist + t] = bf2f(xraw[t]);
-    }
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      float acc = w0 * xt[t];
-      acc = fmaf(w1, xt[t + 1], acc);
-      acc = fmaf(w2, xt[t + 2], acc);
-      acc = fmaf(w3, xt[t + 3], acc);
-      dst[t * dstride] = p.act ? silu(acc) : acc;
-    }
-    if (write_ring) {
-      uint16_t *ringw = p.ring + size_t(b) * R * C + c;
-#pragma unroll
-      for (int t = 0; t < T; ++t) ringw[size_t(ring_slot(off + t, R)) * C] = xraw[t];
-    }
-  }
-  if (tid < T) {
-    sBeta[tid] = p.beta[(size_t(b) * T + tid) * H_v + h];
-  }
-  if (tid == 0) {
-    float acc = 0.f;
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const float gt = p.g[(size_t(b) * T + t) * H_v + h];
-      acc += gt;
-      sG[t] = acc;
-      sAlpha[t] = expf(gt);
-    }
-  }
-  __syncthreads();
-
-  // 3. L2 norms of q_t and k_t (q also scaled by 1/sqrt(D)).
-  for (int pr = warp; pr < 2 * T; pr += kVerifyThreads / 32) {
-    const float *v = pr < T ? sq[pr] : sk[pr - T];
-    float ss = 0.f;
-    for (int i = lane; i < D; i += 32) ss = fmaf(v[i], v[i], ss);
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    if (lane == 0) {
-      const float inv = 1.0f / sqrtf(ss + kNormEps);
-      s_inv[pr] = pr < T ? inv * (1.0f / sqrtf(float(D))) : inv;
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < 2 * T * D; i += kVerifyThreads) {
-    const int pr = i / D, e = i % D;
-    if (pr < T) sq[pr][e] *= s_inv[pr];
-    else sk[pr - T][e] *= s_inv[pr];
-  }
-  __syncthreads();
-
-  // 4. Per-head scalars: k_s.k_t, k_s.q_t and the decay/strength coefficients.
-  for (int pr = warp; pr < 2 * T * T; pr += kVerifyThreads / 32) {
-    const int which = pr / (T * T), st = pr % (T * T), s0 = st / T, t0 = st % T;
-    const float *va = sk[s0];
-    const float *vb = which ? sq[t0] : sk[t0];
-    float d = 0.f;
-    for (int i = lane; i < D; i += 32) d = fmaf(va[i], vb[i], d);
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) d += __shfl_xor_sync(0xffffffffu, d, m);
-    if (lane == 0) s_dot[which][s0][t0] = d;
-  }
-  __syncthreads();
-  if (tid < T * T) {
-    const int t = tid / T, s0 = tid % T;
-    const float r = expf(sG[t] - sG[s0]);
-    sM[t][s0] = s0 < t ? sBeta[t] * r * s_dot[0][s0][t] : 0.f;
-    sN[t][s0] = s0 <= t ? r * s_dot[1][s0][t] : 0.f;
-    if (s0 == 0) {
-      sGam[t] = expf(sG[t]);
-      sBg[t] = sBeta[t] * sGam[t];
-    }
-  }
-  __syncthreads();
-
-  // 5. The 2T dot products of every state row with S_0, one butterfly each.
+  for (int i = 0; i < RPL; ++i)
+    s[i] = *reinterpret_cast<const float4 *>(&sS[(warp * 8 + grp + GPW * i) * D + 4 * sub]);
   float red[2 * T];
 #pragma unroll
-  for (int m = 0; m < 2 * T; ++m) {
-    const float4 vec = *reinterpret_cast<const float4 *>(m < T ? &sk[m][4 * sub] : &sq[m - T][4 * sub]);
+  for (int mvec = 0; mvec < 2 * T; ++mvec) {
+    const float *vv = mvec < T ? k[mvec] : q[mvec - T];
+    const float4 vec = make_float4(vv[0], vv[1], vv[2], vv[3]);
     float acc[RPL];
 #pragma unroll
     for (int i = 0; i < RPL; ++i) acc[i] = dot4(s[i], vec);
-    red[m] = reduce_rows<D>(acc, lane);
+    red[mvec] = reduce_rows<D>(acc, lane);
   }
 
-  // 6. Scalar recurrence for the row this lane now holds.
-  const int istar = row_of_lane<D>(lane);
-  const int jj = warp * 8 + grp + GPW * istar;  // row within the tile
-  float e[T];
-  float o[T];
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    float acc = fmaf(sBeta[t], sv[t][jj], -sBg[t] * red[t]);
-#pragma unroll
-    for (int s0 = 0; s0 < t; ++s0) acc = fmaf(-sM[t][s0], e[s0], acc);
-    e[t] = acc;
-    float ot = sGam[t] * red[T + t];
-#pragma unroll
-    for (int s0 = 0; s0 <= t; ++s0) ot = fmaf(sN[t][s0], e[s0], ot);
-    o[t] = ot;
-  }
-  const bool row_leader = (lane & 3) == 0;  // four lanes hold each row after the butterfly
-  if (row_leader) {
+  // ---- 5. per-head coefficients (every lane, in registers) -----------------
+  float inv_q[T], inv_k[T], Gc[T], gam[T];
+  {
+    const float qs = 1.0f / sqrtf(float(D));
+    float acc = 0.f;
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-      const size_t idx = ((size_t(b) * T + t) * H_v + h) * D + j0 + jj;
+      inv_q[t] = rsqrtf(red_h[2 * t] + kNormEps) * qs;
+      inv_k[t] = rsqrtf(red_h[2 * t + 1] + kNormEps);
+      acc += gt[t];
+      Gc[t] = acc;
+      gam[t] = expf(acc);
+    }
+  }
+
+  // ---- 6. scalar recurrence for the row this lane holds --------------------
+  float e[T], o[T];
+  {
+    int nkk = 2 * T, nkq = 2 * T + NKK;
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      float decay[T];  // exp(G_t - G_s), s < t
+#pragma unroll
+      for (int s0 = 0; s0 < t; ++s0) decay[s0] = expf(Gc[t] - Gc[s0]);
+      float acc = fmaf(bt[t], v[t], -(bt[t] * gam[t]) * (red[t] * inv_k[t]));
+#pragma unroll
+      for (int s0 = 0; s0 < t; ++s0) {
+        const float kk = red_h[nkk++] * inv_k[s0] * inv_k[t];
+        acc = fmaf(-(bt[t] * decay[s0] * kk), e[s0], acc);
+      }
+      e[t] = acc;
+      float ot = gam[t] * (red[T + t] * inv_q[t]);
+#pragma unroll
+      for (int s0 = 0; s0 <= t; ++s0) {
+        const float kq = red_h[nkq++] * inv_k[s0] * inv_q[t];
+        ot = fmaf((s0 == t ? 1.0f : decay[s0]) * kq, e[s0], ot);
+      }
+      o[t] = ot;
+    }
+  }
+
+  // ---- 7. outputs and captures ----------------------------------------------
+  if (leader) {
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const size_t idx = ((size_t(b) * T + t) * H_v + h) * D + jrow;
       p.out[idx] = f2bf(o[t]);
       if (MODE == GDN_COMMIT_RECOMPUTE) p.ws_e[idx] = e[t];
     }
   }
-
   if (MODE == GDN_COMMIT_RECOMPUTE) {
-    if (qk_writer)
-      for (int i = tid; i < T * D; i += kVerifyThreads) {
-        const int t = i / D, e2 = i % D;
-        p.ws_k[((size_t(b) * T + t) * H_k + hk) * D + e2] = sk[t][e2];
-      }
-    if (tile == 0 && tid < T) p.ws_G[(size_t(b) * T + tid) * H_v + h] = sG[tid];
+    if (qk_writer && warp == 0 && grp == 0)
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+        st_f4(p.ws_k + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub,
+              make_float4(k[t][0] * inv_k[t], k[t][1] * inv_k[t], k[t][2] * inv_k[t], k[t][3] * inv_k[t]));
+    if (tile == 0 && warp == 0 && lane < T) {
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+        if (lane == t) p.ws_G[(size_t(b) * T + t) * H_v + h] = Gc[t];
+    }
   } else {
     // SNAPSHOT: every lane needs e_t of each of its rows; fetch them from the
     // lane that computed them, then step the rows through S_t = a_t S_{t-1} + e_t k_t.
     const size_t plane = size_t(p.B) * H_v * D * D;
-    float *snap = p.ws_snap + ((size_t(b) * H_v + h) * D + j0 + warp * 8) * D;
+    float *snap = p.ws_snap + ((size_t(b) * H_v + h) * D + jw) * D;
+    float alpha[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) alpha[t] = expf(gt[t]);
 #pragma unroll
     for (int i = 0; i < RPL; ++i) {
       const int src = grp * LPR + lane_of_row<D>(i);
@@ -240,12 +313,11 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_kernel(const VerifyPara
 #pragma unroll
       for (int t = 0; t < T; ++t) {
         const float et = __shfl_sync(0xffffffffu, e[t], src);
-        const float4 kv = *reinterpret_cast<const float4 *>(&sk[t][4 * sub]);
-        const float a = sAlpha[t];
-        st.x = fmaf(et, kv.x, a * st.x);
-        st.y = fmaf(et, kv.y, a * st.y);
-        st.z = fmaf(et, kv.z, a * st.z);
-        st.w = fmaf(et, kv.w, a * st.w);
+        const float a = alpha[t];
+        st.x = fmaf(et, k[t][0] * inv_k[t], a * st.x);
+        st.y = fmaf(et, k[t][1] * inv_k[t], a * st.y);
+        st.z = fmaf(et, k[t][2] * inv_k[t], a * st.z);
+        st.w = fmaf(et, k[t][3] * inv_k[t], a * st.w);
         st_f4(snap + t * plane + size_t(grp + GPW * i) * D + 4 * sub, st);
       }
     }
@@ -255,13 +327,11 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_kernel(const VerifyPara
 template <int D>
 cudaError_t launch_verify_d(const VerifyParams &p, int T, int mode, cudaStream_t stream) {
   const dim3 grid(D / kTileRows, p.H_v, p.B), block(kVerifyThreads);
-#define GDN_VERIFY_CASE(TT)                                                                   \
-  case TT:                                                                                    \
-    if (mode == GDN_COMMIT_RECOMPUTE)                                                         \
-      verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE><<<grid, block, 0, stream>>>(p);              \
-    else                                                                                      \
-      verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT><<<grid, block, 0, stream>>>(p);               \
-    break;
+#define GDN_VERIFY_CASE(TT)                                                                     \
+  case TT:                                                                                      \
+    return mode == GDN_COMMIT_RECOMPUTE                                                         \
+               ? launch_pdl(verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>, grid, block, stream, p) \
+               : launch_pdl(verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>, grid, block, stream, p);
   switch (T) {
     GDN_VERIFY_CASE(1)
     GDN_VERIFY_CASE(2)
@@ -275,7 +345,6 @@ cudaError_t launch_verify_d(const VerifyParams &p, int T, int mode, cudaStream_t
       return cudaErrorInvalidValue;
   }
 #undef GDN_VERIFY_CASE
-  return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -24,6 +24,8 @@ GDN_ACT_NONE = 0
 GDN_ACT_SILU = 1
 GDN_COMMIT_RECOMPUTE = 0
 GDN_COMMIT_SNAPSHOT = 1
+GDN_VERIFY_OVERLAP = 0x100
+GDN_STATUS_TIMEOUT = 2
 GDN_STATUS_BAD_KEEP = 1
 GDN_MAX_LAYERS = 256
 

@@ -83,8 +83,9 @@ class GpuStack:
         g = geom
         self.out = torch.empty((n_layers, g.B, g.T, g.H_v, g.d), dtype=torch.bfloat16, device="cuda")
 
-    def verify(self, layer: int, x_bits, g, beta):
-        L.gdn_conv_verify(self.dims, self.mode, dev_bf16(x_bits), self.w[layer],
+    def verify(self, layer: int, x_bits, g, beta, overlap=False):
+        mode = self.mode | (L.GDN_VERIFY_OVERLAP if overlap else 0)
+        L.gdn_conv_verify(self.dims, mode, dev_bf16(x_bits), self.w[layer],
                           torch.from_numpy(np.ascontiguousarray(g)).cuda(),
                           torch.from_numpy(np.ascontiguousarray(beta)).cuda(),
                           self.state[layer], self.ring[layer], self.offsets, self.active,

@@ -224,7 +224,10 @@ def test_stack_30_layers_256_cycles_sampled(gdn):
         cy = pool_in[c % pool]
         xd, gd, bd = dev_pool[c % pool]
         for l in range(n_layers):
-            L.gdn_conv_verify(gpu.dims, gpu.mode, xd[l], gpu.w[l], gd[l], bd[l], gpu.state[l], gpu.ring[l],
+            # the launch configuration the benchmark times: layers after the
+            # first stage their state while the previous layer's verify ends
+            mode = gpu.mode | (L.GDN_VERIFY_OVERLAP if l > 0 else 0)
+            L.gdn_conv_verify(gpu.dims, mode, xd[l], gpu.w[l], gd[l], bd[l], gpu.state[l], gpu.ring[l],
                               gpu.offsets, gpu.active, gpu.out[l], gpu.ws[l])
         o_units = [u.verify(cy["x"][u.layer], cy["g"][u.layer], cy["beta"][u.layer], active[u.b]) for u in units]
         out = gpu.out
@@ -242,3 +245,34 @@ def test_stack_30_layers_256_cycles_sampled(gdn):
                 win = ring_window(ring, offsets[u.b:u.b + 1], geom.R)[:, u.ch]
                 assert np.array_equal(win, u.win), f"cycle {c} unit window"
     assert L.gdn_get_status(clear=True) == 0
+
+
+def test_overlap_flag_is_bit_identical(gdn):
+    """GDN_VERIFY_OVERLAP changes only when the state tile is fetched, never a value."""
+    geom = synth.COHORT
+    st = synth.layer_state(geom, 14, 3)
+    cy = synth.cycle_inputs(geom, 14, 0, 3)
+    keep = np.array([2, 1, 0, 2, 1, 2, 0, 1], np.int32)
+    runs = []
+    for overlap in (False, True):
+        gpu = GpuStack(geom, st, synth.active_mask(8, (6, 7)), L.GDN_COMMIT_RECOMPUTE, 3)
+        for l in range(3):
+            gpu.verify(l, cy["x"][l], cy["g"][l], cy["beta"][l], overlap=overlap and l > 0)
+        gpu.commit(keep)
+        torch.cuda.synchronize()
+        runs.append((gpu.out.clone(), gpu.state.clone(), host_bits(gpu.ring), gpu.offsets.clone()))
+    a, b = runs
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1]) and np.array_equal(a[2], b[2]) and torch.equal(a[3], b[3])
+
+
+def test_unknown_mode_flag_rejected(gdn):
+    geom = synth.TINY
+    st = synth.layer_state(geom, 0, 1)
+    gpu = GpuStack(geom, st, synth.active_mask(1), L.GDN_COMMIT_RECOMPUTE, 1)
+    cy = synth.cycle_inputs(geom, 0, 0, 1)
+    with pytest.raises(L.GdnError) as ei:
+        L.gdn_conv_verify(gpu.dims, 0x200, dev_bf16(cy["x"][0]), gpu.w[0],
+                          torch.from_numpy(cy["g"][0]).cuda(), torch.from_numpy(cy["beta"][0]).cuda(),
+                          gpu.state[0], gpu.ring[0], gpu.offsets, gpu.active, gpu.out[0], gpu.ws[0])
+    assert ei.value.code == L.GDN_ERR_INVALID_ARG
