@@ -210,6 +210,43 @@ int gdn_prefill_chunked(const gdn_dims *dims, int L, const gdn_bf16 *x, const gd
                         void *stream);
 
 /*
+ * gdn_conv_verify_noalloc -- gdn_conv_verify for callers that cannot allocate
+ * device memory.  (The pages describe no such call; it exists for hosts of
+ * this library.)
+ *
+ * Some callers have no way to hand the library a workspace: a plug-in running
+ * inside a host framework that owns every device allocation and gives the
+ * plug-in only its input and output tensors, or a latency-critical serving
+ * loop where a cudaMalloc (which can synchronise the device) is not allowed
+ * once serving has started.  This entry point does what gdn_conv_verify does,
+ * with the same arguments except the workspace: the verify captures go to a
+ * scratch array built into the library's device code, GDN_NOALLOC_WS_BYTES
+ * (4 MiB) per GPU, which every GPU that loads the library holds until the
+ * process exits.  It allocates nothing and frees nothing.
+ *  - Shapes whose workspace (gdn_layer_workspace_bytes) exceeds the scratch
+ *    are rejected with GDN_ERR_WORKSPACE before anything is launched (e.g. the
+ *    B=8, T=2, 32x128 cohort needs about 0.4 MiB in RECOMPUTE mode and fits;
+ *    its SNAPSHOT mode needs 32 MiB and does not).
+ *  - The first call on each device looks up the scratch's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture begins.
+ *  - The scratch's device address is stored in *layer_ws_used (if not NULL):
+ *    pass it as this layer's workspace to gdn_commit (n_layers = 1).
+ *  - Every call shares the one scratch array and it keeps the last call's
+ *    contents; nothing in it needs to start at zero, since verify writes every
+ *    entry the commit reads.  The captures of one call are valid only until
+ *    the next call of this entry point on the same device, so commit that
+ *    layer before verifying another with it.  Calls that overlap on the GPU
+ *    (other streams, other host threads) race on the scratch.
+ * Errors: as gdn_conv_verify, plus GDN_ERR_WORKSPACE for shapes too large.
+ */
+#define GDN_NOALLOC_WS_BYTES (4u << 20)
+int gdn_conv_verify_noalloc(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w,
+                            const float *g, const float *beta, const float *state, gdn_bf16 *ring,
+                            const int32_t *offsets, const uint8_t *active, gdn_bf16 *out,
+                            void **layer_ws_used, void *stream);
+
+/*
  * Read the sticky device status word of the current device (GDN_STATUS_*
  * bits) into *status; clear it if `clear` is nonzero.  Synchronises the
  * device.  Returns GDN_OK or GDN_ERR_CUDA / GDN_ERR_INVALID_ARG.

@@ -9,6 +9,7 @@
 // layers).
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "gdn_common.cuh"
@@ -221,6 +222,60 @@ __attribute__((visibility("default"))) int gdn_get_status(int clear, uint32_t *s
     if (e != cudaSuccess) return cuda_fail(e, "gdn_get_status clear");
   }
   return ok();
+}
+
+// ---- verify without caller-provided workspace ---------------------------------
+// Scratch for gdn_conv_verify_noalloc: one layer's verify captures.  It lives
+// in the library's own device memory, so every GPU that loads the library
+// holds these bytes until the process exits.  Host code may not use the name
+// `g_noalloc_ws` as an address (on the host it is only a stand-in for the
+// device symbol); the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_ws[GDN_NOALLOC_WS_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_lock;
+void *g_noalloc_ptr[64] = {nullptr};  // device address of g_noalloc_ws, per device
+
+// Look up (once per device, with that device current) where the scratch
+// array lives on the current device.
+int noalloc_scratch(void **ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_conv_verify_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device index %d above 63", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_lock);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_ws);
+    if (e != cudaSuccess || !p) return cuda_fail(e, "gdn_conv_verify_noalloc: cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
+__attribute__((visibility("default"))) int gdn_conv_verify_noalloc(
+    const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
+    const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
+    const uint8_t *active, gdn_bf16 *out, void **layer_ws_used, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_mode(mode & 0xff))) return rc;
+  const size_t need = layer_ws_bytes(dims, mode & 0xff);
+  if (need > GDN_NOALLOC_WS_BYTES)
+    return fail(GDN_ERR_WORKSPACE,
+                "gdn_conv_verify_noalloc: this shape and mode need %zu bytes of scratch, the library's "
+                "built-in scratch holds %zu; use gdn_conv_verify with a caller-allocated workspace",
+                need, size_t(GDN_NOALLOC_WS_BYTES));
+  void *ws = nullptr;
+  if ((rc = noalloc_scratch(&ws))) return rc;
+  rc = gdn_conv_verify(dims, mode, x, conv_w, g, beta, state, ring, offsets, active, out, ws,
+                       GDN_NOALLOC_WS_BYTES, stream);
+  if (rc == GDN_OK && layer_ws_used) *layer_ws_used = ws;
+  return rc;
 }
 
 }  // extern "C"

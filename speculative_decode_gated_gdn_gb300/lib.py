@@ -28,9 +28,11 @@ GDN_VERIFY_OVERLAP = 0x100
 GDN_STATUS_TIMEOUT = 2
 GDN_STATUS_BAD_KEEP = 1
 GDN_MAX_LAYERS = 256
+GDN_NOALLOC_WS_BYTES = 4 << 20
 
 EXPORTS = ("gdn_version", "gdn_last_error", "gdn_layer_workspace_bytes", "gdn_conv_verify",
-           "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status")
+           "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status",
+           "gdn_conv_verify_noalloc")
 
 
 class GdnError(RuntimeError):
@@ -74,6 +76,8 @@ def _declare(lib):
     lib.gdn_prefill_workspace_bytes.argtypes = [D, ctypes.c_int]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
     lib.gdn_prefill_chunked.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
+    lib.gdn_conv_verify_noalloc.restype = ctypes.c_int
+    lib.gdn_conv_verify_noalloc.argtypes = [D, ctypes.c_int] + [_P] * 9 + [ctypes.POINTER(_P), _P]
     lib.gdn_get_status.restype = ctypes.c_int
     lib.gdn_get_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)]
 
@@ -158,6 +162,26 @@ def gdn_conv_verify(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets,
         _ptr(active, "active", torch.uint8), _ptr(out, "out", torch.bfloat16), _ptr(layer_ws, "layer_ws"),
         int(layer_ws_bytes), _stream(stream))
     _check(rc, "gdn_conv_verify")
+
+
+def gdn_conv_verify_noalloc(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets, active, out,
+                            stream=None) -> int:
+    """gdn_conv_verify with the library's built-in scratch as the workspace.
+
+    For callers that cannot allocate device memory.  Returns the scratch's
+    device address, to be passed as this layer's workspace to gdn_commit
+    before the next call of this function on the device.
+    """
+    torch = _t()
+    used = _P(0)
+    rc = load().gdn_conv_verify_noalloc(
+        ctypes.byref(d), mode, _ptr(x, "x", torch.bfloat16), _ptr(conv_w, "conv_w", torch.bfloat16),
+        _ptr(g, "g", torch.float32), _ptr(beta, "beta", torch.float32), _ptr(state, "state", torch.float32),
+        _ptr(ring, "ring", torch.bfloat16), _ptr(offsets, "offsets", torch.int32),
+        _ptr(active, "active", torch.uint8), _ptr(out, "out", torch.bfloat16), ctypes.byref(used),
+        _stream(stream))
+    _check(rc, "gdn_conv_verify_noalloc")
+    return int(used.value)
 
 
 def gdn_commit(d: gdn_dims, mode, states, layer_ws, keep, active, offsets, stream=None):
