@@ -35,6 +35,8 @@ int ok() {
   return GDN_OK;
 }
 
+constexpr int kMaxPrefillLen = 1 << 20;
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_dims(const gdn_dims *d) {
@@ -194,18 +196,35 @@ __attribute__((visibility("default"))) int gdn_commit(const gdn_dims *dims, int 
 }
 
 __attribute__((visibility("default"))) size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L) {
-  (void)dims;
-  (void)L;
-  return 0;
+  if (check_dims(dims) != GDN_OK || L < 1 || L > kMaxPrefillLen) return 0;
+  return prefill_workspace_bytes(dims->B, L, dims->H_k, dims->H_v, dims->d_k);
 }
 
 __attribute__((visibility("default"))) int gdn_prefill_chunked(
     const gdn_dims *dims, int L, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
     const float *beta, float *state, gdn_bf16 *ring, int32_t *offsets, gdn_bf16 *out, void *ws,
     size_t ws_bytes, void *stream) {
-  (void)dims, (void)L, (void)x, (void)conv_w, (void)g, (void)beta, (void)state, (void)ring;
-  (void)offsets, (void)out, (void)ws, (void)ws_bytes, (void)stream;
-  return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked is not available in this build");
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (L < 0 || L > kMaxPrefillLen)
+    return fail(GDN_ERR_UNSUPPORTED, "prompt length L=%d outside [0, %d]", L, kMaxPrefillLen);
+  if (dims->B == 0 || L == 0) return ok();
+  GDN_NEED_PTR(x, 16);
+  GDN_NEED_PTR(conv_w, 16);
+  GDN_NEED_PTR(g, 16);
+  GDN_NEED_PTR(beta, 16);
+  GDN_NEED_PTR(state, 16);
+  GDN_NEED_PTR(ring, 16);
+  GDN_NEED_PTR(offsets, 4);
+  GDN_NEED_PTR(out, 16);
+  GDN_NEED_PTR(ws, 256);
+  const size_t need = prefill_workspace_bytes(dims->B, L, dims->H_k, dims->H_v, dims->d_k);
+  if (ws_bytes < need) return fail(GDN_ERR_WORKSPACE, "prefill workspace has %zu bytes, needs %zu", ws_bytes, need);
+  cudaError_t e = launch_prefill(x, conv_w, g, beta, state, ring, offsets, out, ws, dims->B, L, dims->H_k,
+                                 dims->H_v, dims->d_k, kHist + dims->T_max, dims->act,
+                                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_prefill_chunked launch");
+  return ok();
 }
 
 __attribute__((visibility("default"))) int gdn_get_status(int clear, uint32_t *status) {

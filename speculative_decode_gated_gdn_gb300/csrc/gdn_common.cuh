@@ -243,6 +243,10 @@ cudaError_t launch_verify_32(const VerifyParams &p, int T, int mode, cudaStream_
 cudaError_t launch_verify_64(const VerifyParams &p, int T, int mode, cudaStream_t s);
 cudaError_t launch_verify_128(const VerifyParams &p, int T, int mode, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, int D, int mode, cudaStream_t s);
+size_t prefill_workspace_bytes(int B, int L, int H_k, int H_v, int D);
+cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g, const float *beta, float *state,
+                           uint16_t *ring, int32_t *offsets, uint16_t *out, void *ws, int B, int L, int H_k,
+                           int H_v, int D, int R, int act, cudaStream_t stream);
 uint32_t *status_word_address();  // device address of the sticky status word
 
 }  // namespace gdn

@@ -75,7 +75,7 @@ def _declare(lib):
     lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_prefill_workspace_bytes.argtypes = [D, ctypes.c_int]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
-    lib.gdn_prefill_chunked.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
+    lib.gdn_prefill_chunked.argtypes = [D, ctypes.c_int] + [_P] * 9 + [ctypes.c_size_t, _P]
     lib.gdn_conv_verify_noalloc.restype = ctypes.c_int
     lib.gdn_conv_verify_noalloc.argtypes = [D, ctypes.c_int] + [_P] * 9 + [ctypes.POINTER(_P), _P]
     lib.gdn_get_status.restype = ctypes.c_int

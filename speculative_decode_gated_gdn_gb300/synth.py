@@ -49,20 +49,44 @@ def _key(seed: int, name: str) -> np.uint64:
     return _mix64(base)[0]
 
 
-def uniform(seed: int, name: str, n: int) -> np.ndarray:
-    """n doubles in the open interval (0, 1) from stream (seed, name)."""
-    i = np.arange(1, n + 1, dtype=np.uint64)
+def uniform(seed: int, name: str, n: int, start: int = 0) -> np.ndarray:
+    """Doubles start .. start+n-1 of stream (seed, name), in the open interval (0, 1)."""
+    i = np.arange(start + 1, start + n + 1, dtype=np.uint64)
     with np.errstate(over="ignore"):
         z = _mix64(_key(seed, name) + i * _GOLDEN)
     return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
 
 
-def normal(seed: int, name: str, shape, std: float = 1.0) -> np.ndarray:
-    """fp64 normals N(0, std^2) of the given shape (Box-Muller, cosine branch)."""
-    n = int(np.prod(shape))
-    u = uniform(seed, name, 2 * n)
+_BLOCK = 1 << 22  # normals generated per block (bounds temporary memory)
+
+
+def _normal_block(seed, name, start, n, std):
+    u = uniform(seed, name, 2 * n, 2 * start)
     r = np.sqrt(-2.0 * np.log(u[0::2]))
-    return (std * r * np.cos(2.0 * np.pi * u[1::2])).reshape(shape)
+    return std * r * np.cos(2.0 * np.pi * u[1::2])
+
+
+def normal(seed: int, name: str, shape, std: float = 1.0) -> np.ndarray:
+    """fp64 normals N(0, std^2) of the given shape (Box-Muller, cosine branch).
+
+    Value i uses uniforms 2i and 2i+1 of the stream, so blocks of any size give
+    the same array."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float64)
+    for s0 in range(0, n, _BLOCK):
+        m = min(_BLOCK, n - s0)
+        out[s0:s0 + m] = _normal_block(seed, name, s0, m, std)
+    return out.reshape(shape)
+
+
+def normal_bf16(seed: int, name: str, shape, std: float = 1.0) -> np.ndarray:
+    """normal() rounded to bf16 bits, generated block by block (for large arrays)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    for s0 in range(0, n, _BLOCK):
+        m = min(_BLOCK, n - s0)
+        out[s0:s0 + m] = bf16_bits(_normal_block(seed, name, s0, m, std))
+    return out.reshape(shape)
 
 
 def integers(seed: int, name: str, shape, lo: int, hi: int) -> np.ndarray:
@@ -159,7 +183,7 @@ def cycle_inputs(geom: Geometry, seed: int, cycle: int, n_layers: int = 1) -> di
     """
     g = geom
     tag = f"c{cycle}"
-    x = bf16_bits(normal(seed, "x" + tag, (n_layers, g.B, g.T, g.C)))
+    x = normal_bf16(seed, "x" + tag, (n_layers, g.B, g.T, g.C))
     gl = (-softplus(normal(seed, "g" + tag, (n_layers, g.B, g.T, g.H_v))) * 0.5).astype(np.float32)
     bz = normal(seed, "beta" + tag, (n_layers, g.B, g.T, g.H_v))
     beta = (1.0 / (1.0 + np.exp(-bz))).astype(np.float32)
@@ -180,7 +204,7 @@ def prompt_inputs(geom: Geometry, seed: int, L: int) -> dict:
       x    uint16 bf16 [B][L][C],  g, beta float32 [B][L][H_v]
     """
     g = geom
-    x = bf16_bits(normal(seed, "px", (g.B, L, g.C)))
+    x = normal_bf16(seed, "px", (g.B, L, g.C))
     gl = (-softplus(normal(seed, "pg", (g.B, L, g.H_v))) * 0.5).astype(np.float32)
     bz = normal(seed, "pbeta", (g.B, L, g.H_v))
     beta = (1.0 / (1.0 + np.exp(-bz))).astype(np.float32)

@@ -108,3 +108,23 @@ def test_empty_batch_is_a_no_op(lib):
     P = ctypes.c_void_p
     arr = (P * 1)(1 << 20)
     assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, arr, None, None, None, None) == L.GDN_OK
+
+
+def declared_arity():
+    """Number of parameters of every gdn_* function declared in the headers."""
+    arity = {}
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(HEADER_DIR, fn)).read(), flags=re.S)
+            for name, params in re.findall(r"\b(gdn_\w+)\s*\(([^)]*)\)\s*;", text):
+                params = params.strip()
+                arity[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return arity
+
+
+def test_binding_argument_counts_match_header(lib):
+    arity = declared_arity()
+    assert arity, "no declarations parsed"
+    for name, n in arity.items():
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, f"{name}: header has {n} parameters, binding {argtypes}"

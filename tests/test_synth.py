@@ -44,3 +44,12 @@ def test_cohort_recipe():
         for s in range(g.R):
             isnan = np.isnan(synth.bf16_to_f32(st["ring"][0, b, s]))
             assert isnan.all() == (s not in win_slots)
+
+
+def test_blocked_generation_is_block_size_independent(monkeypatch):
+    a = synth.normal(9, "blk", (3000,))
+    monkeypatch.setattr(synth, "_BLOCK", 256)
+    b = synth.normal(9, "blk", (3000,))
+    c = synth.normal_bf16(9, "blk", (3000,))
+    assert np.array_equal(a, b)
+    assert np.array_equal(c, synth.bf16_bits(a))
