@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default="cycle", choices=["cycle", "prefill"],
+                    help="cycle: the verify+commit headline; prefill: chunked state priming of one row")
+    ap.add_argument("--L", type=int, default=4096, help="prompt length for --workload prefill")
     return ap.parse_args()
 
 
@@ -507,6 +510,67 @@ def run_e2e(args, geom, d, mode, dev, inp, keeps_np, state, ring, conv_w, offset
                    "outputs and offsets copied out; one CUDA graph per step"}
 
 
+# ---------------------------------------------------------------- prefill leg
+def prefill_flops(L, H_v, d, chunk=64):
+    """Algorithmic FLOPs of the chunked form per prompt: per (chunk, value head)
+    K K^T, Q K^T, W, U (n x n x d each), E = U - W S^T, Q S^T, S += K~^T E
+    (n x d x d each), Pm E (n x n x d), plus the n^3/3 triangular solve."""
+    total = 0
+    for c0 in range(0, L, chunk):
+        n = min(chunk, L - c0)
+        total += H_v * (4 * 2 * n * n * d + 3 * 2 * n * d * d + 2 * n * n * d + n ** 3 // 3)
+    return total
+
+
+def run_prefill_bench(args, rank, world, local):
+    """Time gdn_prefill_chunked: B rows primed over L tokens per step."""
+    import torch
+    from speculative_decode_gated_gdn_gb300 import lib as L
+    from speculative_decode_gated_gdn_gb300 import synth
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    geom = synth.Geometry(B=args.B if args.B != 8 else 1, T=2, H_k=16, H_v=32, d=128)
+    Lp, K, W = args.L, args.steps, args.warmup
+    d = L.dims_of(geom)
+    pr = synth.prompt_inputs(geom, args.seed + rank, Lp)
+    st = synth.layer_state(geom, args.seed + rank, 1, offsets=np.zeros(geom.B, np.int32))
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x, w = bf(pr["x"]), bf(st["conv_w"][0])
+    g, beta = torch.from_numpy(pr["g"]).to(dev), torch.from_numpy(pr["beta"]).to(dev)
+    state = torch.zeros((geom.B, geom.H_v, geom.d, geom.d), dtype=torch.float32, device=dev)
+    ring = torch.zeros((geom.B, geom.R, geom.C), dtype=torch.bfloat16, device=dev)
+    offsets = torch.zeros(geom.B, dtype=torch.int32, device=dev)
+    out = torch.empty((geom.B, Lp, geom.H_v, geom.d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.gdn_prefill_workspace_bytes(d, Lp), dtype=torch.uint8, device=dev)
+
+    def step():
+        L.gdn_prefill_chunked(d, Lp, x, w, g, beta, state, ring, offsets, out, ws)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(K):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / K
+    flops = prefill_flops(Lp, geom.H_v, geom.d) * geom.B
+    hbm = geom.B * (Lp * geom.C * 2 + Lp * geom.H_v * geom.d * 2 + 2 * geom.H_v * geom.d * geom.d * 4
+                    + 2 * Lp * geom.H_v * 4)
+    return {"metric": "GDN chunked prefill prompt tokens/s (1 GPU)", "value": geom.B * Lp / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"chunked prefill B={geom.B} L={Lp} H_k=16 H_v=32 d=128 chunk 64",
+                       "B": geom.B, "L": Lp},
+            "algorithmic_gflop_per_step": flops / 1e9, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
+            "algorithmic_hbm_mb_per_step": hbm / 1e6, "achieved_hbm_gbs": hbm / (ms * 1e-3) / 1e9}
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """The oracle (plain fp64 C, as it stands) on the host cores, on this
@@ -565,6 +629,11 @@ def main():
         line = run_reference(args, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+    if args.workload == "prefill":
+        res = run_prefill_bench(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
         return
     res = run_gpu(args, rank, world, local)
     if rank == 0:

@@ -19,7 +19,8 @@
 //
 // Kernels (one stream, in order):
 //   prefill_conv_kernel   conv + SiLU + L2 norm of every token  -> Q, K, V (fp32)
-//   prefill_chunk_kernel  per (chunk, value head): G, A, Tm, W, U, Pm
+//   prefill_chunk_tc_kernel  per (chunk pair, value head): G, A, Tm, W, U, Pm
+//                         (the products on tcgen05)
 //   prefill_state_kernel  per (value head, 32-row d_v slice): the chunk loop
 //   prefill_ring_kernel   last three raw inputs into the ring
 // The state kernel also advances offsets by L.
@@ -46,11 +47,19 @@ struct PrefillParams {
   float *U;   // [B][H_v][L][D]
   float *Gc;  // [B][H_v][L]     within-chunk cumulative log-decay
   float *Pm;  // [B][H_v][NC][64][64]
-  int B, L, NC, H_k, H_v, C, R, act;
+  // bf16 hi/lo operand tiles for the tensor-core chunk kernel, one 64-token
+  // chunk per tile, in the tcgen05 K-major no-swizzle canonical layout
+  // (8-row x 16-byte core matrices; K-direction stride 128 B).
+  uint16_t *qn_hi, *qn_lo;  // [B][H_k][NCp] tiles of q  as [t][i] (K dim = d)
+  uint16_t *kn_hi, *kn_lo;  // [B][H_k][NCp] tiles of k  as [t][i]
+  uint16_t *kt_hi, *kt_lo;  // [B][H_k][NCp] tiles of k^T as [i][t] (K dim = 64 tokens)
+  uint16_t *vt_hi, *vt_lo;  // [B][H_v][NCp] tiles of v^T as [j][t]
+  uint32_t *status;         // sticky device status word
+  int B, L, NC, NCp, H_k, H_v, C, R, act;
 };
 
 struct PrefillWs {
-  size_t q, k, v, W, U, Gc, Pm, total;
+  size_t q, k, v, W, U, Gc, Pm, qn_hi, qn_lo, kn_hi, kn_lo, kt_hi, kt_lo, vt_hi, vt_lo, total;
 };
 
 inline PrefillWs prefill_ws(int B, int L, int H_k, int H_v, int D) {
@@ -65,8 +74,61 @@ inline PrefillWs prefill_ws(int B, int L, int H_k, int H_v, int D) {
   w.U = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp * D);
   w.Gc = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp);
   w.Pm = o, o += align256(sizeof(float) * size_t(B) * H_v * NC * kChunk * kChunk);
+  const int NCp = (NC + 1) & ~1;  // the tensor-core kernel works on chunk pairs
+  const size_t tile = size_t(kChunk) * D * sizeof(uint16_t);
+  size_t *hk_tiles[6] = {&w.qn_hi, &w.qn_lo, &w.kn_hi, &w.kn_lo, &w.kt_hi, &w.kt_lo};
+  for (size_t *f : hk_tiles) *f = o, o += align256(tile * B * H_k * NCp);
+  w.vt_hi = o, o += align256(tile * B * H_v * NCp);
+  w.vt_lo = o, o += align256(tile * B * H_v * NCp);
   w.total = o;
   return w;
+}
+
+// Byte offset of element (row, k) in a K-major no-swizzle canonical tile whose
+// K extent is Kd bf16 elements: core matrix (row/8, k/8) at
+// (row/8) * (Kd/8)*128 + (k/8) * 128, then row%8 * 16 + k%8 * 2 inside it.
+__host__ __device__ constexpr uint32_t canon_off(int row, int k, int Kd) {
+  return uint32_t((row / 8) * (Kd / 8) * 128 + (k / 8) * 128 + (row % 8) * 16 + (k % 8) * 2);
+}
+
+__device__ __forceinline__ void split_bf16(float y, uint16_t &hi, uint16_t &lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(y);
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(__float2bfloat16_rn(y - __bfloat162float(h)));
+}
+
+// Write one channel's 64 values into a natural tile ([t][i], K dim D) and,
+// when `transposed` is set, into a transposed tile ([i][t], K dim 64).
+template <int D>
+__device__ __forceinline__ void store_tiles(const float (&y)[kChunk], int ch, uint16_t *nat_hi, uint16_t *nat_lo,
+                                            uint16_t *tr_hi, uint16_t *tr_lo) {
+  if (nat_hi) {
+#pragma unroll
+    for (int t = 0; t < kChunk; ++t) {
+      uint16_t hi, lo;
+      split_bf16(y[t], hi, lo);
+      const uint32_t o = canon_off(t, ch, D) / 2;
+      nat_hi[o] = hi;
+      nat_lo[o] = lo;
+    }
+  }
+  if (tr_hi) {
+#pragma unroll
+    for (int t8 = 0; t8 < kChunk; t8 += 8) {
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint16_t h0, l0, h1, l1;
+        split_bf16(y[t8 + 2 * q], h0, l0);
+        split_bf16(y[t8 + 2 * q + 1], h1, l1);
+        h[q] = uint32_t(h0) | (uint32_t(h1) << 16);
+        l[q] = uint32_t(l0) | (uint32_t(l1) << 16);
+      }
+      const uint32_t o = canon_off(ch, t8, kChunk) / 2;  // 16-byte aligned: t8 % 8 == 0
+      *reinterpret_cast<uint4 *>(tr_hi + o) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4 *>(tr_lo + o) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -98,8 +160,9 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
 #pragma unroll
     for (int i = 0; i < kHist; ++i) {
       const int t = t0 - kHist + i;
-      hv[i] = t >= 0 ? bf2f(p.x[(size_t(b) * L + t) * C + c])
-                     : bf2f(p.ring[(size_t(b) * R + ring_slot(off + t, R)) * C + c]);
+      hv[i] = t >= L ? 0.f  // the padding chunk past the prompt
+              : t >= 0 ? bf2f(p.x[(size_t(b) * L + t) * C + c])
+                       : bf2f(p.ring[(size_t(b) * R + ring_slot(off + t, R)) * C + c]);
     }
     h0 = hv[0], h1 = hv[1], h2 = hv[2];
   }
@@ -116,8 +179,13 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
     h0 = h1, h1 = h2, h2 = xt;
   }
   const size_t Lp = size_t(p.NC) * kChunk;
+  const size_t tile = size_t(kChunk) * D;  // elements per bf16 tile
   if (kind == 2) {
-    float *dst = p.v + ((size_t(b) * p.H_v + (head - 2 * H_k)) * Lp + t0) * D + tid;
+    const int hv = head - 2 * H_k;
+    const size_t tbase = ((size_t(b) * p.H_v + hv) * p.NCp + chunk) * tile;
+    store_tiles<D>(y, tid, nullptr, nullptr, p.vt_hi + tbase, p.vt_lo + tbase);
+    if (chunk >= p.NC) return;
+    float *dst = p.v + ((size_t(b) * p.H_v + hv) * Lp + t0) * D + tid;
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) dst[size_t(i) * D] = y[i];
     return;
@@ -140,149 +208,286 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
   }
   __syncthreads();
   const int hk = kind == 0 ? head : head - H_k;
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) y[i] *= s_inv[i];
+  const size_t tbase = ((size_t(b) * H_k + hk) * p.NCp + chunk) * tile;
+  if (kind == 0)
+    store_tiles<D>(y, tid, p.qn_hi + tbase, p.qn_lo + tbase, nullptr, nullptr);
+  else
+    store_tiles<D>(y, tid, p.kn_hi + tbase, p.kn_lo + tbase, p.kt_hi + tbase, p.kt_lo + tbase);
+  if (chunk >= p.NC) return;
   float *dst = (kind == 0 ? p.q : p.k) + ((size_t(b) * H_k + hk) * Lp + t0) * D + tid;
 #pragma unroll
-  for (int i = 0; i < kChunk; ++i) dst[size_t(i) * D] = y[i] * s_inv[i];
+  for (int i = 0; i < kChunk; ++i) dst[size_t(i) * D] = y[i];
 }
 
 // ---------------------------------------------------------------------------
-// 2. per (chunk, value head): G, A, the UT transform Tm = (I + A)^-1, W, U, Pm.
-//    256 threads; K, Q, V tiles of the chunk in shared memory.
+// 2. per (pair of chunks, value head): G, A, Tm = (I + A)^-1, W, U, Pm, with
+//    the four products on the tensor cores (tcgen05, accumulators in TMEM).
+//
+//    Two consecutive 64-token chunks are stacked so every product has M = 128:
+//      KK = K K^T and QK = Q K^T   (128 x 128, K dim d)   -> A and Pm of each
+//                                   chunk are the diagonal 64 x 64 blocks
+//      W  = (Tm diag(beta gamma)) K,  U = (Tm diag(beta)) V  (128 x d, K dim
+//           128 tokens; Tm is block diagonal, so the chunks stay separate)
+//    Each product is taken in three bf16 passes, x = x_hi + x_lo with
+//    x_hi = bf16(x), x_lo = bf16(x - x_hi):  a b ~ a_hi b_hi + a_hi b_lo +
+//    a_lo b_hi, which keeps about 16 bits of the fp32 operands (the state
+//    tolerance is 1e-3 relative; a single bf16 pass would sit at that level).
+//    The UT transform itself is a forward substitution on the CUDA cores:
+//    each thread solves one column of one chunk's Tm, without block barriers.
 // ---------------------------------------------------------------------------
-constexpr int kChunkThreads = 256;
-constexpr int kPad = kChunk + 1;
+constexpr int kPairRows = 2 * kChunk;  // M of every product
+constexpr int kTcThreads = 128;        // thread t <-> TMEM lane t <-> token t of the pair
+constexpr uint32_t kTmemCols = 256;    // [0,128): KK then W; [128,256): QK then U
 
 template <int D>
-struct ChunkSmem {
-  float K[kChunk][D];
-  float Q[kChunk][D];
-  float V[kChunk][D];
-  float A[kChunk][kPad];
-  float Tm[kChunk][kPad];
-  float G[kChunk];
-  float bt[kChunk];
+struct TcLayout {
+  static constexpr uint32_t nat_pair = 2u * kChunk * D * 2;       // a [t][i] tile pair, one of hi/lo
+  static constexpr uint32_t tr_tile = uint32_t(D) * kChunk * 2;    // one [i][t] tile
+  static constexpr uint32_t sq_op = kPairRows * kPairRows * 2;     // a 128 x 128 bf16 operand
+  static constexpr uint32_t R0 = 0, R1 = 65536, R2 = 131072, R3 = 196608;
+  static constexpr uint32_t solve_bytes = 2 * kChunk * (kChunk + 1) * 4;
+  static constexpr uint32_t misc = R3 + solve_bytes;              // G[128], beta[128]
+  static constexpr uint32_t total = misc + 2 * kPairRows * 4;
+  static_assert(2 * nat_pair <= 65536 && 4 * tr_tile <= 65536 && 2 * sq_op <= 65536, "regions");
 };
 
 template <int D>
-__global__ void __launch_bounds__(kChunkThreads) prefill_chunk_kernel(const PrefillParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  ChunkSmem<D> &sm = *reinterpret_cast<ChunkSmem<D> *>(smem_raw);
-  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
-  pdl_wait();
-  pdl_trigger();
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const PrefillParams p) {
+  using Lay = TcLayout<D>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bars[6];
+  __shared__ uint32_t s_tmem;
+  __shared__ float s_wsum[4];
+  float(*As)[kChunk][kChunk + 1] = reinterpret_cast<float(*)[kChunk][kChunk + 1]>(smem + Lay::R3);
+  float *sG = reinterpret_cast<float *>(smem + Lay::misc);
+  float *sBeta = sG + kPairRows;
+
+  const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H_v = p.H_v, H_k = p.H_k, L = p.L;
   const int hk = h / (H_v / H_k);
+  const int c0 = 2 * pair;
   const size_t Lp = size_t(p.NC) * kChunk;
-  const int t0 = chunk * kChunk;
-  const int n = min(kChunk, L - t0);
-  const float *Kg = p.k + ((size_t(b) * H_k + hk) * Lp + t0) * D;
-  const float *Qg = p.q + ((size_t(b) * H_k + hk) * Lp + t0) * D;
-  const float *Vg = p.v + ((size_t(b) * H_v + h) * Lp + t0) * D;
-  for (int i = tid; i < kChunk * D / 4; i += kChunkThreads) {
-    reinterpret_cast<float4 *>(&sm.K[0][0])[i] = reinterpret_cast<const float4 *>(Kg)[i];
-    reinterpret_cast<float4 *>(&sm.Q[0][0])[i] = reinterpret_cast<const float4 *>(Qg)[i];
-    reinterpret_cast<float4 *>(&sm.V[0][0])[i] = reinterpret_cast<const float4 *>(Vg)[i];
-  }
-  if (tid < 32) {
-    // within-chunk cumulative log-decay (two tokens per lane, warp scan)
-    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-    const int ta = 2 * tid, tb = 2 * tid + 1;
-    if (ta < n) g0 = p.g[(size_t(b) * L + t0 + ta) * H_v + h], b0 = p.beta[(size_t(b) * L + t0 + ta) * H_v + h];
-    if (tb < n) g1 = p.g[(size_t(b) * L + t0 + tb) * H_v + h], b1 = p.beta[(size_t(b) * L + t0 + tb) * H_v + h];
-    float pair = g0 + g1;
-    float incl = pair;
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const float o = __shfl_up_sync(0xffffffffu, incl, m);
-      if (tid >= m) incl += o;
-    }
-    const float excl = incl - pair;
-    sm.G[ta] = excl + g0;
-    sm.G[tb] = excl + g0 + g1;
-    sm.bt[ta] = b0;
-    sm.bt[tb] = b1;
-  }
-  __syncthreads();
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t lane_base = uint32_t(warp * 32) << 16;  // this warp's TMEM lanes
 
-  // A (strictly lower, decay- and beta-weighted K K^T) and Pm (lower incl.
-  // diagonal, decay-weighted Q K^T).  Each thread: a 4 x 4 block of (t, s).
-  float *Pg = p.Pm + ((size_t(b) * H_v + h) * p.NC + chunk) * kChunk * kChunk;
-  {
-    const int tb = (tid / 16) * 4, sb = (tid % 16) * 4;
-    float kk[4][4] = {}, qk[4][4] = {};
-    for (int i = 0; i < D; i += 4) {
-      float4 kt[4], qt[4], ks[4];
+  if (tid == 0) {
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        kt[a] = *reinterpret_cast<const float4 *>(&sm.K[tb + a][i]);
-        qt[a] = *reinterpret_cast<const float4 *>(&sm.Q[tb + a][i]);
-        ks[a] = *reinterpret_cast<const float4 *>(&sm.K[sb + a][i]);
+    for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
+  pdl_wait();
+  pdl_trigger();
+
+  const size_t tile_el = size_t(kChunk) * D;
+  if (tid == 0) {
+    const size_t kq = ((size_t(b) * H_k + hk) * p.NCp + c0) * tile_el;
+    mbar_arrive_expect_tx(&bars[0], 4 * Lay::nat_pair);
+    bulk_g2s(smem + Lay::R0, p.kn_hi + kq, Lay::nat_pair, &bars[0]);
+    bulk_g2s(smem + Lay::R0 + Lay::nat_pair, p.kn_lo + kq, Lay::nat_pair, &bars[0]);
+    bulk_g2s(smem + Lay::R1, p.qn_hi + kq, Lay::nat_pair, &bars[0]);
+    bulk_g2s(smem + Lay::R1 + Lay::nat_pair, p.qn_lo + kq, Lay::nat_pair, &bars[0]);
+    mbar_arrive_expect_tx(&bars[1], 4 * Lay::tr_tile);
+    bulk_g2s(smem + Lay::R2, p.kt_hi + kq, 2 * Lay::tr_tile, &bars[1]);
+    bulk_g2s(smem + Lay::R2 + 2 * Lay::tr_tile, p.kt_lo + kq, 2 * Lay::tr_tile, &bars[1]);
+  }
+
+  // within-chunk cumulative log-decay: threads 0-63 scan chunk c0, 64-127 chunk c0+1
+  const int tok = c0 * kChunk + tid;
+  float gt = 0.f, bt = 0.f;
+  if (tok < L) {
+    gt = p.g[(size_t(b) * L + tok) * H_v + h];
+    bt = p.beta[(size_t(b) * L + tok) * H_v + h];
+  }
+  float incl = gt;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, incl, m);
+    if (lane >= m) incl += o;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  tc_fence_before();
+  __syncthreads();  // barriers, TMEM address, warp sums
+  tc_fence_after();
+  if (warp & 1) incl += s_wsum[warp - 1];
+  sG[tid] = incl;
+  sBeta[tid] = bt;
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+
+  // ---- phase 1: KK and QK ---------------------------------------------------
+  constexpr int pa[3] = {0, 0, 1}, pb[3] = {0, 1, 0};  // (hi,hi), (hi,lo), (lo,hi)
+  if (tid == 0) {
+    if (!mbar_wait_bounded(&bars[0], 0)) {
+      ok = false;
+    } else {
+      tc_fence_after();
+      constexpr uint32_t idesc = umma_idesc_bf16(kPairRows, kPairRows);
+      constexpr uint32_t sbo = (D / 8) * 128;
+      const uint32_t aK[2] = {sbase + Lay::R0, sbase + Lay::R0 + Lay::nat_pair};
+      const uint32_t aQ[2] = {sbase + Lay::R1, sbase + Lay::R1 + Lay::nat_pair};
+#pragma unroll
+      for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_bf16(tmem, umma_desc(aK[pa[ps]] + k * 256, 128, sbo), umma_desc(aK[pb[ps]] + k * 256, 128, sbo),
+                    idesc, ps | k);
+#pragma unroll
+      for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_bf16(tmem + 128, umma_desc(aQ[pa[ps]] + k * 256, 128, sbo),
+                    umma_desc(aK[pb[ps]] + k * 256, 128, sbo), idesc, ps | k);
+    }
+    umma_commit(&bars[2]);  // also arrives when nothing was issued
+  }
+  ok = mbar_wait_bounded(&bars[2], 0) && ok;
+  tc_fence_after();
+  __syncthreads();  // sG / sBeta of every token are visible
+
+  // ---- epilogue 1: A (strictly lower, beta- and decay-weighted KK) and Pm ---
+  const int q = tid >> 6, tl = tid & (kChunk - 1);  // chunk in the pair, row in the chunk
+  const int chunk = c0 + q;
+  if (ok) {
+    const float Gt = sG[tid], bq = sBeta[tid];
+    const int cb = q * kChunk;
+    float *Pg = p.Pm + (((size_t(b) * H_v + h) * p.NC + chunk) * kChunk + tl) * kChunk;
+#pragma unroll
+    for (int cc = 0; cc < kChunk; cc += 32) {
+      float kk[32], qk[32];
+      tmem_ld32(tmem + lane_base + cb + cc, kk);
+      tmem_ld32(tmem + lane_base + 128 + cb + cc, qk);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int sl = cc + j;
+        const float decay = sl <= tl ? expf(Gt - sG[cb + sl]) : 0.f;
+        As[q][tl][sl] = sl < tl ? bq * decay * kk[j] : 0.f;
+        if (chunk < p.NC) Pg[sl] = decay * qk[j];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- UT transform: column s of chunk q of Tm, by forward substitution ----
+  if (ok) {
+    const int s = tl;
+    float x[kChunk];
+#pragma unroll
+    for (int r = 0; r < kChunk; ++r) {
+      float a0 = r == s ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int u = 0; u + 3 < r; u += 4) {
+        a0 = fmaf(-As[q][r][u], x[u], a0);
+        a1 = fmaf(-As[q][r][u + 1], x[u + 1], a1);
+        a2 = fmaf(-As[q][r][u + 2], x[u + 2], a2);
+        a3 = fmaf(-As[q][r][u + 3], x[u + 3], a3);
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int u = r & ~3; u < r; ++u) a0 = fmaf(-As[q][r][u], x[u], a0);
+      x[r] = (a0 + a1) + (a2 + a3);
+    }
+    // operands of W and U: Tm scaled by beta_s gamma_s (resp. beta_s) per
+    // column, block diagonal over the pair, split into bf16 hi/lo
+    const int ks = q * kChunk + s, kz = (1 - q) * kChunk + s;
+    const float bs = sBeta[ks], bgs = bs * expf(sG[ks]);
+    uint16_t *awh = reinterpret_cast<uint16_t *>(smem + Lay::R0), *awl = awh + kPairRows * kPairRows;
+    uint16_t *auh = reinterpret_cast<uint16_t *>(smem + Lay::R1), *aul = auh + kPairRows * kPairRows;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          kk[a][c] += dot4(kt[a], ks[c]);
-          qk[a][c] += dot4(qt[a], ks[c]);
+    for (int r = 0; r < kChunk; ++r) {
+      const int tr = q * kChunk + r;
+      uint16_t hi, lo;
+      const uint32_t o = canon_off(tr, ks, kPairRows) / 2, oz = canon_off(tr, kz, kPairRows) / 2;
+      split_bf16(x[r] * bgs, hi, lo);
+      awh[o] = hi, awl[o] = lo;
+      split_bf16(x[r] * bs, hi, lo);
+      auh[o] = hi, aul[o] = lo;
+      awh[oz] = 0, awl[oz] = 0, auh[oz] = 0, aul[oz] = 0;
+    }
+  }
+  fence_async_smem();  // generic-proxy writes above -> tensor-core reads below
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- phase 2: W = A_W K (via K^T tiles), U = A_U V (via V^T tiles) -------
+  if (tid == 0) {
+    bool issued = false;
+    if (ok && mbar_wait_bounded(&bars[1], 0)) {
+      tc_fence_after();
+      constexpr uint32_t idesc = umma_idesc_bf16(kPairRows, D);
+      constexpr uint32_t sbo_a = (kPairRows / 8) * 128, sbo_t = (kChunk / 8) * 128;
+      const uint32_t aW[2] = {sbase + Lay::R0, sbase + Lay::R0 + Lay::sq_op};
+      const uint32_t aU[2] = {sbase + Lay::R1, sbase + Lay::R1 + Lay::sq_op};
+      const uint32_t bT[2] = {sbase + Lay::R2, sbase + Lay::R2 + 2 * Lay::tr_tile};
+#pragma unroll
+      for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+        for (int k = 0; k < kPairRows / 16; ++k)
+          umma_bf16(tmem, umma_desc(aW[pa[ps]] + k * 256, 128, sbo_a),
+                    umma_desc(bT[pb[ps]] + (k / 4) * Lay::tr_tile + (k % 4) * 256, 128, sbo_t), idesc, ps | k);
+      umma_commit(&bars[3]);
+      issued = true;
+      // the K^T tiles are free once W is done: bring in V^T
+      if (mbar_wait_bounded(&bars[3], 0)) {
+        const size_t vq = ((size_t(b) * H_v + h) * p.NCp + c0) * tile_el;
+        mbar_arrive_expect_tx(&bars[4], 4 * Lay::tr_tile);
+        bulk_g2s(smem + Lay::R2, p.vt_hi + vq, 2 * Lay::tr_tile, &bars[4]);
+        bulk_g2s(smem + Lay::R2 + 2 * Lay::tr_tile, p.vt_lo + vq, 2 * Lay::tr_tile, &bars[4]);
+        if (mbar_wait_bounded(&bars[4], 0)) {
+          tc_fence_after();
+#pragma unroll
+          for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+            for (int k = 0; k < kPairRows / 16; ++k)
+              umma_bf16(tmem + 128, umma_desc(aU[pa[ps]] + k * 256, 128, sbo_a),
+                        umma_desc(bT[pb[ps]] + (k / 4) * Lay::tr_tile + (k % 4) * 256, 128, sbo_t), idesc,
+                        ps | k);
         }
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int t = tb + a, s = sb + c;
-        const bool valid = t < n && s < n;
-        const float decay = valid && s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
-        sm.A[t][s] = s < t ? sm.bt[t] * decay * kk[a][c] : 0.f;
-        Pg[t * kChunk + s] = s <= t ? decay * qk[a][c] : 0.f;
       }
+      umma_commit(&bars[5]);
+    }
+    if (!issued) {  // let the waiting threads through
+      umma_commit(&bars[3]);
+      umma_commit(&bars[5]);
+    }
   }
+
+  // ---- epilogue 2: W and U rows (fp32) for the state pass; decay -----------
+  const bool okw = mbar_wait_bounded(&bars[3], 0) && ok;
+  tc_fence_after();
+  if (okw && chunk < p.NC) {
+    float *Wg = p.W + ((size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl) * D;
+#pragma unroll
+    for (int cc = 0; cc < D; cc += 32) {
+      float v[32];
+      tmem_ld32(tmem + lane_base + cc, v);
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) st_f4(Wg + cc + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+    }
+    p.Gc[(size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl] = sG[tid];
+  }
+  const bool oku = mbar_wait_bounded(&bars[5], 0) && okw;
+  tc_fence_after();
+  if (oku && chunk < p.NC) {
+    float *Ug = p.U + ((size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl) * D;
+#pragma unroll
+    for (int cc = 0; cc < D; cc += 32) {
+      float v[32];
+      tmem_ld32(tmem + lane_base + 128 + cc, v);
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) st_f4(Ug + cc + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+    }
+  }
+  if (!oku && lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
+  tc_fence_before();
   __syncthreads();
-
-  // Tm = (I + A)^-1 by forward substitution, one row at a time:
-  // Tm[t][s] = [t == s] - sum_{s <= r < t} A[t][r] Tm[r][s].
-  for (int t = 0; t < kChunk; ++t) {
-    if (tid < kChunk) {
-      const int s = tid;
-      float acc = s == t ? 1.f : 0.f;
-      if (s < t)
-        for (int r = s; r < t; ++r) acc = fmaf(-sm.A[t][r], sm.Tm[r][s], acc);
-      sm.Tm[t][s] = s <= t ? acc : 0.f;
-    }
-    __syncthreads();
-  }
-
-  // W = Tm diag(beta gamma) K and U = Tm diag(beta) V.  Each thread: 2 rows
-  // t and 16 columns.
-  {
-    float *Wg = p.W + ((size_t(b) * H_v + h) * Lp + t0) * D;
-    float *Ug = p.U + ((size_t(b) * H_v + h) * Lp + t0) * D;
-    constexpr int CPT = D * kChunk / kChunkThreads;  // outputs per thread per matrix
-    const int col0 = (tid % (D / 4)) * 4;
-    const int rowg = tid / (D / 4);
-    constexpr int ROWS_PER = kChunk / (kChunkThreads / (D / 4));
-    static_assert(ROWS_PER * 4 == CPT, "thread tiling");
-#pragma unroll
-    for (int rr = 0; rr < ROWS_PER; ++rr) {
-      const int t = rowg * ROWS_PER + rr;
-      float4 aw = make_float4(0.f, 0.f, 0.f, 0.f), au = aw;
-      for (int s = 0; s <= t && s < n; ++s) {
-        const float tm = sm.Tm[t][s] * sm.bt[s];
-        const float tw = tm * expf(sm.G[s]);
-        const float4 kv = *reinterpret_cast<const float4 *>(&sm.K[s][col0]);
-        const float4 vv = *reinterpret_cast<const float4 *>(&sm.V[s][col0]);
-        aw.x = fmaf(tw, kv.x, aw.x), aw.y = fmaf(tw, kv.y, aw.y), aw.z = fmaf(tw, kv.z, aw.z),
-        aw.w = fmaf(tw, kv.w, aw.w);
-        au.x = fmaf(tm, vv.x, au.x), au.y = fmaf(tm, vv.y, au.y), au.z = fmaf(tm, vv.z, au.z),
-        au.w = fmaf(tm, vv.w, au.w);
-      }
-      if (t >= n) aw = au = make_float4(0.f, 0.f, 0.f, 0.f);
-      st_f4(Wg + size_t(t) * D + col0, aw);
-      st_f4(Ug + size_t(t) * D + col0, au);
-    }
-  }
-  if (tid < kChunk) p.Gc[(size_t(b) * H_v + h) * Lp + t0 + tid] = tid < n ? sm.G[tid] : 0.f;
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -423,27 +628,27 @@ __global__ void prefill_ring_kernel(const PrefillParams p) {
 template <int D>
 static cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream) {
   cudaError_t e;
-  e = launch_pdl(prefill_conv_kernel<D>, dim3(p.NC, 2 * p.H_k + p.H_v, p.B), dim3(D), stream, p);
+  e = launch_pdl(prefill_conv_kernel<D>, dim3(p.NCp, 2 * p.H_k + p.H_v, p.B), dim3(D), stream, p);
   if (e != cudaSuccess) return e;
   // the ring update must follow the conv (which reads the old window) and
   // precede the state pass (which advances offsets)
   e = launch_pdl(prefill_ring_kernel, dim3((p.C + 255) / 256, p.B), dim3(256), stream, p);
   if (e != cudaSuccess) return e;
-  const size_t chunk_smem = sizeof(ChunkSmem<D>);
-  e = cudaFuncSetAttribute(prefill_chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(chunk_smem));
+  e = cudaFuncSetAttribute(prefill_chunk_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(TcLayout<D>::total));
   if (e != cudaSuccess) return e;
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.NC, p.H_v, p.B);
-    cfg.blockDim = dim3(kChunkThreads);
-    cfg.dynamicSmemBytes = chunk_smem;
+    cfg.gridDim = dim3(p.NCp / 2, p.H_v, p.B);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcLayout<D>::total;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_chunk_kernel<D>, p);
+    e = cudaLaunchKernelEx(&cfg, prefill_chunk_tc_kernel<D>, p);
     if (e != cudaSuccess) return e;
   }
   const size_t state_smem = sizeof(StateSmem<D>);
@@ -483,7 +688,18 @@ cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g,
   p.U = reinterpret_cast<float *>(base + l.U);
   p.Gc = reinterpret_cast<float *>(base + l.Gc);
   p.Pm = reinterpret_cast<float *>(base + l.Pm);
+  p.qn_hi = reinterpret_cast<uint16_t *>(base + l.qn_hi);
+  p.qn_lo = reinterpret_cast<uint16_t *>(base + l.qn_lo);
+  p.kn_hi = reinterpret_cast<uint16_t *>(base + l.kn_hi);
+  p.kn_lo = reinterpret_cast<uint16_t *>(base + l.kn_lo);
+  p.kt_hi = reinterpret_cast<uint16_t *>(base + l.kt_hi);
+  p.kt_lo = reinterpret_cast<uint16_t *>(base + l.kt_lo);
+  p.vt_hi = reinterpret_cast<uint16_t *>(base + l.vt_hi);
+  p.vt_lo = reinterpret_cast<uint16_t *>(base + l.vt_lo);
   p.B = B, p.L = L, p.NC = (L + kChunk - 1) / kChunk, p.H_k = H_k, p.H_v = H_v;
+  p.NCp = (p.NC + 1) & ~1;
+  p.status = status_word_address();
+  if (!p.status) return cudaErrorInvalidValue;
   p.C = (2 * H_k + H_v) * D, p.R = R, p.act = act;
   switch (D) {
     case 32: return launch_prefill_d<32>(p, stream);
