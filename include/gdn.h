@@ -103,12 +103,15 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
 /* flag OR-ed into the mode argument of gdn_conv_verify.  Every kernel of
  * the library is launched with programmatic dependent launch and waits for
  * the preceding kernel on the stream before reading anything it may write.
- * With GDN_VERIFY_OVERLAP the caller also guarantees that the work issued
- * immediately before this call on the stream writes none of this call's
- * `state`, `ring`, `active` and `conv_w`; the kernel then stages its state
- * tiles while that work is still finishing.  Do not pass it to the first
- * verify after gdn_commit, gdn_prefill_chunked or any other write of these
- * buffers; it is always safe to omit. */
+ * With GDN_VERIFY_OVERLAP the call's kernel also lets the next kernel on the
+ * stream start as soon as it has started, and stages its own state tiles
+ * before waiting for its predecessor, so consecutive flagged verifies stream
+ * their state ahead of one another.  The caller guarantees that no work
+ * issued since the last library call made WITHOUT the flag writes this
+ * call's `state`, `ring`, `active` or `conv_w`.  In a verify cycle over a
+ * layer stack that means: flag every layer but the first one after
+ * gdn_commit, gdn_prefill_chunked or any other write of these buffers.  It is
+ * always safe to omit. */
 #define GDN_VERIFY_OVERLAP 0x100
 
 /* sticky device status bits (gdn_get_status) */

@@ -1,15 +1,14 @@
 // verify.cuh -- the fused conv + L2-norm + gated-delta-rule verify kernel.
 //
-// Work decomposition.  A CTA of 4 warps owns 32 state rows (d_v) of one
-// (row b, value head h).  Its state tile (32 contiguous rows) is staged in
-// shared memory by one bulk copy on the TMA engine issued at entry.  The q/k
-// conv of the key head is split over the CTA's threads and exchanged through
-// shared memory at the kernel's one block barrier; after it every warp owns 8
-// rows and works alone.  Lane l works on the d_k segment [4*(l % LPR), +4) of
-// its rows.  Every global load (state tile, conv window, new inputs, taps,
-// gates) is issued before the barrier, so the critical path is one memory
-// round trip plus a few hundred instructions per warp, which is what a
-// one-wave kernel of a few microseconds needs.
+// Work decomposition.  One CTA of 2*d threads owns one (row b, value head h):
+// its whole d_v x d_k state (64 KiB at d = 128) is staged in shared memory by
+// d/32 bulk copies on the TMA engine, issued at entry, each completing on its
+// own mbarrier.  Each thread convolves one q or k channel of the key head;
+// the conv outputs are exchanged at the kernel's one block barrier, after
+// which every warp owns 16 state rows (two groups of 8) and works alone.
+// Lane l works on the d_k segment [4*(l % LPR), +4) of its rows.  A layer
+// occupies about 1.3 CTAs per SM at B = 8, so with GDN_VERIFY_OVERLAP the next
+// layer's CTAs fit beside it and stream their state while this one computes.
 //
 // The pre-verification state S_0 is only read ("MTP inference: review and
 // commit structure", Functional commits item 2: speculative transactions with
@@ -97,93 +96,107 @@ __device__ __forceinline__ void conv_channel(const VerifyParams &p, int b, int c
   }
 }
 
+// Shared memory of one verify CTA: the (row, head) state tile and the conv
+// outputs of its key head.
+template <int D, int T>
+struct VerifySmem {
+  float S[D * D];
+  float q[T][D];
+  float k[T][D];
+  uint64_t bar[D / kTileRows];
+};
+
 template <int D, int T, int MODE>
-__global__ void __launch_bounds__(kVerifyThreads, T <= 2 ? 6 : 1) verify_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const VerifyParams p) {
   using G = RowLanes<D>;
   constexpr int RPL = G::RPL, GPW = G::GPW, LPR = G::LPR;
+  constexpr int NT = D / kTileRows;   // 32-row tiles, one bulk copy and barrier each
   // per-head reductions: |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t)
   constexpr int NKK = T * (T - 1) / 2, NKQ = T * (T + 1) / 2, NV = 2 * T + NKK + NKQ;
 
-  __shared__ __align__(128) float sS[kTileRows * D];
-  __shared__ __align__(16) float sq[T][D];
-  __shared__ __align__(16) float sk[T][D];
-  __shared__ __align__(8) uint64_t sbar;
+  extern __shared__ __align__(128) unsigned char vsm_raw[];
+  VerifySmem<D, T> &sm = *reinterpret_cast<VerifySmem<D, T> *>(vsm_raw);
 
-  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane % LPR, grp = lane / LPR;
   const int H_v = p.H_v, H_k = p.H_k, R = p.R;
   const int rep = H_v / H_k;
   const int hk = h / rep;
-  const int jw = tile * kTileRows + warp * 8;  // first state row of this warp
-  const int istar = row_of_lane<D>(lane);      // row this lane holds after the reduction
-  const int jrow = jw + grp + GPW * istar;
-  const bool leader = (lane & 3) == 0;         // four lanes share a row after the reduction
+  const int istar = row_of_lane<D>(lane);  // row (within a group of 8) this lane holds after a reduction
+  const bool leader = (lane & 3) == 0;     // four lanes share a row after the reduction
 
-  // With GDN_VERIFY_OVERLAP the caller guarantees that the preceding work on
-  // the stream writes none of this call's state, ring, active mask or taps, so
-  // the state tile is staged before waiting for that work; otherwise
-  // everything waits first.
-  if (!p.overlap) {
+  // With GDN_VERIFY_OVERLAP the caller guarantees that nothing issued since
+  // the last call without the flag writes this call's state, ring, active
+  // mask or taps: the kernel lets the next kernel start at once and stages its
+  // state tiles before waiting for the preceding one.  Without the flag it
+  // waits first and only then lets the next kernel start, so a chain of
+  // flagged verifies can never run ahead of the last unflagged call.
+  if (p.overlap) {
+    pdl_trigger();
+  } else {
     pdl_wait();
     pdl_trigger();
   }
   if (!p.active[b]) {
     // Inactive / padding / finished rows are inert: zero output, no state,
     // ring or workspace access.
-    if (p.overlap) {
-      pdl_wait();
-      pdl_trigger();
-    }
-    if (leader)
-#pragma unroll
-      for (int t = 0; t < T; ++t) p.out[((size_t(b) * T + t) * H_v + h) * D + jrow] = 0;
+    if (p.overlap) pdl_wait();
+    for (int i = tid; i < T * D; i += 2 * D)
+      p.out[((size_t(b) * T + i / D) * H_v + h) * D + i % D] = 0;
     return;
   }
 
-  // ---- 1. stage the state tile (bulk copy on the TMA engine) ----------------
+  // ---- 1. stage the (row, head) state, 32 rows per bulk copy ----------------
   constexpr uint32_t kTileBytes = kTileRows * D * sizeof(float);
   if (tid == 0) {
-    mbar_init(&sbar, 1);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) mbar_init(&sm.bar[i], 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&sbar, kTileBytes);
-    bulk_g2s(sS, p.state + ((size_t(b) * H_v + h) * D + size_t(tile) * kTileRows) * D, kTileBytes, &sbar);
+    const float *src = p.state + (size_t(b) * H_v + h) * D * D;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      mbar_arrive_expect_tx(&sm.bar[i], kTileBytes);
+      bulk_g2s(sm.S + i * kTileRows * D, src + size_t(i) * kTileRows * D, kTileBytes, &sm.bar[i]);
+    }
   }
-  if (p.overlap) {
-    pdl_wait();
-    pdl_trigger();
-  }
+  if (p.overlap) pdl_wait();
 
-  // ---- 2. conv + activation: q/k channels of the key head split over the CTA,
-  //         the v channel of each lane's row done by the lanes of that row ----
+  // ---- 2. conv + activation: one q or k channel of the key head per thread --
   const int off = p.offsets[b];
   const int slot0 = ring_slot(off - kHist, R);
   const int wslot0 = ring_slot(off, R);
-  const bool qk_writer = (tile == 0) && (h % rep == 0);  // one CTA per key head writes its q/k ring slots
-  for (int c2 = tid; c2 < 2 * D; c2 += kVerifyThreads) {
-    const bool is_k = c2 >= D;
-    const int ch = is_k ? c2 - D : c2;
-    const int c = (is_k ? H_k * D : 0) + hk * D + ch;
+  const bool qk_writer = (h % rep) == 0;  // one CTA per key head writes its q/k ring slots
+  {
+    const bool is_k = tid >= D;
+    const int ch = is_k ? tid - D : tid;
     float y[T];
-    conv_channel<T>(p, b, c, slot0, wslot0, qk_writer, y);
+    conv_channel<T>(p, b, (is_k ? H_k * D : 0) + hk * D + ch, slot0, wslot0, qk_writer, y);
 #pragma unroll
-    for (int t = 0; t < T; ++t) (is_k ? sk : sq)[t][ch] = y[t];
+    for (int t = 0; t < T; ++t) (is_k ? sm.k : sm.q)[t][ch] = y[t];
   }
-  float v[T];
-  conv_channel<T>(p, b, 2 * H_k * D + h * D + jrow, slot0, wslot0, leader, v);
   float gt[T], bt[T];
 #pragma unroll
   for (int t = 0; t < T; ++t) {
     gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
     bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
   }
-  __syncthreads();  // conv outputs and the initialised barrier are visible
+  // the v channels of the two rows this lane will hold, also before the barrier
+  // so their loads overlap the state copy
+  constexpr int ROWS_W = 16;  // state rows per warp: two groups of 8
+  const int jw0 = warp * ROWS_W;
+  float vrow[ROWS_W / 8][T];
+#pragma unroll
+  for (int grp8 = 0; grp8 < ROWS_W / 8; ++grp8)
+    conv_channel<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, slot0, wslot0, leader,
+                    vrow[grp8]);
+  __syncthreads();  // conv outputs and the initialised barriers are visible
 
   float q[T][4], k[T][4];
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    const float4 qv = *reinterpret_cast<const float4 *>(&sq[t][4 * sub]);
-    const float4 kv = *reinterpret_cast<const float4 *>(&sk[t][4 * sub]);
+    const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
+    const float4 kv = *reinterpret_cast<const float4 *>(&sm.k[t][4 * sub]);
     q[t][0] = qv.x, q[t][1] = qv.y, q[t][2] = qv.z, q[t][3] = qv.w;
     k[t][0] = kv.x, k[t][1] = kv.y, k[t][2] = kv.z, k[t][3] = kv.w;
   }
@@ -213,31 +226,7 @@ __global__ void __launch_bounds__(kVerifyThreads, T <= 2 ? 6 : 1) verify_kernel(
 #pragma unroll
     for (int i = 0; i < NV; ++i) red_h[i] += __shfl_xor_sync(0xffffffffu, red_h[i], m);
 
-  // ---- 4. the 2T dot products of every state row with S_0 (raw q/k) -------
-  if (!mbar_wait_bounded(&sbar, 0)) {
-    // The staged tile never arrived: flag it, give the copy one more bounded
-    // wait so it does not land in a retired CTA's shared memory, and write
-    // nothing for this tile.
-    if (lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
-    mbar_wait_bounded(&sbar, 0);
-    return;
-  }
-  float4 s[RPL];
-#pragma unroll
-  for (int i = 0; i < RPL; ++i)
-    s[i] = *reinterpret_cast<const float4 *>(&sS[(warp * 8 + grp + GPW * i) * D + 4 * sub]);
-  float red[2 * T];
-#pragma unroll
-  for (int mvec = 0; mvec < 2 * T; ++mvec) {
-    const float *vv = mvec < T ? k[mvec] : q[mvec - T];
-    const float4 vec = make_float4(vv[0], vv[1], vv[2], vv[3]);
-    float acc[RPL];
-#pragma unroll
-    for (int i = 0; i < RPL; ++i) acc[i] = dot4(s[i], vec);
-    red[mvec] = reduce_rows<D>(acc, lane);
-  }
-
-  // ---- 5. per-head coefficients (every lane, in registers) -----------------
+  // ---- 4. per-head coefficients (every lane, in registers) -----------------
   float inv_q[T], inv_k[T], Gc[T], gam[T];
   {
     const float qs = 1.0f / sqrtf(float(D));
@@ -251,87 +240,135 @@ __global__ void __launch_bounds__(kVerifyThreads, T <= 2 ? 6 : 1) verify_kernel(
       gam[t] = expf(acc);
     }
   }
+  float decay[T][T];  // exp(G_t - G_s), s < t
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+#pragma unroll
+    for (int s0 = 0; s0 < t; ++s0) decay[t][s0] = expf(Gc[t] - Gc[s0]);
 
-  // ---- 6. scalar recurrence for the row this lane holds --------------------
-  float e[T], o[T];
-  {
-    int nkk = 2 * T, nkq = 2 * T + NKK;
+  // ---- 5. this warp's 16 rows, in two groups of 8 ---------------------------
+  if (!mbar_wait_bounded(&sm.bar[jw0 / kTileRows], 0)) {
+    // The staged tile never arrived: flag it, give the copies one more bounded
+    // wait so they do not land in a retired CTA's shared memory, and write
+    // nothing for these rows.
+    if (lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-      float decay[T];  // exp(G_t - G_s), s < t
+    for (int i = 0; i < NT; ++i) mbar_wait_bounded(&sm.bar[i], 0);
+    return;
+  }
+  const size_t plane = size_t(p.B) * H_v * D * D;
 #pragma unroll
-      for (int s0 = 0; s0 < t; ++s0) decay[s0] = expf(Gc[t] - Gc[s0]);
-      float acc = fmaf(bt[t], v[t], -(bt[t] * gam[t]) * (red[t] * inv_k[t]));
+  for (int grp8 = 0; grp8 < ROWS_W / 8; ++grp8) {
+    const int jw = jw0 + 8 * grp8;  // first state row of this group
+    const int jrow = jw + grp + GPW * istar;
+    float4 s[RPL];
 #pragma unroll
-      for (int s0 = 0; s0 < t; ++s0) {
-        const float kk = red_h[nkk++] * inv_k[s0] * inv_k[t];
-        acc = fmaf(-(bt[t] * decay[s0] * kk), e[s0], acc);
+    for (int i = 0; i < RPL; ++i)
+      s[i] = *reinterpret_cast<const float4 *>(&sm.S[(jw + grp + GPW * i) * D + 4 * sub]);
+    float red[2 * T];
+#pragma unroll
+    for (int mvec = 0; mvec < 2 * T; ++mvec) {
+      const float *vv = mvec < T ? k[mvec] : q[mvec - T];
+      const float4 vec = make_float4(vv[0], vv[1], vv[2], vv[3]);
+      float acc[RPL];
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) acc[i] = dot4(s[i], vec);
+      red[mvec] = reduce_rows<D>(acc, lane);
+    }
+    const float *v = vrow[grp8];
+
+    // scalar recurrence for the row this lane holds
+    float e[T], o[T];
+    {
+      int nkk = 2 * T, nkq = 2 * T + NKK;
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        float acc = fmaf(bt[t], v[t], -(bt[t] * gam[t]) * (red[t] * inv_k[t]));
+#pragma unroll
+        for (int s0 = 0; s0 < t; ++s0) {
+          const float kk = red_h[nkk++] * inv_k[s0] * inv_k[t];
+          acc = fmaf(-(bt[t] * decay[t][s0] * kk), e[s0], acc);
+        }
+        e[t] = acc;
+        float ot = gam[t] * (red[T + t] * inv_q[t]);
+#pragma unroll
+        for (int s0 = 0; s0 <= t; ++s0) {
+          const float kq = red_h[nkq++] * inv_k[s0] * inv_q[t];
+          ot = fmaf((s0 == t ? 1.0f : decay[t][s0]) * kq, e[s0], ot);
+        }
+        o[t] = ot;
       }
-      e[t] = acc;
-      float ot = gam[t] * (red[T + t] * inv_q[t]);
+    }
+    if (leader) {
 #pragma unroll
-      for (int s0 = 0; s0 <= t; ++s0) {
-        const float kq = red_h[nkq++] * inv_k[s0] * inv_q[t];
-        ot = fmaf((s0 == t ? 1.0f : decay[s0]) * kq, e[s0], ot);
+      for (int t = 0; t < T; ++t) {
+        const size_t idx = ((size_t(b) * T + t) * H_v + h) * D + jrow;
+        p.out[idx] = f2bf(o[t]);
+        if (MODE == GDN_COMMIT_RECOMPUTE) p.ws_e[idx] = e[t];
       }
-      o[t] = ot;
+    }
+    if (MODE == GDN_COMMIT_SNAPSHOT) {
+      // every lane needs e_t of each of its rows; fetch them from the lane
+      // that computed them, then step the rows through S_t = a_t S_{t-1} + e_t k_t
+      float *snap = p.ws_snap + ((size_t(b) * H_v + h) * D + jw) * D;
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) {
+        const int src = grp * LPR + lane_of_row<D>(i);
+        float4 st = s[i];
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const float et = __shfl_sync(0xffffffffu, e[t], src);
+          const float a = expf(gt[t]);
+          st.x = fmaf(et, k[t][0] * inv_k[t], a * st.x);
+          st.y = fmaf(et, k[t][1] * inv_k[t], a * st.y);
+          st.z = fmaf(et, k[t][2] * inv_k[t], a * st.z);
+          st.w = fmaf(et, k[t][3] * inv_k[t], a * st.w);
+          st_f4(snap + t * plane + size_t(grp + GPW * i) * D + 4 * sub, st);
+        }
+      }
     }
   }
 
-  // ---- 7. outputs and captures ----------------------------------------------
-  if (leader) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const size_t idx = ((size_t(b) * T + t) * H_v + h) * D + jrow;
-      p.out[idx] = f2bf(o[t]);
-      if (MODE == GDN_COMMIT_RECOMPUTE) p.ws_e[idx] = e[t];
-    }
-  }
+  // ---- 6. captures of the key head and decay --------------------------------
   if (MODE == GDN_COMMIT_RECOMPUTE) {
     if (qk_writer && warp == 0 && grp == 0)
 #pragma unroll
       for (int t = 0; t < T; ++t)
         st_f4(p.ws_k + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub,
               make_float4(k[t][0] * inv_k[t], k[t][1] * inv_k[t], k[t][2] * inv_k[t], k[t][3] * inv_k[t]));
-    if (tile == 0 && warp == 0 && lane < T) {
+    if (warp == 0 && lane < T) {
 #pragma unroll
       for (int t = 0; t < T; ++t)
         if (lane == t) p.ws_G[(size_t(b) * T + t) * H_v + h] = Gc[t];
     }
-  } else {
-    // SNAPSHOT: every lane needs e_t of each of its rows; fetch them from the
-    // lane that computed them, then step the rows through S_t = a_t S_{t-1} + e_t k_t.
-    const size_t plane = size_t(p.B) * H_v * D * D;
-    float *snap = p.ws_snap + ((size_t(b) * H_v + h) * D + jw) * D;
-    float alpha[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) alpha[t] = expf(gt[t]);
-#pragma unroll
-    for (int i = 0; i < RPL; ++i) {
-      const int src = grp * LPR + lane_of_row<D>(i);
-      float4 st = s[i];
-#pragma unroll
-      for (int t = 0; t < T; ++t) {
-        const float et = __shfl_sync(0xffffffffu, e[t], src);
-        const float a = alpha[t];
-        st.x = fmaf(et, k[t][0] * inv_k[t], a * st.x);
-        st.y = fmaf(et, k[t][1] * inv_k[t], a * st.y);
-        st.z = fmaf(et, k[t][2] * inv_k[t], a * st.z);
-        st.w = fmaf(et, k[t][3] * inv_k[t], a * st.w);
-        st_f4(snap + t * plane + size_t(grp + GPW * i) * D + 4 * sub, st);
-      }
-    }
   }
+}
+
+// Launch one verify instantiation, raising its dynamic shared-memory limit on
+// the first launch of that instantiation on each device.
+template <int D, int T, int MODE>
+cudaError_t launch_verify_kernel(dim3 grid, dim3 block, cudaStream_t stream, const VerifyParams &p) {
+  static bool configured[64] = {false};  // one flag set per instantiation
+  constexpr int smem = int(sizeof(VerifySmem<D, T>));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(verify_kernel<D, T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  return launch_pdl_smem(verify_kernel<D, T, MODE>, grid, block, smem, stream, p);
 }
 
 template <int D>
 cudaError_t launch_verify_d(const VerifyParams &p, int T, int mode, cudaStream_t stream) {
-  const dim3 grid(D / kTileRows, p.H_v, p.B), block(kVerifyThreads);
-#define GDN_VERIFY_CASE(TT)                                                                     \
-  case TT:                                                                                      \
-    return mode == GDN_COMMIT_RECOMPUTE                                                         \
-               ? launch_pdl(verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>, grid, block, stream, p) \
-               : launch_pdl(verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>, grid, block, stream, p);
+  const dim3 grid(p.H_v, p.B), block(2 * D);
+#define GDN_VERIFY_CASE(TT)                                                            \
+  case TT:                                                                             \
+    return mode == GDN_COMMIT_RECOMPUTE                                                \
+               ? launch_verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>(grid, block, stream, p) \
+               : launch_verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>(grid, block, stream, p);
   switch (T) {
     GDN_VERIFY_CASE(1)
     GDN_VERIFY_CASE(2)
