@@ -13,7 +13,7 @@ the 480 MiB state stack is larger than the 129 MB L2, so no flush is needed.
 Each cycle is one captured CUDA graph of the C-ABI calls.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-        [--mode recompute|snapshot] [--B 8 --T 2 --layers 30] [--no-cpu-baseline]
+        [--mode recompute|snapshot|deferred] [--B 8 --T 2 --layers 30] [--no-cpu-baseline]
 Under torchrun (N > 1) every rank runs its own cohort (weak scaling, no
 collective on the data path) and rank 0 prints the max-over-ranks result.
 """
@@ -48,13 +48,16 @@ KERNEL_SOURCES = {
 }
 
 
+MODES = {"recompute": 0, "snapshot": 1, "deferred": 2}  # GDN_COMMIT_* of the C ABI
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1024)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="recompute", choices=["recompute", "snapshot"])
+    ap.add_argument("--mode", default="recompute", choices=list(MODES))
     ap.add_argument("--B", type=int, default=8)
     ap.add_argument("--T", type=int, default=2)
     ap.add_argument("--layers", type=int, default=30)
@@ -100,19 +103,42 @@ def state_row_bytes(geom):
     return geom.H_v * geom.d * geom.d * 4
 
 
-def verify_bytes(geom, n_active):
+def verify_bytes(geom, n_active, mode="recompute", n_apply=0):
     """Algorithmic bytes of one verify launch: state read once per active row,
-    raw inputs, taps, conv window read + new ring slots, gates, outputs."""
+    raw inputs, taps, conv window read + new ring slots, gates, outputs; in
+    SNAPSHOT mode the T snapshots written per active row; in DEFERRED mode the
+    committed state written back for the n_apply rows whose commit it applies."""
     C = geom.C
-    return (state_row_bytes(geom) * n_active + n_active * geom.T * C * 2 + C * 4 * 2
-            + n_active * (3 + geom.T) * C * 2 + n_active * geom.T * geom.H_v * 4 * 2
-            + geom.B * geom.T * geom.H_v * geom.d * 2)
+    b = (state_row_bytes(geom) * n_active + n_active * geom.T * C * 2 + C * 4 * 2
+         + n_active * (3 + geom.T) * C * 2 + n_active * geom.T * geom.H_v * 4 * 2
+         + geom.B * geom.T * geom.H_v * geom.d * 2)
+    if mode == "snapshot":
+        b += geom.T * state_row_bytes(geom) * n_active
+    if mode == "deferred":
+        b += state_row_bytes(geom) * n_apply
+    return b
 
 
-def commit_bytes(geom, n_keep, n_layers):
-    """Algorithmic bytes of one grouped commit launch: read S_0 and write S_keep
-    for every (layer, row) with keep' >= 1."""
-    return 2 * state_row_bytes(geom) * n_keep * n_layers
+def ring_shift_bytes(geom, n_keep, n_layers):
+    """Conv-window shift of the commit: three slots read and written per kept row."""
+    return 2 * 3 * geom.C * 2 * n_keep * n_layers
+
+
+def commit_bytes(geom, n_keep, n_layers, mode="recompute"):
+    """Algorithmic bytes of one grouped commit launch.  RECOMPUTE: read S_0 and
+    write S_keep for every (layer, row) with keep' >= 1; SNAPSHOT: read the
+    snapshot S_keep and write it; DEFERRED: only the keep record and the window
+    shift (the state update moves into the next verify)."""
+    state = 0 if mode == "deferred" else 2 * state_row_bytes(geom) * n_keep * n_layers
+    return state + ring_shift_bytes(geom, n_keep, n_layers)
+
+
+def path_min_bytes(geom, n_active, n_keep, n_layers):
+    """The least HBM traffic of a cycle whatever the commit strategy: every
+    active row's state read once, every kept row's state written once, plus
+    the inputs, outputs and conv windows."""
+    per_layer = verify_bytes(geom, n_active) + state_row_bytes(geom) * n_keep
+    return n_layers * per_layer + ring_shift_bytes(geom, n_keep, n_layers)
 
 
 # ---------------------------------------------------------------- environment
@@ -121,6 +147,27 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def rank_seed(seed, rank):
+    """Each rank verifies its own cohort: disjoint seeded draws per rank."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(ms, device, world):
+    """The job's elapsed time is its slowest rank's: max of the per-rank times."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank_step, step_ms):
+    """Whole-job throughput: every rank processes its own units each step."""
+    return world * units_per_rank_step / (step_ms * 1e-3)
 
 
 class ClockSampler:
@@ -231,13 +278,12 @@ def profiled_traffic(kind, workload_key):
 def oracle_layer_cycle(orc, geom, st, cy, layer, active, keep):
     """One layer's verify + commit on the CPU oracle (fp64)."""
     from speculative_decode_gated_gdn_gb300 import synth
-    R = geom.R
     ring = st["ring"][layer]
     offsets = st["offsets"]
     win = np.empty((geom.B, geom.C, 3))
     for b in range(geom.B):
         for i in range(3):
-            win[b, :, i] = synth.bf16_to_f32(ring[b, (int(offsets[b]) - 3 + i) % R])
+            win[b, :, i] = synth.bf16_to_f32(ring[b, i])  # committed window: slots 0..2
     x = synth.bf16_to_f32(cy["x"][layer]).astype(np.float64)
     w = synth.bf16_to_f32(st["conv_w"][layer]).astype(np.float64)
     S = st["state"][layer].copy()
@@ -289,9 +335,11 @@ def timing_event():
 
 def verify_mode(mode, layer):
     """Layers after the first follow another layer's verify, which writes none of
-    their buffers, so they may stage state before that verify finishes."""
+    their buffers, so they may stage state before that verify finishes.  In
+    DEFERRED mode the commit before layer 0 writes no state either."""
     from speculative_decode_gated_gdn_gb300 import lib as L
-    return mode | (L.GDN_VERIFY_OVERLAP if layer > 0 else 0)
+    flag = layer > 0 or mode == L.GDN_COMMIT_DEFERRED
+    return mode | (L.GDN_VERIFY_OVERLAP if flag else 0)
 
 
 def run_gpu(args, rank, world, local):
@@ -303,8 +351,8 @@ def run_gpu(args, rank, world, local):
     dev = torch.device("cuda", local)
     geom, inactive = workload(args)
     n_layers = args.layers
-    mode = L.GDN_COMMIT_SNAPSHOT if args.mode == "snapshot" else L.GDN_COMMIT_RECOMPUTE
-    seed = args.seed + 1000 * rank
+    mode = MODES[args.mode]
+    seed = rank_seed(args.seed, rank)
     pool = 16
     d = L.dims_of(geom)
     K, W = args.steps, args.warmup
@@ -325,12 +373,13 @@ def run_gpu(args, rank, world, local):
     active = torch.from_numpy(active_np).to(dev)
     keeps = torch.from_numpy(keeps_np).to(dev)
     ws_bytes = L.gdn_layer_workspace_bytes(d, mode)
-    ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(n_layers)]
+    ws = [torch.zeros(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(n_layers)]  # DEFERRED: zeroed
     out = torch.empty((n_layers, geom.B, geom.T, geom.H_v, geom.d), dtype=torch.bfloat16, device=dev)
     xs = [bf(c["x"]) for c in inp]
     gs = [torch.from_numpy(c["g"]).to(dev) for c in inp]
     bs = [torch.from_numpy(c["beta"]).to(dev) for c in inp]
     states = [state[l] for l in range(n_layers)]
+    rings = [ring[l] for l in range(n_layers)]
 
     def cycle(c, x, g, beta, keep, ev=None):
         for l in range(n_layers):
@@ -338,7 +387,7 @@ def run_gpu(args, rank, world, local):
                               offsets, active, out[l], ws[l], ws_bytes)
         if ev is not None:
             ev[0].record()
-        L.gdn_commit(d, mode, states, ws, keep, active, offsets)
+        L.gdn_commit(d, mode, states, rings, ws, keep, active, offsets)
         if ev is not None:
             ev[1].record()
 
@@ -361,6 +410,8 @@ def run_gpu(args, rank, world, local):
     state.copy_(torch.from_numpy(st["state"]).to(dev))
     ring.copy_(bf(st["ring"]))
     offsets.copy_(torch.from_numpy(st["offsets"].copy()).to(dev))
+    for w in ws:
+        w.zero_()
     torch.cuda.synchronize()
 
     for c in range(W):
@@ -385,24 +436,25 @@ def run_gpu(args, rank, world, local):
         clk.mark_end()
     if world > 1:
         dist.barrier()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dev, world)
     commit_ms = [events[c][0].elapsed_time(events[c][1]) for c in range(W, W + K)]
 
     n_active = int(active_np.sum())
-    kp = np.where(active_np[None, :] == 1, keeps_np[W:W + K], 0)
-    n_keep = (kp >= 1).sum(axis=1)
-    commit_alg = np.array([commit_bytes(geom, int(nk), n_layers) for nk in n_keep], dtype=np.float64)
-    step_bytes = commit_alg + n_layers * verify_bytes(geom, n_active)
+    kp_all = np.where(active_np[None, :] == 1, keeps_np, 0)
+    n_keep_all = (kp_all >= 1).sum(axis=1)
+    n_keep = n_keep_all[W:W + K]
+    # DEFERRED: the verify of cycle c applies the commit of cycle c - 1
+    n_apply = n_keep_all[W - 1:W + K - 1] if args.mode == "deferred" else np.zeros(K, np.int64)
+    commit_alg = np.array([commit_bytes(geom, int(nk), n_layers, args.mode) for nk in n_keep], dtype=np.float64)
+    verify_alg = np.array([verify_bytes(geom, n_active, args.mode, int(na)) for na in n_apply], dtype=np.float64)
+    step_bytes = commit_alg + n_layers * verify_alg
+    min_bytes = np.array([path_min_bytes(geom, n_active, int(nk), n_layers) for nk in n_keep], dtype=np.float64)
     peak, peak_kind = measured_peak()
     step_ms = ms / K
     commit_avg_ms = float(np.mean(commit_ms))
     verify_avg_ms = max(step_ms - commit_avg_ms, 1e-9) / n_layers
     commit_gbs = float(commit_alg.mean()) / (commit_avg_ms * 1e-3) / 1e9
-    verify_gbs = verify_bytes(geom, n_active) / (verify_avg_ms * 1e-3) / 1e9
+    verify_gbs = float(verify_alg.mean()) / (verify_avg_ms * 1e-3) / 1e9
     step_gbs = float(step_bytes.mean()) / (step_ms * 1e-3) / 1e9
     dominant = "commit" if commit_avg_ms >= verify_avg_ms * n_layers else "verify"
     wl_key = f"B{geom.B}T{geom.T}L{n_layers}{args.mode}"
@@ -416,15 +468,17 @@ def run_gpu(args, rank, world, local):
         roof = {"kernel": "verify_kernel", "bound": "hbm", "achieved": round(verify_gbs, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(verify_gbs / peak, 4),
                 "traffic": profiled_traffic("verify", wl_key), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": float(verify_bytes(geom, n_active)),
+                "algorithmic_bytes_per_launch": float(verify_alg.mean()),
                 "avg_launch_ms": round(verify_avg_ms, 5)}
     res = {
-        "metric": METRIC, "value": world * geom.B * geom.T / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_rate(world, geom.B * geom.T, step_ms), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_dict(args, geom, inactive),
         "hbm": {"step_algorithmic_bytes": float(step_bytes.mean()), "achieved_gbs": round(step_gbs, 1),
                 "peak_gbs": peak, "frac": round(step_gbs / peak, 4), "peak_source": peak_kind,
+                "path_min_bytes": float(min_bytes.mean()),
+                "path_min_frac": round(float(min_bytes.mean()) / (step_ms * 1e-3) / 1e9 / peak, 4),
                 "verify_gbs": round(verify_gbs, 1), "verify_avg_ms_incl_gaps": round(verify_avg_ms, 5),
                 "commit_gbs": round(commit_gbs, 1), "commit_avg_ms": round(commit_avg_ms, 5)},
         "roofline": roof,
@@ -470,7 +524,7 @@ def run_e2e(args, geom, d, mode, dev, inp, keeps_np, state, ring, conv_w, offset
         for l in range(n_layers):
             L.gdn_conv_verify(d, verify_mode(mode, l), dxb[l], conv_w[l], dg[l], db[l], state[l], ring[l],
                               offsets, active, out[l], ws[l], ws_bytes)
-        L.gdn_commit(d, mode, states, ws, dk, active, offsets)
+        L.gdn_commit(d, mode, states, [ring[l] for l in range(n_layers)], ws, dk, active, offsets)
         hout.copy_(out, non_blocking=True)
         hoff.copy_(offsets, non_blocking=True)
 
@@ -497,14 +551,10 @@ def run_e2e(args, geom, d, mode, dev, inp, keeps_np, state, ring, conv_w, offset
         graphs[c].replay()
     end.record()
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dev, world)
     h2d = hx[0].numel() * 2 + hg[0].numel() * 4 + hb[0].numel() * 4 + geom.B * 4
     d2h = hout.numel() * 2 + hoff.numel() * 4
-    return {"value": world * geom.B * geom.T / (ms / K * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": job_rate(world, geom.B * geom.T, ms / K), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / K,
             "how": "per step: pinned-host x/g/beta/keep copied in, 30 verifies + grouped commit through the C ABI, "
                    "outputs and offsets copied out; one CUDA graph per step"}
@@ -532,8 +582,8 @@ def run_prefill_bench(args, rank, world, local):
     geom = synth.Geometry(B=args.B if args.B != 8 else 1, T=2, H_k=16, H_v=32, d=128)
     Lp, K, W = args.L, args.steps, args.warmup
     d = L.dims_of(geom)
-    pr = synth.prompt_inputs(geom, args.seed + rank, Lp)
-    st = synth.layer_state(geom, args.seed + rank, 1, offsets=np.zeros(geom.B, np.int32))
+    pr = synth.prompt_inputs(geom, rank_seed(args.seed, rank), Lp)
+    st = synth.layer_state(geom, rank_seed(args.seed, rank), 1, offsets=np.zeros(geom.B, np.int32))
 
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -558,11 +608,11 @@ def run_prefill_bench(args, rank, world, local):
         step()
     end.record()
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end) / K
+    ms = max_over_ranks(start.elapsed_time(end), dev, world) / K
     flops = prefill_flops(Lp, geom.H_v, geom.d) * geom.B
     hbm = geom.B * (Lp * geom.C * 2 + Lp * geom.H_v * geom.d * 2 + 2 * geom.H_v * geom.d * geom.d * 4
                     + 2 * Lp * geom.H_v * 4)
-    return {"metric": "GDN chunked prefill prompt tokens/s (1 GPU)", "value": geom.B * Lp / (ms * 1e-3),
+    return {"metric": "GDN chunked prefill prompt tokens/s", "value": job_rate(world, geom.B * Lp, ms),
             "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms,
             "higher_is_better": True, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"chunked prefill B={geom.B} L={Lp} H_k=16 H_v=32 d=128 chunk 64",

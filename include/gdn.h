@@ -12,7 +12,10 @@
  *   gdn_commit        once per cycle for all layers: keep the accepted prefix
  *                     keep[b] of every row; keep=0 and inactive rows restore
  *                     the pre-verification state exactly (nothing is
- *                     written); advances the per-row committed offsets.
+ *                     written); shifts the conv window; advances the per-row
+ *                     committed offsets.
+ *   gdn_flush         materialise commits that a DEFERRED-mode cycle left
+ *                     pending in its workspaces.
  *   gdn_prefill_chunked  the same recurrence over a prompt of L tokens in
  *                     chunked (WY/UT) form, leaving state, conv ring and
  *                     offsets primed for the first verify.
@@ -57,11 +60,15 @@
  *                                     and write strength
  *  state    [B][H_v][d_v][d_k]  fp32  S with v ~ S k: row j (d_v) holds a
  *                                     contiguous d_k vector
- *  ring     [B][R][C]           bf16  raw inputs of absolute position p in slot
- *                                     p mod R; the committed conv window of row
- *                                     b is positions offsets[b]-3 .. offsets[b]-1
+ *  ring     [B][R][C]           bf16  conv cache: slots 0..2 hold the raw inputs
+ *                                     of the three committed positions before the
+ *                                     next token (oldest first); slots 3..2+T hold
+ *                                     the raw inputs of the latest verify's T
+ *                                     positions.  A fresh row has zeros in 0..2.
  *  offsets  [B]                 int32 committed tokens per row (one array shared
- *                                     by all layers)
+ *                                     by all layers); bookkeeping for the caller,
+ *                                     advanced by gdn_commit and
+ *                                     gdn_prefill_chunked, not read by verify
  *  active   [B]                 uint8 0 = inactive/padding/finished row
  *  out      [B][T][H_v][d_v]    bf16  o_t for each position
  *
@@ -99,6 +106,15 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
                                   rebuilds S_keep from the untouched S_0 */
 #define GDN_COMMIT_SNAPSHOT 1  /* verify writes S_1..S_T to the workspace;
                                   commit copies S_keep back */
+#define GDN_COMMIT_DEFERRED 2  /* as RECOMPUTE, but gdn_commit only records
+                                  keep and the state update of each (row, head)
+                                  is applied by that layer's next verify, which
+                                  reads the state anyway: each committed row is
+                                  read once and written once per cycle.  The
+                                  state buffer then lags the committed state
+                                  until that verify or gdn_flush runs.  The
+                                  workspace must be zero-filled once before its
+                                  first use; dims must not change after that. */
 
 /* flag OR-ed into the mode argument of gdn_conv_verify.  Every kernel of
  * the library is launched with programmatic dependent launch and waits for
@@ -108,10 +124,12 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
  * before waiting for its predecessor, so consecutive flagged verifies stream
  * their state ahead of one another.  The caller guarantees that no work
  * issued since the last library call made WITHOUT the flag writes this
- * call's `state`, `ring`, `active` or `conv_w`.  In a verify cycle over a
- * layer stack that means: flag every layer but the first one after
- * gdn_commit, gdn_prefill_chunked or any other write of these buffers.  It is
- * always safe to omit. */
+ * call's `state` or `active`.  In a verify cycle over a layer stack that
+ * means: flag every layer but the first one after an eager gdn_commit
+ * (RECOMPUTE or SNAPSHOT), gdn_prefill_chunked, gdn_flush or any other write
+ * of these buffers; a DEFERRED gdn_commit writes no state, so every layer of
+ * a DEFERRED cycle may be flagged.  Never flag a repeated verify of the same
+ * layer.  It is always safe to omit. */
 #define GDN_VERIFY_OVERLAP 0x100
 
 /* sticky device status bits (gdn_get_status) */
@@ -146,19 +164,22 @@ const char *gdn_last_error(void);
  * Bytes of per-layer workspace that gdn_conv_verify fills and gdn_commit reads
  * for `mode`; 0 if dims or mode are invalid.  RECOMPUTE needs
  * 4*B*T*(H_v*d_v + H_k*d_k + H_v) bytes (+ alignment padding); SNAPSHOT needs
- * 4*T*B*H_v*d_v*d_k bytes.
+ * 4*T*B*H_v*d_v*d_k bytes; DEFERRED twice RECOMPUTE's captures plus a header.
  */
 size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int mode);
 
 /*
  * Verify one layer: for every active row b run the T positions from the
  * committed window and the pre-verification state, writing o_t to `out`.
- *  - reads  x, conv_w, g, beta, state, ring (window slots), offsets, active;
- *  - writes out; the ring slots of positions offsets[b] .. offsets[b]+T-1 of
- *    active rows (never the committed window); layer_ws (the captured
- *    verification quantities the matching gdn_commit needs).
- *  - never writes `state`; inactive rows get out = 0 and no ring or state
- *    access.
+ *  - reads  x, conv_w, g, beta, state, ring slots 0..2, active;
+ *  - writes out; ring slots 3..2+T of active rows (never the committed
+ *    window); layer_ws (the captured verification quantities the matching
+ *    gdn_commit needs).
+ *  - RECOMPUTE / SNAPSHOT: never writes `state`.  DEFERRED: first applies the
+ *    commit the last gdn_commit left pending for this layer to the state rows
+ *    it concerns (also for rows now inactive), then verifies from them.
+ *  - inactive rows get out = 0 and no ring access.
+ *  - `offsets` is not read (it may be NULL).
  * layer_ws must stay untouched until the matching gdn_commit has run.
  * Errors: GDN_ERR_INVALID_ARG, _UNSUPPORTED, _MISALIGNED, _WORKSPACE
  * (layer_ws_bytes < gdn_layer_workspace_bytes), _CUDA.
@@ -173,11 +194,13 @@ int gdn_conv_verify(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn
  * (grouped across layers).  keep'[b] = keep[b] if active[b] and
  * 0 <= keep[b] <= T, else 0 (an active row with keep outside [0, T] also sets
  * GDN_STATUS_BAD_KEEP).  For keep' >= 1 the layer's state rows of b become the
- * state after the first keep' positions; for keep' = 0 nothing of row b is
- * written (exact restore).  offsets[b] += keep' (once, not per layer).  The
- * ring is not touched: advancing the offset is what moves the committed
- * window over the positions verify already wrote.
+ * state after the first keep' positions (RECOMPUTE, SNAPSHOT: now; DEFERRED:
+ * recorded, applied by the layer's next verify or gdn_flush) and the conv
+ * window becomes ring slots keep'..keep'+2 (written to slots 0..2); for
+ * keep' = 0 nothing of row b is written (exact restore).
+ * offsets[b] += keep' (once, not per layer).
  *  state    host array [n_layers] of device pointers to each layer's state
+ *  ring     host array [n_layers] of device pointers to each layer's ring
  *  layer_ws host array [n_layers] of device pointers to each layer's workspace
  *           (as filled by that layer's gdn_conv_verify with the same dims/mode)
  *  keep, active, offsets  device arrays [B]; keep/active are read on the
@@ -186,8 +209,19 @@ int gdn_conv_verify(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn
  * entries), _UNSUPPORTED, _MISALIGNED, _CUDA.
  */
 int gdn_commit(const gdn_dims *dims, int mode, int n_layers, float *const *state,
-               void *const *layer_ws, const int32_t *keep, const uint8_t *active,
-               int32_t *offsets, void *stream);
+               gdn_bf16 *const *ring, void *const *layer_ws, const int32_t *keep,
+               const uint8_t *active, int32_t *offsets, void *stream);
+
+/*
+ * Apply every commit a DEFERRED cycle left pending in the n_layers layer
+ * workspaces to the state buffers, so that they hold the committed state (as
+ * an eager commit would have left them).  Call it before reading a state
+ * buffer directly, before gdn_prefill_chunked, and before switching a layer
+ * to another mode.  Idempotent; a no-op for RECOMPUTE and SNAPSHOT.
+ * Errors: as gdn_commit.
+ */
+int gdn_flush(const gdn_dims *dims, int mode, int n_layers, float *const *state,
+              void *const *layer_ws, void *stream);
 
 /*
  * Bytes of workspace gdn_prefill_chunked needs for a prompt of L tokens;
@@ -197,13 +231,15 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L);
 
 /*
  * Prime every row over a prompt of L tokens in chunked form (chunk = 64):
- * conv from the committed window, L2 norm, then per chunk the UT transform of
- * the decay-weighted strictly-lower K K^T block on tensor cores and a
- * sequential pass of the state across chunks.  Equivalent, up to rounding, to
- * gdn_conv_verify with T = L followed by gdn_commit with keep = L for all rows.
+ * conv from the committed window (ring slots 0..2), L2 norm, then per chunk
+ * the UT transform of the decay-weighted strictly-lower K K^T block on tensor
+ * cores and a sequential pass of the state across chunks.  Equivalent, up to
+ * rounding, to gdn_conv_verify with T = L followed by gdn_commit with
+ * keep = L for all rows.
  *  x [B][L][C] bf16; g, beta [B][L][H_v] fp32; state [B][H_v][d_v][d_k] fp32
- *  in (initial) / out (final); ring and offsets updated as a commit of L
- *  tokens would (offsets[b] += L); out [B][L][H_v][d_v] bf16.
+ *  in (initial) / out (final); ring slots 0..2 set to the last three raw
+ *  inputs of window ++ prompt; offsets[b] += L; out [B][L][H_v][d_v] bf16.
+ * A layer run in DEFERRED mode must be flushed (gdn_flush) first.
  * dims->T and T_max describe the ring the state is primed for (R = 3 + T_max).
  * Errors: as gdn_conv_verify; GDN_ERR_WORKSPACE if ws_bytes is too small.
  */
@@ -226,6 +262,7 @@ int gdn_prefill_chunked(const gdn_dims *dims, int L, const gdn_bf16 *x, const gd
  * scratch array built into the library's device code, GDN_NOALLOC_WS_BYTES
  * (4 MiB) per GPU, which every GPU that loads the library holds until the
  * process exits.  It allocates nothing and frees nothing.
+ *  - DEFERRED mode is not accepted (its workspace must persist per layer).
  *  - Shapes whose workspace (gdn_layer_workspace_bytes) exceeds the scratch
  *    are rejected with GDN_ERR_WORKSPACE before anything is launched (e.g. the
  *    B=8, T=2, 32x128 cohort needs about 0.4 MiB in RECOMPUTE mode and fits;

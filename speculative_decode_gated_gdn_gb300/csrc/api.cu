@@ -58,14 +58,38 @@ int check_dims(const gdn_dims *d) {
 }
 
 int check_mode(int mode) {
-  if (mode != GDN_COMMIT_RECOMPUTE && mode != GDN_COMMIT_SNAPSHOT)
-    return fail(GDN_ERR_INVALID_ARG, "mode must be GDN_COMMIT_RECOMPUTE or GDN_COMMIT_SNAPSHOT (got %d)", mode);
+  if (mode != GDN_COMMIT_RECOMPUTE && mode != GDN_COMMIT_SNAPSHOT && mode != GDN_COMMIT_DEFERRED)
+    return fail(GDN_ERR_INVALID_ARG,
+                "mode must be GDN_COMMIT_RECOMPUTE, GDN_COMMIT_SNAPSHOT or GDN_COMMIT_DEFERRED (got %d)", mode);
   return GDN_OK;
 }
 
 size_t layer_ws_bytes(const gdn_dims *d, int mode) {
   if (mode == GDN_COMMIT_RECOMPUTE) return recompute_ws(d->B, d->T, d->H_k, d->H_v, d->d_k).total;
+  if (mode == GDN_COMMIT_DEFERRED) return deferred_ws(d->B, d->T, d->H_k, d->H_v, d->d_k).total;
   return snapshot_ws(d->B, d->T, d->H_v, d->d_k);
+}
+
+// Host arrays of per-layer device pointers for gdn_commit / gdn_flush.
+int fill_layers(CommitParams &p, int n_layers, float *const *state, gdn_bf16 *const *ring, void *const *layer_ws) {
+  if (n_layers < 1 || n_layers > kMaxLayers)
+    return fail(GDN_ERR_INVALID_ARG, "n_layers=%d outside [1, %d]", n_layers, kMaxLayers);
+  if (!state || !layer_ws) return fail(GDN_ERR_INVALID_ARG, "state / layer_ws host arrays are NULL");
+  for (int l = 0; l < n_layers; ++l) {
+    if (!state[l] || !layer_ws[l]) return fail(GDN_ERR_INVALID_ARG, "layer %d: NULL state or workspace", l);
+    if (!aligned(state[l], 16)) return fail(GDN_ERR_MISALIGNED, "layer %d: state not 16-byte aligned", l);
+    if (!aligned(layer_ws[l], 256))
+      return fail(GDN_ERR_MISALIGNED, "layer %d: workspace not 256-byte aligned", l);
+    p.state[l] = state[l];
+    p.ws[l] = static_cast<float *>(layer_ws[l]);
+    if (ring) {
+      if (!ring[l]) return fail(GDN_ERR_INVALID_ARG, "layer %d: NULL ring", l);
+      if (!aligned(ring[l], 16)) return fail(GDN_ERR_MISALIGNED, "layer %d: ring not 16-byte aligned", l);
+      p.ring[l] = reinterpret_cast<uint16_t *>(ring[l]);
+    }
+  }
+  p.n_layers = n_layers;
+  return GDN_OK;
 }
 
 #define GDN_NEED_PTR(ptr, align)                                                             \
@@ -112,10 +136,10 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
   GDN_NEED_PTR(beta, 16);
   GDN_NEED_PTR(state, 16);
   GDN_NEED_PTR(ring, 16);
-  GDN_NEED_PTR(offsets, 4);
   GDN_NEED_PTR(active, 1);
   GDN_NEED_PTR(out, 16);
   GDN_NEED_PTR(layer_ws, 256);
+  (void)offsets;  // the committed window lives at fixed ring slots
   const size_t need = layer_ws_bytes(dims, mode);
   if (layer_ws_bytes_given < need)
     return fail(GDN_ERR_WORKSPACE, "layer workspace has %zu bytes, needs %zu", layer_ws_bytes_given, need);
@@ -127,10 +151,10 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
   p.beta = beta;
   p.state = state;
   p.ring = ring;
-  p.offsets = offsets;
   p.active = active;
   p.out = out;
   p.B = dims->B;
+  p.T = dims->T;
   p.H_k = dims->H_k;
   p.H_v = dims->H_v;
   p.C = (2 * dims->H_k + dims->H_v) * dims->d_k;
@@ -145,8 +169,21 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
     p.ws_e = reinterpret_cast<float *>(ws + w.e);
     p.ws_k = reinterpret_cast<float *>(ws + w.k);
     p.ws_G = reinterpret_cast<float *>(ws + w.G);
-  } else {
+  } else if (mode == GDN_COMMIT_SNAPSHOT) {
     p.ws_snap = reinterpret_cast<float *>(ws);
+  } else {
+    const DeferredWs w = deferred_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);
+    const RecomputeWs r = recompute_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);
+    p.ws_epoch = reinterpret_cast<const int *>(ws);
+    p.ws_pend = reinterpret_cast<const int *>(ws + w.pend);
+    p.ws_applied = reinterpret_cast<int *>(ws + w.applied);
+    for (int hf = 0; hf < 2; ++hf) {
+      char *half = ws + w.half0 + size_t(hf) * w.half_bytes;
+      p.dh_e[hf] = reinterpret_cast<float *>(half + r.e);
+      p.dh_k[hf] = reinterpret_cast<float *>(half + r.k);
+      p.dh_G[hf] = reinterpret_cast<float *>(half + r.G);
+    }
+    p.state_w = const_cast<float *>(state);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -160,38 +197,49 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
 }
 
 __attribute__((visibility("default"))) int gdn_commit(const gdn_dims *dims, int mode, int n_layers,
-                                                      float *const *state, void *const *layer_ws,
-                                                      const int32_t *keep, const uint8_t *active,
-                                                      int32_t *offsets, void *stream) {
+                                                      float *const *state, gdn_bf16 *const *ring,
+                                                      void *const *layer_ws, const int32_t *keep,
+                                                      const uint8_t *active, int32_t *offsets, void *stream) {
   int rc = check_dims(dims);
   if (rc) return rc;
   if ((rc = check_mode(mode))) return rc;
-  if (n_layers < 1 || n_layers > kMaxLayers)
-    return fail(GDN_ERR_INVALID_ARG, "n_layers=%d outside [1, %d]", n_layers, kMaxLayers);
-  if (!state || !layer_ws) return fail(GDN_ERR_INVALID_ARG, "state / layer_ws host arrays are NULL");
+  if (!ring) return fail(GDN_ERR_INVALID_ARG, "ring host array is NULL");
+  CommitParams p{};
+  if ((rc = fill_layers(p, n_layers, state, ring, layer_ws))) return rc;
   if (dims->B == 0) return ok();
   GDN_NEED_PTR(keep, 4);
   GDN_NEED_PTR(active, 1);
   GDN_NEED_PTR(offsets, 4);
-  CommitParams p{};
-  for (int l = 0; l < n_layers; ++l) {
-    if (!state[l] || !layer_ws[l]) return fail(GDN_ERR_INVALID_ARG, "layer %d: NULL state or workspace", l);
-    if (!aligned(state[l], 16)) return fail(GDN_ERR_MISALIGNED, "layer %d: state not 16-byte aligned", l);
-    if (!aligned(layer_ws[l], 256))
-      return fail(GDN_ERR_MISALIGNED, "layer %d: workspace not 256-byte aligned", l);
-    p.state[l] = state[l];
-    p.ws[l] = static_cast<const float *>(layer_ws[l]);
-  }
   p.keep = keep;
   p.active = active;
   p.offsets = offsets;
-  p.n_layers = n_layers;
   p.B = dims->B;
   p.T = dims->T;
   p.H_k = dims->H_k;
   p.H_v = dims->H_v;
+  p.C = (2 * dims->H_k + dims->H_v) * dims->d_k;
+  p.R = kHist + dims->T_max;
+  p.status = status_word_address();
+  if (!p.status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
   cudaError_t e = launch_commit(p, dims->d_k, mode, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gdn_commit launch");
+  return ok();
+}
+
+__attribute__((visibility("default"))) int gdn_flush(const gdn_dims *dims, int mode, int n_layers,
+                                                     float *const *state, void *const *layer_ws, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_mode(mode))) return rc;
+  CommitParams p{};
+  if ((rc = fill_layers(p, n_layers, state, nullptr, layer_ws))) return rc;
+  if (dims->B == 0 || mode != GDN_COMMIT_DEFERRED) return ok();
+  p.B = dims->B;
+  p.T = dims->T;
+  p.H_k = dims->H_k;
+  p.H_v = dims->H_v;
+  cudaError_t e = launch_flush(p, dims->d_k, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_flush launch");
   return ok();
 }
 
@@ -283,6 +331,9 @@ __attribute__((visibility("default"))) int gdn_conv_verify_noalloc(
   int rc = check_dims(dims);
   if (rc) return rc;
   if ((rc = check_mode(mode & 0xff))) return rc;
+  if ((mode & 0xff) == GDN_COMMIT_DEFERRED)
+    return fail(GDN_ERR_INVALID_ARG,
+                "gdn_conv_verify_noalloc: DEFERRED mode needs a workspace that persists per layer");
   const size_t need = layer_ws_bytes(dims, mode & 0xff);
   if (need > GDN_NOALLOC_WS_BYTES)
     return fail(GDN_ERR_WORKSPACE,

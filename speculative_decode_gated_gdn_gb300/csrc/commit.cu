@@ -10,7 +10,10 @@
 // of 32 state rows); a persistent grid strides over them and skips every unit
 // whose row has keep' = 0, so restored rows cost no state traffic at all and
 // their bytes are never written.  A committed unit reads S_0 once and writes
-// S_keep once (RECOMPUTE) or copies the verify-time snapshot (SNAPSHOT).
+// S_keep once (RECOMPUTE) or copies the verify-time snapshot (SNAPSHOT); in
+// DEFERRED mode the commit only records keep' per layer, and the next verify
+// of each (row, head) applies it.  Every mode also shifts the conv window of
+// committed rows (the conv-cache mutation).
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -36,6 +39,61 @@ __device__ __forceinline__ int effective_keep(const CommitParams &p, int b) {
   return (k >= 0 && k <= p.T) ? k : 0;
 }
 
+// S_keep of 8 state rows (this warp's), in place on the lane's float4
+// segments: S <- gamma_{K-1} S + sum_{t<K} exp(G_{K-1} - G_t) e_t k_t^T with the
+// captures e [B][T][H_v][D], k [B][T][H_k][D], G [B][T][H_v] of one verify.
+template <int D>
+__device__ __forceinline__ void rebuild_rows(float4 (&s)[RowLanes<D>::RPL], const float *we, const float *wk,
+                                             const float *wG, int b, int h, int hk, int row0, int K, int T, int H_k,
+                                             int H_v, int sub, int grp) {
+  using G = RowLanes<D>;
+  const float GK = wG[(size_t(b) * T + (K - 1)) * H_v + h];
+  const float gam = expf(GK);
+#pragma unroll
+  for (int i = 0; i < G::RPL; ++i) s[i] = make_float4(gam * s[i].x, gam * s[i].y, gam * s[i].z, gam * s[i].w);
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) {
+    if (t < K) {
+      const float c = expf(GK - wG[(size_t(b) * T + t) * H_v + h]);
+      const float4 kv = *reinterpret_cast<const float4 *>(wk + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub);
+      const float *ert = we + ((size_t(b) * T + t) * H_v + h) * D + row0;
+#pragma unroll
+      for (int i = 0; i < G::RPL; ++i) {
+        const float f = c * ert[grp + G::GPW * i];
+        s[i].x = fmaf(f, kv.x, s[i].x);
+        s[i].y = fmaf(f, kv.y, s[i].y);
+        s[i].z = fmaf(f, kv.z, s[i].z);
+        s[i].w = fmaf(f, kv.w, s[i].w);
+      }
+    }
+  }
+}
+
+// Conv-cache mutation of the commit: for rows with keep' = K >= 1 the new
+// committed window is ring slots K..K+2 (the last three raw inputs of
+// window ++ x_0..x_{K-1}); it is written to slots 0..2.  Each thread moves 8
+// channels; units are (layer, row, 1024-channel block) after `first_unit`.
+__device__ __forceinline__ void shift_windows(const CommitParams &p, long long first_unit) {
+  const int C8 = p.C / 8;
+  const int blocks_per_row = (C8 + blockDim.x - 1) / blockDim.x;
+  const long long units = (long long)p.n_layers * p.B * blocks_per_row;
+  for (long long u = (long long)blockIdx.x - first_unit; u < units; u += gridDim.x) {
+    if (u < 0) continue;
+    const int layer = int(u / ((long long)p.B * blocks_per_row));
+    const int r = int(u % ((long long)p.B * blocks_per_row));
+    const int b = r / blocks_per_row, blk = r % blocks_per_row;
+    const int K = effective_keep(p, b);
+    const int c8 = blk * blockDim.x + threadIdx.x;
+    if (K == 0 || c8 >= C8) continue;
+    uint4 *ring = reinterpret_cast<uint4 *>(p.ring[layer] + size_t(b) * p.R * p.C) + c8;
+    uint4 w[kHist];
+#pragma unroll
+    for (int i = 0; i < kHist; ++i) w[i] = ring[size_t(K + i) * C8];
+#pragma unroll
+    for (int i = 0; i < kHist; ++i) ring[size_t(kWinSlot + i) * C8] = w[i];
+  }
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
   using G = RowLanes<D>;
@@ -43,7 +101,7 @@ __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
   constexpr int TILES = D / kTileRows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane % LPR, grp = lane / LPR;
-  pdl_wait();  // every state, workspace and offsets access follows the preceding kernel
+  pdl_wait();  // every state, ring, workspace and offsets access follows the preceding kernel
   pdl_trigger();
 
   if (blockIdx.x == 0) {
@@ -52,16 +110,23 @@ __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
       int kp = 0;
       if (p.active[b]) {
         if (k >= 0 && k <= p.T) kp = k;
-        else atomicOr(&g_status, GDN_STATUS_BAD_KEEP);
+        else atomicOr(p.status, GDN_STATUS_BAD_KEEP);
       }
       p.offsets[b] += kp;
+      if (MODE == GDN_COMMIT_DEFERRED) {
+        const DeferredWs dl = deferred_ws(p.B, p.T, p.H_k, p.H_v, D);
+        for (int l = 0; l < p.n_layers; ++l)
+          reinterpret_cast<int *>(reinterpret_cast<char *>(p.ws[l]) + dl.pend)[b] = kp;
+      }
     }
+    if (MODE == GDN_COMMIT_DEFERRED)
+      for (int l = tid; l < p.n_layers; l += blockDim.x) *reinterpret_cast<int *>(p.ws[l]) += 1;
   }
 
   const int H_v = p.H_v, T = p.T;
   const int rep = H_v / p.H_k;
   const long long per_layer = (long long)p.B * H_v * TILES;
-  const long long total = per_layer * p.n_layers;
+  const long long total = MODE == GDN_COMMIT_DEFERRED ? 0 : per_layer * p.n_layers;
   for (long long u = blockIdx.x; u < total; u += gridDim.x) {
     const int layer = int(u / per_layer);
     long long r = u - layer * per_layer;
@@ -72,52 +137,69 @@ __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
     const int K = effective_keep(p, b);
     if (K == 0) continue;
 
-    float *S = p.state[layer] + ((size_t(b) * H_v + h) * D + tile * kTileRows + warp * 8) * D;
+    const int row0 = tile * kTileRows + warp * 8;
+    float *S = p.state[layer] + ((size_t(b) * H_v + h) * D + row0) * D;
+    float4 s[RPL];
     if (MODE == GDN_COMMIT_SNAPSHOT) {
       const size_t plane = size_t(p.B) * H_v * D * D;
-      const float *src = p.ws[layer] + size_t(K - 1) * plane +
-                         ((size_t(b) * H_v + h) * D + tile * kTileRows + warp * 8) * D;
-      float4 v[RPL];
+      const float *src = p.ws[layer] + size_t(K - 1) * plane + ((size_t(b) * H_v + h) * D + row0) * D;
 #pragma unroll
-      for (int i = 0; i < RPL; ++i) v[i] = ld_stream_f4(src + size_t(grp + GPW * i) * D + 4 * sub);
-#pragma unroll
-      for (int i = 0; i < RPL; ++i) st_f4(S + size_t(grp + GPW * i) * D + 4 * sub, v[i]);
+      for (int i = 0; i < RPL; ++i) s[i] = ld_stream_f4(src + size_t(grp + GPW * i) * D + 4 * sub);
     } else {
       const RecomputeWs wl = recompute_ws(p.B, T, p.H_k, H_v, D);
       const char *base = reinterpret_cast<const char *>(p.ws[layer]);
-      const float *we = reinterpret_cast<const float *>(base + wl.e);
-      const float *wk = reinterpret_cast<const float *>(base + wl.k);
-      const float *wG = reinterpret_cast<const float *>(base + wl.G);
-      const int hk = h / rep;
-      float4 s[RPL];
 #pragma unroll
       for (int i = 0; i < RPL; ++i) s[i] = ld_stream_f4(S + size_t(grp + GPW * i) * D + 4 * sub);
-      const float GK = wG[(size_t(b) * T + (K - 1)) * H_v + h];
-      const float gam = expf(GK);
-      float4 acc[RPL];
-#pragma unroll
-      for (int i = 0; i < RPL; ++i)
-        acc[i] = make_float4(gam * s[i].x, gam * s[i].y, gam * s[i].z, gam * s[i].w);
-#pragma unroll
-      for (int t = 0; t < kMaxT; ++t) {
-        if (t < K) {
-          const float c = expf(GK - wG[(size_t(b) * T + t) * H_v + h]);
-          const float4 kv = *reinterpret_cast<const float4 *>(
-              wk + ((size_t(b) * T + t) * p.H_k + hk) * D + 4 * sub);
-          const float *ert = we + ((size_t(b) * T + t) * H_v + h) * D + tile * kTileRows + warp * 8;
-#pragma unroll
-          for (int i = 0; i < RPL; ++i) {
-            const float f = c * ert[grp + GPW * i];
-            acc[i].x = fmaf(f, kv.x, acc[i].x);
-            acc[i].y = fmaf(f, kv.y, acc[i].y);
-            acc[i].z = fmaf(f, kv.z, acc[i].z);
-            acc[i].w = fmaf(f, kv.w, acc[i].w);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < RPL; ++i) st_f4(S + size_t(grp + GPW * i) * D + 4 * sub, acc[i]);
+      rebuild_rows<D>(s, reinterpret_cast<const float *>(base + wl.e), reinterpret_cast<const float *>(base + wl.k),
+                      reinterpret_cast<const float *>(base + wl.G), b, h, h / rep, row0, K, T, p.H_k, H_v, sub,
+                      grp);
     }
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) st_f4(S + size_t(grp + GPW * i) * D + 4 * sub, s[i]);
+  }
+  shift_windows(p, 0);
+}
+
+// Materialise the commits a DEFERRED cycle left pending: one CTA per
+// (layer, row, head) unit at a time, so the unit's applied epoch is set by the
+// only CTA that handles it.
+template <int D>
+__global__ void __launch_bounds__(128) flush_kernel(const CommitParams p) {
+  using G = RowLanes<D>;
+  constexpr int RPL = G::RPL, GPW = G::GPW, LPR = G::LPR;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sub = lane % LPR, grp = lane / LPR;
+  pdl_wait();
+  pdl_trigger();
+  const int H_v = p.H_v, T = p.T;
+  const DeferredWs dl = deferred_ws(p.B, T, p.H_k, H_v, D);
+  const RecomputeWs rl = recompute_ws(p.B, T, p.H_k, H_v, D);
+  const long long total = (long long)p.n_layers * p.B * H_v;
+  for (long long u = blockIdx.x; u < total; u += gridDim.x) {
+    const int layer = int(u / ((long long)p.B * H_v));
+    const int r = int(u % ((long long)p.B * H_v));
+    const int b = r / H_v, h = r % H_v;
+    char *ws = reinterpret_cast<char *>(p.ws[layer]);
+    const int E = *reinterpret_cast<const int *>(ws);
+    int *applied = reinterpret_cast<int *>(ws + dl.applied) + size_t(b) * H_v + h;
+    const int K = reinterpret_cast<const int *>(ws + dl.pend)[b];
+    const int A = *applied;
+    if (E > A && K >= 1) {
+      const char *half = ws + dl.half0 + size_t((E - 1) & 1) * dl.half_bytes;
+      for (int row0 = warp * 8; row0 < D; row0 += 32) {
+        float *S = p.state[layer] + ((size_t(b) * H_v + h) * D + row0) * D;
+        float4 s[RPL];
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) s[i] = ld_stream_f4(S + size_t(grp + GPW * i) * D + 4 * sub);
+        rebuild_rows<D>(s, reinterpret_cast<const float *>(half + rl.e), reinterpret_cast<const float *>(half + rl.k),
+                        reinterpret_cast<const float *>(half + rl.G), b, h, h / (H_v / p.H_k), row0, K, T, p.H_k,
+                        H_v, sub, grp);
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) st_f4(S + size_t(grp + GPW * i) * D + 4 * sub, s[i]);
+      }
+    }
+    __syncthreads();  // every CTA thread has read A before it changes
+    if (E > A && tid == 0) *applied = E;
   }
 }
 
@@ -136,13 +218,33 @@ static int sm_count() {
 
 template <int D>
 static cudaError_t launch_commit_d(const CommitParams &p, int mode, cudaStream_t stream) {
-  const long long units = (long long)p.n_layers * p.B * p.H_v * (D / kTileRows);
+  long long units = (long long)p.n_layers * p.B * p.H_v * (D / kTileRows);
+  if (mode == GDN_COMMIT_DEFERRED) units = (long long)p.n_layers * p.B * ((p.C / 8 + 127) / 128);
   long long grid = (long long)sm_count() * 8;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
   if (mode == GDN_COMMIT_RECOMPUTE)
     return launch_pdl(commit_kernel<D, GDN_COMMIT_RECOMPUTE>, dim3(unsigned(grid)), dim3(128), stream, p);
-  return launch_pdl(commit_kernel<D, GDN_COMMIT_SNAPSHOT>, dim3(unsigned(grid)), dim3(128), stream, p);
+  if (mode == GDN_COMMIT_SNAPSHOT)
+    return launch_pdl(commit_kernel<D, GDN_COMMIT_SNAPSHOT>, dim3(unsigned(grid)), dim3(128), stream, p);
+  return launch_pdl(commit_kernel<D, GDN_COMMIT_DEFERRED>, dim3(unsigned(grid)), dim3(128), stream, p);
+}
+
+template <int D>
+static cudaError_t launch_flush_d(const CommitParams &p, cudaStream_t stream) {
+  long long grid = (long long)p.n_layers * p.B * p.H_v;
+  if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
+  if (grid < 1) grid = 1;
+  return launch_pdl(flush_kernel<D>, dim3(unsigned(grid)), dim3(128), stream, p);
+}
+
+cudaError_t launch_flush(const CommitParams &p, int D, cudaStream_t stream) {
+  switch (D) {
+    case 32: return launch_flush_d<32>(p, stream);
+    case 64: return launch_flush_d<64>(p, stream);
+    case 128: return launch_flush_d<128>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_commit(const CommitParams &p, int D, int mode, cudaStream_t stream) {

@@ -23,10 +23,10 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-__device__ __forceinline__ int ring_slot(int pos, int R) {
-  int s = pos % R;
-  return s < 0 ? s + R : s;
-}
+// Conv cache layout: ring slots 0..2 hold the committed window (oldest first),
+// slots 3..2+T the raw inputs of the latest verify.
+constexpr int kWinSlot = 0;
+constexpr int kNewSlot = kHist;
 
 // SiLU with the fast exponential and division intrinsics (a few ulp; the
 // conv output feeds an fp32 recurrence whose tolerance is far looser).
@@ -273,15 +273,21 @@ struct VerifyParams {
   const float *beta;
   const float *state;
   uint16_t *ring;
-  const int32_t *offsets;
   const uint8_t *active;
   uint16_t *out;
   float *ws_e;    // RECOMPUTE: [B][T][H_v][D]
   float *ws_k;    // RECOMPUTE: [B][T][H_k][D]
   float *ws_G;    // RECOMPUTE: [B][T][H_v]
   float *ws_snap; // SNAPSHOT:  [T][B][H_v][D][D]
+  // DEFERRED: header + two capture halves (e, k, G as in RECOMPUTE) used in
+  // turn by consecutive cycles; half[(epoch - 1) & 1] holds the pending commit
+  const int *ws_epoch;  // commits recorded so far
+  const int *ws_pend;   // [B] keep' of the last commit
+  int *ws_applied;      // [B][H_v] epoch up to which the state is materialised
+  float *dh_e[2], *dh_k[2], *dh_G[2];
+  float *state_w;       // DEFERRED: the state, written where a commit is applied
   uint32_t *status; // sticky device status word
-  int B, H_k, H_v, C, R, act;
+  int B, T, H_k, H_v, C, R, act;
   int overlap;      // GDN_VERIFY_OVERLAP: stage the state tile before the PDL wait
 };
 
@@ -289,11 +295,13 @@ constexpr int kMaxLayers = GDN_MAX_LAYERS;
 
 struct CommitParams {
   float *state[kMaxLayers];
-  const float *ws[kMaxLayers];
+  uint16_t *ring[kMaxLayers];  // nullptr in a flush
+  float *ws[kMaxLayers];
   const int32_t *keep;
   const uint8_t *active;
   int32_t *offsets;
-  int n_layers, B, T, H_k, H_v;
+  uint32_t *status;
+  int n_layers, B, T, H_k, H_v, C, R;
 };
 
 // Byte offsets of the RECOMPUTE workspace regions (each 256-byte aligned).
@@ -316,11 +324,28 @@ __host__ __device__ inline size_t snapshot_ws(int B, int T, int H_v, int D) {
   return sizeof(float) * size_t(T) * B * H_v * D * D;
 }
 
+// DEFERRED workspace: epoch at byte 0, pending keep [B], applied epochs
+// [B][H_v], then two RECOMPUTE-layout capture halves.
+struct DeferredWs {
+  size_t pend, applied, half0, half_bytes, total;
+};
+
+__host__ __device__ inline DeferredWs deferred_ws(int B, int T, int H_k, int H_v, int D) {
+  DeferredWs w;
+  w.pend = 256;
+  w.applied = w.pend + align256(sizeof(int) * size_t(B));
+  w.half0 = w.applied + align256(sizeof(int) * size_t(B) * H_v);
+  w.half_bytes = recompute_ws(B, T, H_k, H_v, D).total;
+  w.total = w.half0 + 2 * w.half_bytes;
+  return w;
+}
+
 // launchers (defined in the .cu files)
 cudaError_t launch_verify_32(const VerifyParams &p, int T, int mode, cudaStream_t s);
 cudaError_t launch_verify_64(const VerifyParams &p, int T, int mode, cudaStream_t s);
 cudaError_t launch_verify_128(const VerifyParams &p, int T, int mode, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, int D, int mode, cudaStream_t s);
+cudaError_t launch_flush(const CommitParams &p, int D, cudaStream_t s);
 size_t prefill_workspace_bytes(int B, int L, int H_k, int H_v, int D);
 cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g, const float *beta, float *state,
                            uint16_t *ring, int32_t *offsets, uint16_t *out, void *ws, int B, int L, int H_k,

@@ -153,16 +153,16 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
   const float w2 = bf2f(uint16_t(wr.y & 0xffff)), w3 = bf2f(uint16_t(wr.y >> 16));
   const int t0 = chunk * kChunk;
   // the three inputs before t0: from the prompt, or the committed window
+  // (ring slots 0..2)
   float h0, h1, h2;
   {
     float hv[kHist];
-    const int off = p.offsets[b];
 #pragma unroll
     for (int i = 0; i < kHist; ++i) {
       const int t = t0 - kHist + i;
       hv[i] = t >= L ? 0.f  // the padding chunk past the prompt
               : t >= 0 ? bf2f(p.x[(size_t(b) * L + t) * C + c])
-                       : bf2f(p.ring[(size_t(b) * R + ring_slot(off + t, R)) * C + c]);
+                       : bf2f(p.ring[(size_t(b) * R + kWinSlot + kHist + t) * C + c]);
     }
     h0 = hv[0], h1 = hv[1], h2 = hv[2];
   }
@@ -607,9 +607,10 @@ __global__ void __launch_bounds__(kStateThreads) prefill_state_kernel(const Pref
 }
 
 // ---------------------------------------------------------------------------
-// 4. ring: the raw inputs of the last three positions of window ++ prompt.
-//    Positions before the prompt already sit in their slots, so only prompt
-//    tokens are written.  Runs after the conv kernel has read the old window.
+// 4. ring: slots 0..2 become the raw inputs of the last three positions of
+//    window ++ prompt (for L < 3 partly the old window, read before any
+//    write by the same thread).  Runs after the conv kernel has read the old
+//    window.
 // ---------------------------------------------------------------------------
 __global__ void prefill_ring_kernel(const PrefillParams p) {
   const int b = blockIdx.y;
@@ -617,12 +618,15 @@ __global__ void prefill_ring_kernel(const PrefillParams p) {
   pdl_wait();
   pdl_trigger();
   if (c >= p.C) return;
-  const int off = p.offsets[b];
+  uint16_t *ring = p.ring + size_t(b) * p.R * p.C + c;
+  uint16_t w[kHist];
 #pragma unroll
   for (int i = 0; i < kHist; ++i) {
-    const int t = p.L - kHist + i;
-    if (t >= 0) p.ring[(size_t(b) * p.R + ring_slot(off + t, p.R)) * p.C + c] = p.x[(size_t(b) * p.L + t) * p.C + c];
+    const int t = p.L - kHist + i;  // prompt index; negative reaches the old window
+    w[i] = t >= 0 ? p.x[(size_t(b) * p.L + t) * p.C + c] : ring[size_t(kWinSlot + kHist + t) * p.C];
   }
+#pragma unroll
+  for (int i = 0; i < kHist; ++i) ring[size_t(kWinSlot + i) * p.C] = w[i];
 }
 
 template <int D>

@@ -59,26 +59,22 @@ __device__ __forceinline__ void conv1(const float (&w)[kWidth], const float (&xt
   }
 }
 
-// Load the taps, committed window and new inputs of channel c of row b and run
-// its conv; optionally copy the new raw inputs into the ring slots of their
-// positions.
+// Load the taps, the committed window (ring slots 0..2) and the new inputs of
+// channel c of row b and run its conv; optionally copy the new raw inputs into
+// ring slots 3..2+T.
 template <int T>
-__device__ __forceinline__ void conv_channel(const VerifyParams &p, int b, int c, int slot0, int wslot0,
-                                            bool write_ring, float (&y)[T]) {
+__device__ __forceinline__ void conv_channel(const VerifyParams &p, int b, int c, bool write_ring,
+                                            float (&y)[T]) {
   const int C = p.C, R = p.R;
   const uint2 wr = *reinterpret_cast<const uint2 *>(p.w + size_t(c) * kWidth);
   const float w[kWidth] = {bf2f(uint16_t(wr.x & 0xffff)), bf2f(uint16_t(wr.x >> 16)),
                            bf2f(uint16_t(wr.y & 0xffff)), bf2f(uint16_t(wr.y >> 16))};
-  const uint16_t *ringb = p.ring + size_t(b) * R * C + c;
+  uint16_t *ringb = p.ring + size_t(b) * R * C + c;
   const uint16_t *xb = p.x + size_t(b) * T * C + c;
   float xt[kHist + T];
   uint16_t xraw[T];
-  int slot = slot0;
 #pragma unroll
-  for (int i = 0; i < kHist; ++i) {
-    xt[i] = bf2f(ringb[size_t(slot) * C]);
-    slot = slot + 1 == R ? 0 : slot + 1;
-  }
+  for (int i = 0; i < kHist; ++i) xt[i] = bf2f(ringb[size_t(kWinSlot + i) * C]);
 #pragma unroll
   for (int t = 0; t < T; ++t) {
     xraw[t] = xb[size_t(t) * C];
@@ -86,13 +82,8 @@ __device__ __forceinline__ void conv_channel(const VerifyParams &p, int b, int c
   }
   conv1<T>(w, xt, p.act, y);
   if (write_ring) {
-    uint16_t *ringw = p.ring + size_t(b) * R * C + c;
-    int ws = wslot0;
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-      ringw[size_t(ws) * C] = xraw[t];
-      ws = ws + 1 == R ? 0 : ws + 1;
-    }
+    for (int t = 0; t < T; ++t) ringb[size_t(kNewSlot + t) * C] = xraw[t];
   }
 }
 
@@ -127,83 +118,97 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
   const bool leader = (lane & 3) == 0;     // four lanes share a row after the reduction
 
   // With GDN_VERIFY_OVERLAP the caller guarantees that nothing issued since
-  // the last call without the flag writes this call's state, ring, active
-  // mask or taps: the kernel lets the next kernel start at once and stages its
-  // state tiles before waiting for the preceding one.  Without the flag it
-  // waits first and only then lets the next kernel start, so a chain of
-  // flagged verifies can never run ahead of the last unflagged call.
+  // the last call without the flag writes this call's state or active mask:
+  // the kernel lets the next kernel start at once and stages its state tiles
+  // before waiting for the preceding one.  Without the flag it waits first
+  // and only then lets the next kernel start, so a chain of flagged verifies
+  // can never run ahead of the last unflagged call.
   if (p.overlap) {
     pdl_trigger();
   } else {
     pdl_wait();
     pdl_trigger();
   }
-  if (!p.active[b]) {
-    // Inactive / padding / finished rows are inert: zero output, no state,
-    // ring or workspace access.
-    if (p.overlap) pdl_wait();
-    for (int i = tid; i < T * D; i += 2 * D)
-      p.out[((size_t(b) * T + i / D) * H_v + h) * D + i % D] = 0;
-    return;
-  }
-
-  // ---- 1. stage the (row, head) state, 32 rows per bulk copy ----------------
+  const bool active = p.active[b] != 0;
   constexpr uint32_t kTileBytes = kTileRows * D * sizeof(float);
-  if (tid == 0) {
+  const float *Sg = p.state + (size_t(b) * H_v + h) * D * D;
+  auto stage_state = [&]() {
+    if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < NT; ++i) mbar_init(&sm.bar[i], 1);
-    fence_mbar_init();
-    const float *src = p.state + (size_t(b) * H_v + h) * D * D;
+      for (int i = 0; i < NT; ++i) mbar_init(&sm.bar[i], 1);
+      fence_mbar_init();
 #pragma unroll
-    for (int i = 0; i < NT; ++i) {
-      mbar_arrive_expect_tx(&sm.bar[i], kTileBytes);
-      bulk_g2s(sm.S + i * kTileRows * D, src + size_t(i) * kTileRows * D, kTileBytes, &sm.bar[i]);
+      for (int i = 0; i < NT; ++i) {
+        mbar_arrive_expect_tx(&sm.bar[i], kTileBytes);
+        bulk_g2s(sm.S + i * kTileRows * D, Sg + size_t(i) * kTileRows * D, kTileBytes, &sm.bar[i]);
+      }
     }
-  }
+  };
+  // ---- 1. stage the (row, head) state, 32 rows per bulk copy ----------------
+  if (active) stage_state();
   if (p.overlap) pdl_wait();
 
-  // ---- 2. conv + activation: one q or k channel of the key head per thread --
-  const int off = p.offsets[b];
-  const int slot0 = ring_slot(off - kHist, R);
-  const int wslot0 = ring_slot(off, R);
-  const bool qk_writer = (h % rep) == 0;  // one CTA per key head writes its q/k ring slots
-  {
-    const bool is_k = tid >= D;
-    const int ch = is_k ? tid - D : tid;
-    float y[T];
-    conv_channel<T>(p, b, (is_k ? H_k * D : 0) + hk * D + ch, slot0, wslot0, qk_writer, y);
-#pragma unroll
-    for (int t = 0; t < T; ++t) (is_k ? sm.k : sm.q)[t][ch] = y[t];
+  // DEFERRED: is a commit of this (row, head) still to be applied?
+  int E = 0, K = 0;
+  bool pending = false, mark = false;
+  if (MODE == GDN_COMMIT_DEFERRED) {
+    E = *p.ws_epoch;
+    const int A = p.ws_applied[size_t(b) * H_v + h];
+    K = p.ws_pend[b];
+    mark = E > A;
+    pending = mark && K >= 1;
   }
-  float gt[T], bt[T];
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
-    bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
+  if (!active) {
+    // Inactive / padding / finished rows are inert: zero output, no ring
+    // access.  A commit still pending from an earlier cycle is applied.
+    for (int i = tid; i < T * D; i += 2 * D) p.out[((size_t(b) * T + i / D) * H_v + h) * D + i % D] = 0;
+    if (!pending) {
+      if (mark && tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
+      return;
+    }
+    stage_state();
+    __syncthreads();
   }
-  // the v channels of the two rows this lane will hold, also before the barrier
-  // so their loads overlap the state copy
-  constexpr int ROWS_W = 16;  // state rows per warp: two groups of 8
-  const int jw0 = warp * ROWS_W;
-  float vrow[ROWS_W / 8][T];
-#pragma unroll
-  for (int grp8 = 0; grp8 < ROWS_W / 8; ++grp8)
-    conv_channel<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, slot0, wslot0, leader,
-                    vrow[grp8]);
-  __syncthreads();  // conv outputs and the initialised barriers are visible
 
-  float q[T][4], k[T][4];
+  const bool qk_writer = (h % rep) == 0;  // one CTA per key head writes its q/k ring slots
+  constexpr int ROWS_W = 16;              // state rows per warp: two groups of 8
+  const int jw0 = warp * ROWS_W;
+  float q[T][4], k[T][4], vrow[ROWS_W / 8][T];
+  float gt[T], bt[T];
+  if (active) {
+    // ---- 2. conv + activation: one q or k channel of the key head per thread
+    {
+      const bool is_k = tid >= D;
+      const int ch = is_k ? tid - D : tid;
+      float y[T];
+      conv_channel<T>(p, b, (is_k ? H_k * D : 0) + hk * D + ch, qk_writer, y);
 #pragma unroll
-  for (int t = 0; t < T; ++t) {
-    const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
-    const float4 kv = *reinterpret_cast<const float4 *>(&sm.k[t][4 * sub]);
-    q[t][0] = qv.x, q[t][1] = qv.y, q[t][2] = qv.z, q[t][3] = qv.w;
-    k[t][0] = kv.x, k[t][1] = kv.y, k[t][2] = kv.z, k[t][3] = kv.w;
+      for (int t = 0; t < T; ++t) (is_k ? sm.k : sm.q)[t][ch] = y[t];
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
+      bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
+    }
+    // the v channels of the rows this lane will hold, also before the barrier
+#pragma unroll
+    for (int grp8 = 0; grp8 < ROWS_W / 8; ++grp8)
+      conv_channel<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, leader, vrow[grp8]);
+    __syncthreads();  // conv outputs and the initialised barriers are visible
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
+      const float4 kv = *reinterpret_cast<const float4 *>(&sm.k[t][4 * sub]);
+      q[t][0] = qv.x, q[t][1] = qv.y, q[t][2] = qv.z, q[t][3] = qv.w;
+      k[t][0] = kv.x, k[t][1] = kv.y, k[t][2] = kv.z, k[t][3] = kv.w;
+    }
   }
 
   // ---- 3. per-head sums over the LPR lanes of a row group ------------------
   float red_h[NV];
-  {
+  float inv_q[T], inv_k[T], Gc[T], gam[T];
+  float decay[T][T];  // exp(G_t - G_s), s < t
+  if (active) {
     int n = 0;
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -220,15 +225,12 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
 #pragma unroll
       for (int s0 = 0; s0 <= t; ++s0)
         red_h[n++] = k[s0][0] * q[t][0] + k[s0][1] * q[t][1] + k[s0][2] * q[t][2] + k[s0][3] * q[t][3];
-  }
 #pragma unroll
-  for (int m = LPR / 2; m >= 1; m >>= 1)
+    for (int m = LPR / 2; m >= 1; m >>= 1)
 #pragma unroll
-    for (int i = 0; i < NV; ++i) red_h[i] += __shfl_xor_sync(0xffffffffu, red_h[i], m);
+      for (int i = 0; i < NV; ++i) red_h[i] += __shfl_xor_sync(0xffffffffu, red_h[i], m);
 
-  // ---- 4. per-head coefficients (every lane, in registers) -----------------
-  float inv_q[T], inv_k[T], Gc[T], gam[T];
-  {
+    // ---- 4. per-head coefficients (every lane, in registers) ---------------
     const float qs = 1.0f / sqrtf(float(D));
     float acc = 0.f;
 #pragma unroll
@@ -239,12 +241,17 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
       Gc[t] = acc;
       gam[t] = expf(acc);
     }
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+      for (int s0 = 0; s0 < t; ++s0) decay[t][s0] = expf(Gc[t] - Gc[s0]);
   }
-  float decay[T][T];  // exp(G_t - G_s), s < t
-#pragma unroll
-  for (int t = 0; t < T; ++t)
-#pragma unroll
-    for (int s0 = 0; s0 < t; ++s0) decay[t][s0] = expf(Gc[t] - Gc[s0]);
+
+  // DEFERRED: coefficients of the pending commit, S <- gamma S + sum_s c_s e_s k_s^T
+  // with the captures of the verify that preceded it
+  const int old = (E - 1) & 1, cur = E & 1;
+  float pc_gam = 0.f;
+  if (MODE == GDN_COMMIT_DEFERRED && pending) pc_gam = expf(p.dh_G[old][(size_t(b) * T + (K - 1)) * H_v + h]);
 
   // ---- 5. this warp's 16 rows, in two groups of 8 ---------------------------
   if (!mbar_wait_bounded(&sm.bar[jw0 / kTileRows], 0)) {
@@ -265,6 +272,36 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
 #pragma unroll
     for (int i = 0; i < RPL; ++i)
       s[i] = *reinterpret_cast<const float4 *>(&sm.S[(jw + grp + GPW * i) * D + 4 * sub]);
+    if (MODE == GDN_COMMIT_DEFERRED && pending) {
+      // apply the pending commit to these rows (same arithmetic as the eager
+      // RECOMPUTE commit) and write them back as the committed state
+      const float GK = p.dh_G[old][(size_t(b) * T + (K - 1)) * H_v + h];
+#pragma unroll
+      for (int i = 0; i < RPL; ++i)
+        s[i] = make_float4(pc_gam * s[i].x, pc_gam * s[i].y, pc_gam * s[i].z, pc_gam * s[i].w);
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t) {
+        if (t < K) {
+          const float c = expf(GK - p.dh_G[old][(size_t(b) * T + t) * H_v + h]);
+          const float4 kv =
+              *reinterpret_cast<const float4 *>(p.dh_k[old] + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub);
+          const float *ert = p.dh_e[old] + ((size_t(b) * T + t) * H_v + h) * D + jw;
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) {
+            const float f = c * ert[grp + GPW * i];
+            s[i].x = fmaf(f, kv.x, s[i].x);
+            s[i].y = fmaf(f, kv.y, s[i].y);
+            s[i].z = fmaf(f, kv.z, s[i].z);
+            s[i].w = fmaf(f, kv.w, s[i].w);
+          }
+        }
+      }
+      float *Sw = p.state_w + ((size_t(b) * H_v + h) * D + jw) * D;
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) st_f4(Sw + size_t(grp + GPW * i) * D + 4 * sub, s[i]);
+    }
+    if (!active) continue;
+
     float red[2 * T];
 #pragma unroll
     for (int mvec = 0; mvec < 2 * T; ++mvec) {
@@ -305,6 +342,7 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
         const size_t idx = ((size_t(b) * T + t) * H_v + h) * D + jrow;
         p.out[idx] = f2bf(o[t]);
         if (MODE == GDN_COMMIT_RECOMPUTE) p.ws_e[idx] = e[t];
+        if (MODE == GDN_COMMIT_DEFERRED) p.dh_e[cur][idx] = e[t];
       }
     }
     if (MODE == GDN_COMMIT_SNAPSHOT) {
@@ -328,18 +366,22 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
       }
     }
   }
+  if (MODE == GDN_COMMIT_DEFERRED && mark && tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
+  if (!active) return;
 
   // ---- 6. captures of the key head and decay --------------------------------
-  if (MODE == GDN_COMMIT_RECOMPUTE) {
+  if (MODE == GDN_COMMIT_RECOMPUTE || MODE == GDN_COMMIT_DEFERRED) {
+    float *wk = MODE == GDN_COMMIT_RECOMPUTE ? p.ws_k : p.dh_k[cur];
+    float *wG = MODE == GDN_COMMIT_RECOMPUTE ? p.ws_G : p.dh_G[cur];
     if (qk_writer && warp == 0 && grp == 0)
 #pragma unroll
       for (int t = 0; t < T; ++t)
-        st_f4(p.ws_k + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub,
+        st_f4(wk + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub,
               make_float4(k[t][0] * inv_k[t], k[t][1] * inv_k[t], k[t][2] * inv_k[t], k[t][3] * inv_k[t]));
     if (warp == 0 && lane < T) {
 #pragma unroll
       for (int t = 0; t < T; ++t)
-        if (lane == t) p.ws_G[(size_t(b) * T + t) * H_v + h] = Gc[t];
+        if (lane == t) wG[(size_t(b) * T + t) * H_v + h] = Gc[t];
     }
   }
 }
@@ -364,11 +406,13 @@ cudaError_t launch_verify_kernel(dim3 grid, dim3 block, cudaStream_t stream, con
 template <int D>
 cudaError_t launch_verify_d(const VerifyParams &p, int T, int mode, cudaStream_t stream) {
   const dim3 grid(p.H_v, p.B), block(2 * D);
-#define GDN_VERIFY_CASE(TT)                                                            \
-  case TT:                                                                             \
-    return mode == GDN_COMMIT_RECOMPUTE                                                \
-               ? launch_verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>(grid, block, stream, p) \
-               : launch_verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>(grid, block, stream, p);
+#define GDN_VERIFY_CASE(TT)                                                                   \
+  case TT:                                                                                    \
+    return mode == GDN_COMMIT_RECOMPUTE                                                       \
+               ? launch_verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>(grid, block, stream, p)    \
+               : mode == GDN_COMMIT_SNAPSHOT                                                  \
+                     ? launch_verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>(grid, block, stream, p) \
+                     : launch_verify_kernel<D, TT, GDN_COMMIT_DEFERRED>(grid, block, stream, p);
   switch (T) {
     GDN_VERIFY_CASE(1)
     GDN_VERIFY_CASE(2)

@@ -24,6 +24,7 @@ GDN_ACT_NONE = 0
 GDN_ACT_SILU = 1
 GDN_COMMIT_RECOMPUTE = 0
 GDN_COMMIT_SNAPSHOT = 1
+GDN_COMMIT_DEFERRED = 2
 GDN_VERIFY_OVERLAP = 0x100
 GDN_STATUS_TIMEOUT = 2
 GDN_STATUS_BAD_KEEP = 1
@@ -32,7 +33,7 @@ GDN_NOALLOC_WS_BYTES = 4 << 20
 
 EXPORTS = ("gdn_version", "gdn_last_error", "gdn_layer_workspace_bytes", "gdn_conv_verify",
            "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status",
-           "gdn_conv_verify_noalloc")
+           "gdn_conv_verify_noalloc", "gdn_flush")
 
 
 class GdnError(RuntimeError):
@@ -71,7 +72,9 @@ def _declare(lib):
     lib.gdn_conv_verify.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
     lib.gdn_commit.restype = ctypes.c_int
     lib.gdn_commit.argtypes = [D, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P), ctypes.POINTER(_P),
-                               _P, _P, _P, _P]
+                               ctypes.POINTER(_P), _P, _P, _P, _P]
+    lib.gdn_flush.restype = ctypes.c_int
+    lib.gdn_flush.argtypes = [D, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]
     lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_prefill_workspace_bytes.argtypes = [D, ctypes.c_int]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
@@ -184,18 +187,31 @@ def gdn_conv_verify_noalloc(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, 
     return int(used.value)
 
 
-def gdn_commit(d: gdn_dims, mode, states, layer_ws, keep, active, offsets, stream=None):
-    """states / layer_ws: sequences (one per layer) of tensors or int device pointers."""
+def _layer_ptrs(seq, what, dtype=None):
+    return (_P * max(len(seq), 1))(*[_ptr(t, f"{what}[{i}]", dtype) for i, t in enumerate(seq)])
+
+
+def gdn_commit(d: gdn_dims, mode, states, rings, layer_ws, keep, active, offsets, stream=None):
+    """states / rings / layer_ws: sequences (one per layer) of tensors or int device pointers."""
     torch = _t()
     n = len(states)
-    if len(layer_ws) != n:
-        raise ValueError("states and layer_ws must have one entry per layer")
-    sp = (_P * max(n, 1))(*[_ptr(s, f"state[{i}]", torch.float32) for i, s in enumerate(states)])
-    wp = (_P * max(n, 1))(*[_ptr(w, f"layer_ws[{i}]") for i, w in enumerate(layer_ws)])
-    rc = load().gdn_commit(ctypes.byref(d), mode, n, sp, wp, _ptr(keep, "keep", torch.int32),
-                           _ptr(active, "active", torch.uint8), _ptr(offsets, "offsets", torch.int32),
-                           _stream(stream))
+    if len(layer_ws) != n or len(rings) != n:
+        raise ValueError("states, rings and layer_ws must have one entry per layer")
+    rc = load().gdn_commit(ctypes.byref(d), mode, n, _layer_ptrs(states, "state", torch.float32),
+                           _layer_ptrs(rings, "ring", torch.bfloat16), _layer_ptrs(layer_ws, "layer_ws"),
+                           _ptr(keep, "keep", torch.int32), _ptr(active, "active", torch.uint8),
+                           _ptr(offsets, "offsets", torch.int32), _stream(stream))
     _check(rc, "gdn_commit")
+
+
+def gdn_flush(d: gdn_dims, mode, states, layer_ws, stream=None):
+    """Materialise commits a DEFERRED cycle left pending (no-op in other modes)."""
+    torch = _t()
+    if len(layer_ws) != len(states):
+        raise ValueError("states and layer_ws must have one entry per layer")
+    rc = load().gdn_flush(ctypes.byref(d), mode, len(states), _layer_ptrs(states, "state", torch.float32),
+                          _layer_ptrs(layer_ws, "layer_ws"), _stream(stream))
+    _check(rc, "gdn_flush")
 
 
 def gdn_prefill_workspace_bytes(d: gdn_dims, L: int) -> int:

@@ -19,9 +19,9 @@ cohorts of hybrid Qwen models):
 * log-decay g = -softplus(N(0, 1)) * 0.5  (so g <= 0, alpha = e^g in (0, 1]);
 * write strength beta = sigmoid(N(0, 1));
 * recurrent state S0 ~ N(0, 0.1^2) (std 0.1), fp32;
-* primed conv window ~ N(0, 1) bf16; ring slots outside the committed window
+* primed conv window ~ N(0, 1) bf16 in ring slots 0..2; the verify slots 3..
   hold bf16 NaN so that any read outside the window poisons the result;
-* committed offsets uniform in [3, 1000) so ring indices wrap arbitrarily;
+* committed offsets (bookkeeping only) uniform in [3, 1000);
 * keep per row uniform in {0..T}.
 """
 from __future__ import annotations
@@ -155,7 +155,8 @@ def layer_state(geom: Geometry, seed: int, n_layers: int = 1, offsets=None) -> d
     Returns numpy arrays:
       conv_w  uint16 bf16 [n_layers][C][4]
       state   float32     [n_layers][B][H_v][d_v][d_k]
-      ring    uint16 bf16 [n_layers][B][R][C]  (slot = absolute position mod R)
+      ring    uint16 bf16 [n_layers][B][R][C]  conv cache: slots 0..2 hold the
+              committed window (oldest first), slots 3.. are verify scratch
       offsets int32       [B]  committed tokens per row (shared by all layers)
     """
     g = geom
@@ -165,11 +166,7 @@ def layer_state(geom: Geometry, seed: int, n_layers: int = 1, offsets=None) -> d
         offsets = integers(seed, "offsets", (g.B,), 3, 1000)
     offsets = np.asarray(offsets, dtype=np.int32)
     ring = np.full((n_layers, g.B, g.R, g.C), BF16_NAN, dtype=np.uint16)
-    win = bf16_bits(normal(seed, "window", (n_layers, g.B, g.width - 1, g.C)))
-    for b in range(g.B):
-        for i in range(g.width - 1):
-            pos = int(offsets[b]) - (g.width - 1) + i
-            ring[:, b, pos % g.R, :] = win[:, b, i, :]
+    ring[:, :, : g.width - 1, :] = bf16_bits(normal(seed, "window", (n_layers, g.B, g.width - 1, g.C)))
     return {"conv_w": w, "state": s0, "ring": ring, "offsets": offsets}
 
 

@@ -34,15 +34,10 @@ def f64(bits: np.ndarray) -> np.ndarray:
     return synth.bf16_to_f32(bits).astype(np.float64)
 
 
-def ring_window(ring_bits: np.ndarray, offsets, R: int) -> np.ndarray:
-    """Committed conv window [B][C][3] (oldest first) read out of a ring [B][R][C]:
-    slot of absolute position p is p mod R, the window is offsets-3 .. offsets-1."""
-    B, _, C = ring_bits.shape
-    out = np.empty((B, C, 3))
-    for b in range(B):
-        for i in range(3):
-            out[b, :, i] = f64(ring_bits[b, (int(offsets[b]) - 3 + i) % R])
-    return out
+def ring_window(ring_bits: np.ndarray) -> np.ndarray:
+    """Committed conv window [B][C][3] (oldest first) of a ring [B][R][C]: the
+    window lives in slots 0..2."""
+    return f64(np.ascontiguousarray(np.transpose(ring_bits[:, :3, :], (0, 2, 1))))
 
 
 def check_out(o_gpu: torch.Tensor, o_ref: np.ndarray, what: str):
@@ -79,7 +74,8 @@ class GpuStack:
         self.offsets = torch.from_numpy(st["offsets"].copy()).cuda()
         self.active = torch.from_numpy(active.copy()).cuda()
         nbytes = L.gdn_layer_workspace_bytes(self.dims, mode)
-        self.ws = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(n_layers)]
+        # zero-filled once: required by DEFERRED, harmless for the other modes
+        self.ws = [torch.zeros(nbytes, dtype=torch.uint8, device="cuda") for _ in range(n_layers)]
         g = geom
         self.out = torch.empty((n_layers, g.B, g.T, g.H_v, g.d), dtype=torch.bfloat16, device="cuda")
 
@@ -92,8 +88,13 @@ class GpuStack:
                           self.out[layer], self.ws[layer])
 
     def commit(self, keep):
-        L.gdn_commit(self.dims, self.mode, [self.state[l] for l in range(self.n)], self.ws,
+        L.gdn_commit(self.dims, self.mode, [self.state[l] for l in range(self.n)],
+                     [self.ring[l] for l in range(self.n)], self.ws,
                      torch.from_numpy(np.asarray(keep, np.int32)).cuda(), self.active, self.offsets)
+
+    def flush(self):
+        """Materialise pending DEFERRED commits so `state` holds the committed state."""
+        L.gdn_flush(self.dims, self.mode, [self.state[l] for l in range(self.n)], self.ws)
 
 
 class OracleStack:
@@ -103,7 +104,7 @@ class OracleStack:
         self.geom, self.n = geom, n_layers
         self.S = st["state"].copy()
         self.w = [f64(st["conv_w"][l]) for l in range(n_layers)]
-        self.win = [ring_window(st["ring"][l], st["offsets"], geom.R) for l in range(n_layers)]
+        self.win = [ring_window(st["ring"][l]) for l in range(n_layers)]
         self.offsets = st["offsets"].copy()
         self.active = active.copy()
         self.pending = [None] * n_layers
@@ -148,7 +149,7 @@ class OracleUnit:
         self.ch = unit_channels(geom, h)
         self.S = np.ascontiguousarray(st["state"][layer, b:b + 1, h:h + 1]).copy()
         self.w = f64(st["conv_w"][layer][self.ch])
-        win = ring_window(st["ring"][layer][b:b + 1], st["offsets"][b:b + 1], geom.R)
+        win = ring_window(st["ring"][layer][b:b + 1])
         self.win = np.ascontiguousarray(win[:, self.ch])
         self.offset = np.array([st["offsets"][b]], np.int32)
 

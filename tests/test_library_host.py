@@ -28,7 +28,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert {"gdn_conv_verify", "gdn_commit", "gdn_prefill_chunked"} <= names
+    assert {"gdn_conv_verify", "gdn_commit", "gdn_flush", "gdn_prefill_chunked"} <= names
     missing = [n for n in sorted(names) if not hasattr(lib, n)]
     assert not missing, f"declared but not exported: {missing}"
     assert set(L.EXPORTS) <= names
@@ -93,13 +93,44 @@ def test_commit_argument_checks(lib):
     d = L.dims(8, 2, 16, 32, 128)
     P = ctypes.c_void_p
     arr = (P * 1)(1 << 20)
-    assert lib.gdn_commit(ctypes.byref(d), 0, 0, arr, arr, 1 << 20, 1 << 20, 1 << 20, None) == L.GDN_ERR_INVALID_ARG
-    assert lib.gdn_commit(ctypes.byref(d), 0, L.GDN_MAX_LAYERS + 1, arr, arr, 1 << 20, 1 << 20, 1 << 20,
+    g = 1 << 20
+    assert lib.gdn_commit(ctypes.byref(d), 0, 0, arr, arr, arr, g, g, g, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_commit(ctypes.byref(d), 0, L.GDN_MAX_LAYERS + 1, arr, arr, arr, g, g, g,
                           None) == L.GDN_ERR_INVALID_ARG
     bad = (P * 1)(None)
-    assert lib.gdn_commit(ctypes.byref(d), 0, 1, bad, arr, 1 << 20, 1 << 20, 1 << 20, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, bad, arr, arr, g, g, g, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, bad, arr, g, g, g, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, None, arr, g, g, g, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, arr, bad, g, g, g, None) == L.GDN_ERR_INVALID_ARG
     mis = (P * 1)((1 << 20) + 8)
-    assert lib.gdn_commit(ctypes.byref(d), 0, 1, mis, arr, 1 << 20, 1 << 20, 1 << 20, None) == L.GDN_ERR_MISALIGNED
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, mis, arr, arr, g, g, g, None) == L.GDN_ERR_MISALIGNED
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, mis, arr, g, g, g, None) == L.GDN_ERR_MISALIGNED
+    assert lib.gdn_commit(ctypes.byref(d), 5, 1, arr, arr, arr, g, g, g, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, arr, arr, None, g, g, None) == L.GDN_ERR_INVALID_ARG
+
+
+def test_flush_argument_checks(lib):
+    d = L.dims(8, 2, 16, 32, 128)
+    P = ctypes.c_void_p
+    arr = (P * 1)(1 << 20)
+    bad = (P * 1)(None)
+    assert lib.gdn_flush(ctypes.byref(d), L.GDN_COMMIT_DEFERRED, 0, arr, arr, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_flush(ctypes.byref(d), L.GDN_COMMIT_DEFERRED, 1, bad, arr, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_flush(ctypes.byref(d), L.GDN_COMMIT_DEFERRED, 1, arr, bad, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_flush(ctypes.byref(d), 7, 1, arr, arr, None) == L.GDN_ERR_INVALID_ARG
+    # the eager modes leave nothing pending: a flush launches nothing
+    assert lib.gdn_flush(ctypes.byref(d), L.GDN_COMMIT_RECOMPUTE, 1, arr, arr, None) == L.GDN_OK
+    assert lib.gdn_flush(ctypes.byref(d), L.GDN_COMMIT_SNAPSHOT, 1, arr, arr, None) == L.GDN_OK
+
+
+def test_deferred_workspace_size(lib):
+    d = L.dims(8, 2, 16, 32, 128)
+    rec = lib.gdn_layer_workspace_bytes(ctypes.byref(d), L.GDN_COMMIT_RECOMPUTE)
+    dfr = lib.gdn_layer_workspace_bytes(ctypes.byref(d), L.GDN_COMMIT_DEFERRED)
+    # two capture halves (one per epoch parity) plus the epoch, keep and
+    # applied-epoch words
+    assert dfr >= 2 * rec + 4 + 8 * 4 + 8 * 32 * 4
+    assert dfr % 256 == 0
 
 
 def test_empty_batch_is_a_no_op(lib):
@@ -107,7 +138,8 @@ def test_empty_batch_is_a_no_op(lib):
     assert lib.gdn_conv_verify(ctypes.byref(d), 0, *([None] * 10), 0, None) == L.GDN_OK
     P = ctypes.c_void_p
     arr = (P * 1)(1 << 20)
-    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, arr, None, None, None, None) == L.GDN_OK
+    assert lib.gdn_commit(ctypes.byref(d), 0, 1, arr, arr, arr, None, None, None, None) == L.GDN_OK
+    assert lib.gdn_flush(ctypes.byref(d), L.GDN_COMMIT_DEFERRED, 1, arr, arr, None) == L.GDN_OK
 
 
 def declared_arity():

@@ -54,14 +54,14 @@ def test_prefill_matches_sequential_oracle(gdn, shape):
     gpu = GpuStack(geom, st, synth.active_mask(B), L.GDN_COMMIT_RECOMPUTE, 1)
     out = gpu_prefill(gpu, 0, pr, Lp)
     S = st["state"][0].copy()
-    win = ring_window(st["ring"][0], st["offsets"], geom.R)
+    win = ring_window(st["ring"][0])
     off = st["offsets"].copy()
     o_ref = oracle.prefill(f64(pr["x"]), f64(st["conv_w"][0]), win, pr["g"], pr["beta"], S, off, H_k=H_k)
     torch.cuda.synchronize()
     check_out(out, o_ref, "prefill outputs")
     check_state(gpu.state[0].cpu().numpy(), S, "prefill final state")
     assert np.array_equal(gpu.offsets.cpu().numpy(), off)
-    assert np.array_equal(ring_window(host_bits(gpu.ring[0]), off, geom.R), win), "primed conv window"
+    assert np.array_equal(ring_window(host_bits(gpu.ring[0])), win), "primed conv window"
 
 
 def test_prefill_then_verify_commit(gdn):
@@ -91,7 +91,7 @@ def _unit_prefill(st, pr, geom, b, h):
     """Oracle priming of one (row, value head), sliced out of the full inputs."""
     ch = unit_channels(geom, h)
     S = np.ascontiguousarray(st["state"][0, b:b + 1, h:h + 1]).copy()
-    win = ring_window(st["ring"][0][b:b + 1], st["offsets"][b:b + 1], geom.R)[:, ch].copy()
+    win = ring_window(st["ring"][0][b:b + 1])[:, ch].copy()
     off = st["offsets"][b:b + 1].copy()
     o = oracle.prefill(f64(pr["x"][b:b + 1][:, :, ch]), f64(st["conv_w"][0][ch]), win,
                        pr["g"][b:b + 1, :, h:h + 1], pr["beta"][b:b + 1, :, h:h + 1], S, off, H_k=1)
@@ -117,7 +117,7 @@ def test_prime_long_prompt(gdn, Lp, heads):
         check_state(gpu.state[0, 0, h].cpu().numpy()[None], S_ref[None], f"head {h} primed state")
         S_after[h] = S_ref
     assert gpu.offsets[0].item() == Lp
-    win = ring_window(host_bits(gpu.ring[0]), np.array([Lp]), geom.R)[0]
+    win = ring_window(host_bits(gpu.ring[0]))[0]
     assert np.array_equal(win, f64(pr["x"][0, Lp - 3:Lp]).T), "primed window = last three prompt inputs"
     # one verify + commit on the primed state, against the oracle continuing
     # from its own primed state

@@ -16,14 +16,21 @@ from tests.gdn_harness import (GpuStack, OracleStack, OracleUnit, check_out, che
                                host_bits, ring_window)
 
 pytestmark = pytest.mark.gpu
-MODES = [L.GDN_COMMIT_RECOMPUTE, L.GDN_COMMIT_SNAPSHOT]
-MODE_IDS = ["recompute", "snapshot"]
+MODES = [L.GDN_COMMIT_RECOMPUTE, L.GDN_COMMIT_SNAPSHOT, L.GDN_COMMIT_DEFERRED]
+MODE_IDS = ["recompute", "snapshot", "deferred"]
 
 
-def run_cycles(geom, seed, active, mode, n_layers, n_cycles, keeps=None, offsets=None):
+def run_cycles(geom, seed, active, mode, n_layers, n_cycles, keeps=None, offsets=None, flush_every=None):
+    """Cycles of verify (every layer) + grouped commit against the oracle.
+
+    Outputs, offsets and conv windows are compared every cycle.  The state is
+    compared every cycle in the eager modes; in DEFERRED mode (where the state
+    buffer lags until the next verify) after a flush every `flush_every`
+    cycles and at the end, so that the apply-in-verify path runs in between."""
     st = synth.layer_state(geom, seed, n_layers, offsets=offsets)
     gpu = GpuStack(geom, st, active, mode, n_layers)
     orc = OracleStack(geom, st, active, n_layers)
+    deferred = mode == L.GDN_COMMIT_DEFERRED
     for c in range(n_cycles):
         cy = synth.cycle_inputs(geom, seed, c, n_layers)
         keep = cy["keep"] if keeps is None else np.asarray(keeps[c], np.int32)
@@ -36,12 +43,16 @@ def run_cycles(geom, seed, active, mode, n_layers, n_cycles, keeps=None, offsets
                 assert torch.all(gpu.out[l][torch.from_numpy(inactive).cuda()] == 0)
         gpu.commit(keep)
         status = orc.commit(keep)
+        last = c == n_cycles - 1
+        if deferred and (last or (flush_every and c % flush_every == flush_every - 1)):
+            gpu.flush()
         torch.cuda.synchronize()
         assert np.array_equal(gpu.offsets.cpu().numpy(), orc.offsets), f"cycle {c} offsets"
-        check_state(gpu.state.cpu().numpy(), orc.S, f"cycle {c} state")
+        if not deferred or last or (flush_every and c % flush_every == flush_every - 1):
+            check_state(gpu.state.cpu().numpy(), orc.S, f"cycle {c} state")
         ring = host_bits(gpu.ring)
         for l in range(n_layers):
-            win = ring_window(ring[l], orc.offsets, geom.R)
+            win = ring_window(ring[l])
             assert np.array_equal(win, orc.win[l]), f"cycle {c} layer {l} conv window"
         assert L.gdn_get_status(clear=True) == status
     return gpu, orc
@@ -74,8 +85,8 @@ def test_shape_sweep(gdn, shape, mode):
     B, T, T_max, H_k, H_v, d = shape
     geom = synth.Geometry(B=B, T=T, H_k=H_k, H_v=H_v, d=d, T_max=T_max)
     active = synth.active_mask(B, (B - 1,) if B > 2 else ())
-    keeps = [[(b + c) % (T + 1) for b in range(B)] for c in range(3)]
-    run_cycles(geom, 10 + T, active, mode, 2, 3, keeps)
+    keeps = [[(b + c) % (T + 1) for b in range(B)] for c in range(4)]
+    run_cycles(geom, 10 + T, active, mode, 2, 4, keeps, flush_every=2)
 
 
 def test_no_activation(gdn):
@@ -98,11 +109,14 @@ def test_keep_zero_restores_bit_exact(gdn, mode):
     gpu.commit(np.zeros(4, np.int32))
     torch.cuda.synchronize()
     assert torch.equal(gpu.state, before_state), "keep=0 must leave state bytes untouched"
+    if mode == L.GDN_COMMIT_DEFERRED:
+        gpu.flush()
+        torch.cuda.synchronize()
+        assert torch.equal(gpu.state, before_state), "a keep=0 commit leaves nothing pending"
     assert np.array_equal(gpu.offsets.cpu().numpy(), st["offsets"])
     ring = host_bits(gpu.ring)
     for l in range(2):
-        assert np.array_equal(ring_window(ring[l], st["offsets"], geom.R),
-                              ring_window(before_ring[l], st["offsets"], geom.R))
+        assert np.array_equal(ring_window(ring[l]), ring_window(before_ring[l]))
     # the inactive row's ring bytes are untouched entirely, not just its window
     assert np.array_equal(ring[:, 1], before_ring[:, 1])
 
@@ -196,7 +210,7 @@ def test_guard_regions_untouched(gdn):
     L.gdn_conv_verify(d, L.GDN_COMMIT_RECOMPUTE, dev_bf16(cy["x"][0]), dev_bf16(st["conv_w"][0]),
                       torch.from_numpy(cy["g"][0]).cuda(), torch.from_numpy(cy["beta"][0]).cuda(),
                       state, ring, offs, act, out, ws)
-    L.gdn_commit(d, L.GDN_COMMIT_RECOMPUTE, [state], [ws], torch.tensor([3, 1, 2], dtype=torch.int32).cuda(),
+    L.gdn_commit(d, L.GDN_COMMIT_RECOMPUTE, [state], [ring], [ws], torch.tensor([3, 1, 2], dtype=torch.int32).cuda(),
                  act, offs)
     torch.cuda.synchronize()
     for big in (g_state, g_ring, g_out, g_ws):
@@ -242,7 +256,7 @@ def test_stack_30_layers_256_cycles_sampled(gdn):
             for u in units:
                 check_state(gpu.state[u.layer, u.b, u.h].cpu().numpy()[None], u.S[0], f"cycle {c} unit state")
                 ring = host_bits(gpu.ring[u.layer, u.b:u.b + 1])
-                win = ring_window(ring, offsets[u.b:u.b + 1], geom.R)[:, u.ch]
+                win = ring_window(ring)[:, u.ch]
                 assert np.array_equal(win, u.win), f"cycle {c} unit window"
     assert L.gdn_get_status(clear=True) == 0
 
@@ -276,3 +290,84 @@ def test_unknown_mode_flag_rejected(gdn):
                           torch.from_numpy(cy["g"][0]).cuda(), torch.from_numpy(cy["beta"][0]).cuda(),
                           gpu.state[0], gpu.ring[0], gpu.offsets, gpu.active, gpu.out[0], gpu.ws[0])
     assert ei.value.code == L.GDN_ERR_INVALID_ARG
+
+
+def _cycle_runs(geom, st, masks, keeps, n_layers, mode, overlap_all=False, repeat_verify=False):
+    """Outputs of every cycle, then the (flushed) state, offsets and rings."""
+    gpu = GpuStack(geom, st, masks[0], mode, n_layers)
+    outs = []
+    for c, keep in enumerate(keeps):
+        gpu.active.copy_(torch.from_numpy(masks[c]))
+        cy = synth.cycle_inputs(geom, 30, c, n_layers)
+        for l in range(n_layers):
+            # flagged unless this layer's verify repeats (its first pass may
+            # have written the state) or the active mask was just rewritten
+            same_mask = c > 0 and np.array_equal(masks[c], masks[c - 1])
+            for rep in range(2 if repeat_verify else 1):
+                flag = overlap_all and rep == 0 and (l > 0 or same_mask)
+                gpu.verify(l, cy["x"][l], cy["g"][l], cy["beta"][l], overlap=flag)
+        outs.append(gpu.out.clone())
+        gpu.commit(np.asarray(keep, np.int32))
+    if mode == L.GDN_COMMIT_DEFERRED:
+        gpu.flush()
+    torch.cuda.synchronize()
+    return outs, gpu.state.clone(), host_bits(gpu.ring), gpu.offsets.clone()
+
+
+@pytest.mark.parametrize("repeat_verify", [False, True], ids=["once", "repeated"])
+def test_deferred_bit_identical_to_recompute(gdn, repeat_verify):
+    """DEFERRED applies a commit inside the next verify with the arithmetic of
+    the eager commit: every output, and the flushed state, equals RECOMPUTE bit
+    for bit.  Rows switch between active and inactive with commits pending, and
+    every layer's verify is flagged GDN_VERIFY_OVERLAP in DEFERRED mode."""
+    geom = synth.Geometry(B=4, T=3, H_k=2, H_v=4, d=128, T_max=4)
+    st = synth.layer_state(geom, 30, 3)
+    masks = [synth.active_mask(4), synth.active_mask(4, (1,)), synth.active_mask(4, (1,)),
+             synth.active_mask(4, (1, 2)), synth.active_mask(4, (3,)), synth.active_mask(4)]
+    keeps = [[3, 2, 1, 0], [1, 3, 3, 2], [2, 0, 3, 1], [0, 1, 2, 3], [2, 2, 0, 3], [3, 0, 1, 1]]
+    ref = _cycle_runs(geom, st, masks, keeps, 3, L.GDN_COMMIT_RECOMPUTE, repeat_verify=repeat_verify)
+    dfr = _cycle_runs(geom, st, masks, keeps, 3, L.GDN_COMMIT_DEFERRED, overlap_all=True,
+                      repeat_verify=repeat_verify)
+    for c, (a, b) in enumerate(zip(ref[0], dfr[0])):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"cycle {c} outputs"
+    assert torch.equal(ref[1], dfr[1]), "flushed state"
+    assert np.array_equal(ref[2], dfr[2]) and torch.equal(ref[3], dfr[3])
+    assert L.gdn_get_status(clear=True) == 0
+
+
+def test_deferred_flush_idempotent(gdn):
+    geom = synth.Geometry(B=3, T=2, H_k=1, H_v=2, d=64)
+    st = synth.layer_state(geom, 31, 2)
+    gpu = GpuStack(geom, st, synth.active_mask(3), L.GDN_COMMIT_DEFERRED, 2)
+    cy = synth.cycle_inputs(geom, 31, 0, 2)
+    for l in range(2):
+        gpu.verify(l, cy["x"][l], cy["g"][l], cy["beta"][l])
+    gpu.commit(np.array([2, 0, 1], np.int32))
+    torch.cuda.synchronize()
+    assert torch.equal(gpu.state, torch.from_numpy(st["state"]).cuda()), "DEFERRED commit writes no state"
+    gpu.flush()
+    torch.cuda.synchronize()
+    once = gpu.state.clone()
+    assert not torch.equal(once[:, 0], torch.from_numpy(st["state"][:, 0]).cuda())
+    assert torch.equal(once[:, 1], torch.from_numpy(st["state"][:, 1]).cuda()), "keep=0 row unchanged"
+    gpu.flush()
+    torch.cuda.synchronize()
+    assert torch.equal(gpu.state, once), "a second flush applies nothing"
+    # and the next verify must not apply the commit again
+    orc_state = once.clone()
+    cy1 = synth.cycle_inputs(geom, 31, 1, 2)
+    gpu.verify(0, cy1["x"][0], cy1["g"][0], cy1["beta"][0])
+    torch.cuda.synchronize()
+    assert torch.equal(gpu.state[0], orc_state[0])
+
+
+def test_deferred_rejected_by_noalloc(gdn):
+    geom = synth.TINY
+    st = synth.layer_state(geom, 0, 1)
+    gpu = GpuStack(geom, st, synth.active_mask(1), L.GDN_COMMIT_DEFERRED, 1)
+    cy = synth.cycle_inputs(geom, 0, 0, 1)
+    with pytest.raises(L.GdnError) as ei:
+        L.gdn_conv_verify_noalloc(gpu.dims, L.GDN_COMMIT_DEFERRED, dev_bf16(cy["x"][0]), gpu.w[0],
+                                  torch.from_numpy(cy["g"][0]).cuda(), torch.from_numpy(cy["beta"][0]).cuda(),
+                                  gpu.state[0], gpu.ring[0], gpu.offsets, gpu.active, gpu.out[0])
+    assert ei.value.code in (L.GDN_ERR_INVALID_ARG, L.GDN_ERR_UNSUPPORTED)

@@ -43,9 +43,9 @@ def test_noalloc_matches_allocated_workspace_two_calls(gdn):
         ref_out = ref.out[0].float().cpu().numpy().astype(np.float64)
         check_out(new.out[0], ref_out, f"call {call} outputs vs gdn_conv_verify")
         assert np.array_equal(host_bits(new.ring), host_bits(ref.ring)), f"call {call} ring"
-        L.gdn_commit(ref.dims, ref.mode, [ref.state[0]], ref.ws, torch.from_numpy(keep).cuda(), ref.active,
+        L.gdn_commit(ref.dims, ref.mode, [ref.state[0]], [ref.ring[0]], ref.ws, torch.from_numpy(keep).cuda(), ref.active,
                      ref.offsets)
-        L.gdn_commit(new.dims, new.mode, [new.state[0]], [scratch], torch.from_numpy(keep).cuda(), new.active,
+        L.gdn_commit(new.dims, new.mode, [new.state[0]], [new.ring[0]], [scratch], torch.from_numpy(keep).cuda(), new.active,
                      new.offsets)
         torch.cuda.synchronize()
         check_state(new.state.cpu().numpy(), ref.state.cpu().numpy(), f"call {call} committed state")
