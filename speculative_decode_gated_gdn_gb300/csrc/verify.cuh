@@ -1,14 +1,15 @@
 // verify.cuh -- the fused conv + L2-norm + gated-delta-rule verify kernel.
 //
-// Work decomposition.  One CTA of 2*d threads owns one (row b, value head h):
+// Work decomposition.  One CTA of 2d threads owns one (row b, value head h):
 // its whole d_v x d_k state (64 KiB at d = 128) is staged in shared memory by
 // d/32 bulk copies on the TMA engine, issued at entry, each completing on its
-// own mbarrier.  Each thread convolves one q or k channel of the key head;
-// the conv outputs are exchanged at the kernel's one block barrier, after
-// which every warp owns 16 state rows (two groups of 8) and works alone.
-// Lane l works on the d_k segment [4*(l % LPR), +4) of its rows.  A layer
-// occupies about 1.3 CTAs per SM at B = 8, so with GDN_VERIFY_OVERLAP the next
-// layer's CTAs fit beside it and stream their state while this one computes.
+// own mbarrier.  The threads convolve the q and k channels of the key head
+// (one per thread); the conv outputs are exchanged at the kernel's one block
+// barrier, after which every warp owns 16 state rows (two groups of 8) and
+// works alone.  Lane l works on the d_k segment [4*(l % LPR), +4) of its
+// rows.  A layer occupies about 1.3 CTAs per SM at B = 8, so with
+// GDN_VERIFY_OVERLAP part of the next layer's CTAs fit beside it and stream
+// their state while this one computes.
 //
 // The pre-verification state S_0 is only read ("MTP inference: review and
 // commit structure", Functional commits item 2: speculative transactions with
@@ -44,63 +45,91 @@
 
 namespace gdn {
 
-// Causal conv of one channel over T new positions: window xt[0..2] (oldest
-// first) followed by the new inputs; taps w[0..3], w[3] on the current token.
+// Raw conv inputs of one channel of one row: taps w[0..3] (w[3] on the
+// current token), the committed window (ring slots 0..2, oldest first) and
+// the T new inputs, all as bf16 bit patterns.  Loading every channel a
+// thread needs before any arithmetic or store keeps the conv to a single
+// round trip to memory.
 template <int T>
-__device__ __forceinline__ void conv1(const float (&w)[kWidth], const float (&xt)[kHist + T], int act,
-                                      float (&y)[T]) {
+struct ConvIn {
+  uint2 w;
+  uint16_t win[kHist];
+  uint16_t x[T];
+};
+
+template <int T>
+__device__ __forceinline__ void conv_load(const VerifyParams &p, int b, int c, ConvIn<T> &in) {
+  const int C = p.C;
+  in.w = *reinterpret_cast<const uint2 *>(p.w + size_t(c) * kWidth);
+  const uint16_t *ringb = p.ring + size_t(b) * p.R * C + c;
+  const uint16_t *xb = p.x + size_t(b) * T * C + c;
+#pragma unroll
+  for (int i = 0; i < kHist; ++i) in.win[i] = ringb[size_t(kWinSlot + i) * C];
+#pragma unroll
+  for (int t = 0; t < T; ++t) in.x[t] = xb[size_t(t) * C];
+}
+
+// Causal conv over the T new positions, then the activation.
+template <int T>
+__device__ __forceinline__ void conv_eval(const ConvIn<T> &in, int act, float (&y)[T]) {
+  const float w0 = bf2f(uint16_t(in.w.x & 0xffff)), w1 = bf2f(uint16_t(in.w.x >> 16));
+  const float w2 = bf2f(uint16_t(in.w.y & 0xffff)), w3 = bf2f(uint16_t(in.w.y >> 16));
+  float xt[kHist + T];
+#pragma unroll
+  for (int i = 0; i < kHist; ++i) xt[i] = bf2f(in.win[i]);
+#pragma unroll
+  for (int t = 0; t < T; ++t) xt[kHist + t] = bf2f(in.x[t]);
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    float acc = w[0] * xt[t];
-    acc = fmaf(w[1], xt[t + 1], acc);
-    acc = fmaf(w[2], xt[t + 2], acc);
-    acc = fmaf(w[3], xt[t + 3], acc);
+    float acc = w0 * xt[t];
+    acc = fmaf(w1, xt[t + 1], acc);
+    acc = fmaf(w2, xt[t + 2], acc);
+    acc = fmaf(w3, xt[t + 3], acc);
     y[t] = act ? silu_fast(acc) : acc;
   }
 }
 
-// Load the taps, the committed window (ring slots 0..2) and the new inputs of
-// channel c of row b and run its conv; optionally copy the new raw inputs into
-// ring slots 3..2+T.
+// The new raw inputs of channel c go to ring slots 3..2+T.
 template <int T>
-__device__ __forceinline__ void conv_channel(const VerifyParams &p, int b, int c, bool write_ring,
-                                            float (&y)[T]) {
-  const int C = p.C, R = p.R;
-  const uint2 wr = *reinterpret_cast<const uint2 *>(p.w + size_t(c) * kWidth);
-  const float w[kWidth] = {bf2f(uint16_t(wr.x & 0xffff)), bf2f(uint16_t(wr.x >> 16)),
-                           bf2f(uint16_t(wr.y & 0xffff)), bf2f(uint16_t(wr.y >> 16))};
-  uint16_t *ringb = p.ring + size_t(b) * R * C + c;
-  const uint16_t *xb = p.x + size_t(b) * T * C + c;
-  float xt[kHist + T];
-  uint16_t xraw[T];
+__device__ __forceinline__ void conv_store_ring(const VerifyParams &p, int b, int c, const ConvIn<T> &in) {
+  uint16_t *ringb = p.ring + size_t(b) * p.R * p.C + c;
 #pragma unroll
-  for (int i = 0; i < kHist; ++i) xt[i] = bf2f(ringb[size_t(kWinSlot + i) * C]);
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    xraw[t] = xb[size_t(t) * C];
-    xt[kHist + t] = bf2f(xraw[t]);
-  }
-  conv1<T>(w, xt, p.act, y);
-  if (write_ring) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) ringb[size_t(kNewSlot + t) * C] = xraw[t];
-  }
+  for (int t = 0; t < T; ++t) ringb[size_t(kNewSlot + t) * p.C] = in.x[t];
 }
 
-// Shared memory of one verify CTA: the (row, head) state tile and the conv
-// outputs of its key head.
+// Shared memory of one verify CTA: the (row, head) state tile, the conv
+// outputs of its key head and, in DEFERRED mode, the captures of the commit
+// still to be applied (e_t of the head, normalised k_t of the key head).
 template <int D, int T>
 struct VerifySmem {
   float S[D * D];
   float q[T][D];
   float k[T][D];
+  float ce[T][D];
+  float ck[T][D];
   uint64_t bar[D / kTileRows];
+  uint64_t cbar;
+};
+
+// Threads per verify CTA: 2d (8 warps at d = 128, 16 state rows per warp).
+// Measured at B = 8, T = 2: d threads (3 CTAs per SM, 32 rows per warp) make
+// a layer about 1 us slower, the longer per-warp row loop costing more than
+// the deeper residency gains.
+template <int D, int T>
+struct VerifyShape {
+  static constexpr int kThreads = 2 * D;
+  static constexpr int kMinBlocks = T <= 4 ? 2 : 1;
 };
 
 template <int D, int T, int MODE>
-__global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>::kMinBlocks)
+    verify_kernel(const VerifyParams p) {
   using G = RowLanes<D>;
   constexpr int RPL = G::RPL, GPW = G::GPW, LPR = G::LPR;
+  constexpr int NTHR = VerifyShape<D, T>::kThreads, NWARP = NTHR / 32;
+  constexpr int ROWS_W = D / NWARP;   // state rows per warp, in groups of 8
+  constexpr int NGRP = ROWS_W / 8;
+  static_assert(ROWS_W % 8 == 0 && NWARP * ROWS_W == D, "rows must split evenly over warps");
   constexpr int NT = D / kTileRows;   // 32-row tiles, one bulk copy and barrier each
   // per-head reductions: |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t)
   constexpr int NKK = T * (T - 1) / 2, NKQ = T * (T + 1) / 2, NV = 2 * T + NKK + NKQ;
@@ -111,7 +140,7 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane % LPR, grp = lane / LPR;
-  const int H_v = p.H_v, H_k = p.H_k, R = p.R;
+  const int H_v = p.H_v, H_k = p.H_k;
   const int rep = H_v / H_k;
   const int hk = h / rep;
   const int istar = row_of_lane<D>(lane);  // row (within a group of 8) this lane holds after a reduction
@@ -135,9 +164,6 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
   auto stage_state = [&]() {
     if (tid == 0) {
 #pragma unroll
-      for (int i = 0; i < NT; ++i) mbar_init(&sm.bar[i], 1);
-      fence_mbar_init();
-#pragma unroll
       for (int i = 0; i < NT; ++i) {
         mbar_arrive_expect_tx(&sm.bar[i], kTileBytes);
         bulk_g2s(sm.S + i * kTileRows * D, Sg + size_t(i) * kTileRows * D, kTileBytes, &sm.bar[i]);
@@ -145,10 +171,19 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
     }
   };
   // ---- 1. stage the (row, head) state, 32 rows per bulk copy ----------------
+  if (tid == 0) {
+#pragma unroll
+    for (int i = 0; i < NT; ++i) mbar_init(&sm.bar[i], 1);
+    mbar_init(&sm.cbar, 1);
+    fence_mbar_init();
+  }
   if (active) stage_state();
+  __syncthreads();  // initialised barriers are visible to every waiter
   if (p.overlap) pdl_wait();
 
-  // DEFERRED: is a commit of this (row, head) still to be applied?
+  // DEFERRED: is a commit of this (row, head) still to be applied?  If so its
+  // captures (written by this layer's previous verify, half (E-1) & 1) are
+  // fetched at once, and it is applied while the conv inputs are in flight.
   int E = 0, K = 0;
   bool pending = false, mark = false;
   if (MODE == GDN_COMMIT_DEFERRED) {
@@ -158,43 +193,143 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
     mark = E > A;
     pending = mark && K >= 1;
   }
+  const int old = (E - 1) & 1, cur = E & 1;
+  if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) {
+    constexpr uint32_t kRow = D * sizeof(float);
+    mbar_arrive_expect_tx(&sm.cbar, 2u * kRow * uint32_t(K));
+    for (int t = 0; t < K; ++t) {
+      bulk_g2s(sm.ce[t], p.dh_e[old] + ((size_t(b) * T + t) * H_v + h) * D, kRow, &sm.cbar);
+      bulk_g2s(sm.ck[t], p.dh_k[old] + ((size_t(b) * T + t) * H_k + hk) * D, kRow, &sm.cbar);
+    }
+  }
+  auto give_up = [&]() {
+    // A staged copy never arrived: flag it, give the copies one more bounded
+    // wait so they do not land in a retired CTA's shared memory, and write
+    // nothing more.
+    if (lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) mbar_wait_bounded(&sm.bar[i], 0);
+    if (MODE == GDN_COMMIT_DEFERRED && pending) mbar_wait_bounded(&sm.cbar, 0);
+  };
+  const int jw0 = warp * ROWS_W;
+  // DEFERRED: S <- gamma S + sum_{s<K} c_s e_s k_s^T on this warp's rows (the
+  // arithmetic of the eager RECOMPUTE commit), in shared memory and written
+  // back as the committed state.  Returns false if a staged copy timed out.
+  auto apply_pending = [&]() -> bool {
+    const float *Gp = p.dh_G[old] + size_t(b) * T * H_v + h;
+    const float GK = Gp[size_t(K - 1) * H_v];
+    const float pc_gam = expf(GK);
+    float pc_c[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) pc_c[t] = t < K ? expf(GK - Gp[size_t(t) * H_v]) : 0.f;
+    if (!mbar_wait_bounded(&sm.cbar, 0)) return false;
+#pragma unroll
+    for (int grp8 = 0; grp8 < NGRP; ++grp8) {
+      const int jw = jw0 + 8 * grp8;
+      if ((grp8 * 8) % kTileRows == 0 && !mbar_wait_bounded(&sm.bar[jw / kTileRows], 0)) return false;
+      float4 sv[RPL];
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) {
+        const float4 s0 = *reinterpret_cast<const float4 *>(&sm.S[(jw + grp + GPW * i) * D + 4 * sub]);
+        sv[i] = make_float4(pc_gam * s0.x, pc_gam * s0.y, pc_gam * s0.z, pc_gam * s0.w);
+      }
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        if (t < K) {
+          const float4 kv = *reinterpret_cast<const float4 *>(&sm.ck[t][4 * sub]);
+          const float *ert = &sm.ce[t][jw];
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) {
+            const float f = pc_c[t] * ert[grp + GPW * i];
+            sv[i].x = fmaf(f, kv.x, sv[i].x);
+            sv[i].y = fmaf(f, kv.y, sv[i].y);
+            sv[i].z = fmaf(f, kv.z, sv[i].z);
+            sv[i].w = fmaf(f, kv.w, sv[i].w);
+          }
+        }
+      }
+      float *Sw = p.state_w + ((size_t(b) * H_v + h) * D + jw) * D;
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) {
+        *reinterpret_cast<float4 *>(&sm.S[(jw + grp + GPW * i) * D + 4 * sub]) = sv[i];
+        st_f4(Sw + size_t(grp + GPW * i) * D + 4 * sub, sv[i]);
+      }
+    }
+    return true;
+  };
   if (!active) {
     // Inactive / padding / finished rows are inert: zero output, no ring
     // access.  A commit still pending from an earlier cycle is applied.
-    for (int i = tid; i < T * D; i += 2 * D) p.out[((size_t(b) * T + i / D) * H_v + h) * D + i % D] = 0;
-    if (!pending) {
-      if (mark && tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
-      return;
+    for (int i = tid; i < T * D; i += NTHR) p.out[((size_t(b) * T + i / D) * H_v + h) * D + i % D] = 0;
+    if (MODE == GDN_COMMIT_DEFERRED && mark) {  // (pending implies mark)
+      bool failed = false;
+      if (pending) {
+        stage_state();
+        failed = !apply_pending();
+      }
+      // every warp has applied (or given up) before the epoch is recorded;
+      // no thread leaves before this barrier
+      if (__syncthreads_or(failed)) {
+        give_up();
+        return;
+      }
+      if (tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
     }
-    stage_state();
-    __syncthreads();
+    return;
   }
 
   const bool qk_writer = (h % rep) == 0;  // one CTA per key head writes its q/k ring slots
-  constexpr int ROWS_W = 16;              // state rows per warp: two groups of 8
-  const int jw0 = warp * ROWS_W;
-  float q[T][4], k[T][4], vrow[ROWS_W / 8][T];
+  float q[T][4], k[T][4], vrow[NGRP][T];
   float gt[T], bt[T];
-  if (active) {
-    // ---- 2. conv + activation: one q or k channel of the key head per thread
-    {
-      const bool is_k = tid >= D;
-      const int ch = is_k ? tid - D : tid;
-      float y[T];
-      conv_channel<T>(p, b, (is_k ? H_k * D : 0) + hk * D + ch, qk_writer, y);
+  {
+    // ---- 2. conv + activation: the key head's q and k channels (spread over
+    // the CTA) and the v channels of the rows this lane will hold; every load
+    // is issued before the first use
+    constexpr int NQK = (2 * D + NTHR - 1) / NTHR;
+    ConvIn<T> inqk[NQK], inv[NGRP];
 #pragma unroll
-      for (int t = 0; t < T; ++t) (is_k ? sm.k : sm.q)[t][ch] = y[t];
+    for (int r = 0; r < NQK; ++r) {
+      const int c2 = tid + r * NTHR;
+      if (c2 < 2 * D) conv_load<T>(p, b, (c2 >= D ? H_k * D + c2 - D : c2) + hk * D, inqk[r]);
     }
+#pragma unroll
+    for (int grp8 = 0; grp8 < NGRP; ++grp8)
+      conv_load<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
       bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
     }
-    // the v channels of the rows this lane will hold, also before the barrier
+    const bool failed = MODE == GDN_COMMIT_DEFERRED && pending && !apply_pending();
 #pragma unroll
-    for (int grp8 = 0; grp8 < ROWS_W / 8; ++grp8)
-      conv_channel<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, leader, vrow[grp8]);
-    __syncthreads();  // conv outputs and the initialised barriers are visible
+    for (int r = 0; r < NQK; ++r) {
+      const int c2 = tid + r * NTHR;
+      if (c2 < 2 * D) {
+        float y[T];
+        conv_eval<T>(inqk[r], p.act, y);
+#pragma unroll
+        for (int t = 0; t < T; ++t) (c2 >= D ? sm.k : sm.q)[t][c2 >= D ? c2 - D : c2] = y[t];
+      }
+    }
+#pragma unroll
+    for (int grp8 = 0; grp8 < NGRP; ++grp8) conv_eval<T>(inv[grp8], p.act, vrow[grp8]);
+    // new raw inputs into the ring: q/k channels by one CTA of the key head,
+    // v channels by one lane of the four sharing a row
+#pragma unroll
+    for (int r = 0; r < NQK; ++r) {
+      const int c2 = tid + r * NTHR;
+      if (qk_writer && c2 < 2 * D) conv_store_ring<T>(p, b, (c2 >= D ? H_k * D + c2 - D : c2) + hk * D, inqk[r]);
+    }
+    if (leader)
+#pragma unroll
+      for (int grp8 = 0; grp8 < NGRP; ++grp8)
+        conv_store_ring<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
+    // conv outputs (and applied state rows) are visible; a timed-out staged
+    // copy stops the CTA here, where no thread has left yet
+    if (__syncthreads_or(failed)) {
+      give_up();
+      return;
+    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
@@ -208,7 +343,7 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
   float red_h[NV];
   float inv_q[T], inv_k[T], Gc[T], gam[T];
   float decay[T][T];  // exp(G_t - G_s), s < t
-  if (active) {
+  {
     int n = 0;
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -247,61 +382,21 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
       for (int s0 = 0; s0 < t; ++s0) decay[t][s0] = expf(Gc[t] - Gc[s0]);
   }
 
-  // DEFERRED: coefficients of the pending commit, S <- gamma S + sum_s c_s e_s k_s^T
-  // with the captures of the verify that preceded it
-  const int old = (E - 1) & 1, cur = E & 1;
-  float pc_gam = 0.f;
-  if (MODE == GDN_COMMIT_DEFERRED && pending) pc_gam = expf(p.dh_G[old][(size_t(b) * T + (K - 1)) * H_v + h]);
-
-  // ---- 5. this warp's 16 rows, in two groups of 8 ---------------------------
-  if (!mbar_wait_bounded(&sm.bar[jw0 / kTileRows], 0)) {
-    // The staged tile never arrived: flag it, give the copies one more bounded
-    // wait so they do not land in a retired CTA's shared memory, and write
-    // nothing for these rows.
-    if (lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
-#pragma unroll
-    for (int i = 0; i < NT; ++i) mbar_wait_bounded(&sm.bar[i], 0);
-    return;
-  }
+  // ---- 5. this warp's rows, in groups of 8 (the state is already staged,
+  // and in DEFERRED mode already brought up to date) -------------------------
   const size_t plane = size_t(p.B) * H_v * D * D;
 #pragma unroll
-  for (int grp8 = 0; grp8 < ROWS_W / 8; ++grp8) {
+  for (int grp8 = 0; grp8 < NGRP; ++grp8) {
     const int jw = jw0 + 8 * grp8;  // first state row of this group
     const int jrow = jw + grp + GPW * istar;
+    if ((grp8 * 8) % kTileRows == 0 && !mbar_wait_bounded(&sm.bar[jw / kTileRows], 0)) {
+      give_up();
+      return;
+    }
     float4 s[RPL];
 #pragma unroll
     for (int i = 0; i < RPL; ++i)
       s[i] = *reinterpret_cast<const float4 *>(&sm.S[(jw + grp + GPW * i) * D + 4 * sub]);
-    if (MODE == GDN_COMMIT_DEFERRED && pending) {
-      // apply the pending commit to these rows (same arithmetic as the eager
-      // RECOMPUTE commit) and write them back as the committed state
-      const float GK = p.dh_G[old][(size_t(b) * T + (K - 1)) * H_v + h];
-#pragma unroll
-      for (int i = 0; i < RPL; ++i)
-        s[i] = make_float4(pc_gam * s[i].x, pc_gam * s[i].y, pc_gam * s[i].z, pc_gam * s[i].w);
-#pragma unroll
-      for (int t = 0; t < kMaxT; ++t) {
-        if (t < K) {
-          const float c = expf(GK - p.dh_G[old][(size_t(b) * T + t) * H_v + h]);
-          const float4 kv =
-              *reinterpret_cast<const float4 *>(p.dh_k[old] + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub);
-          const float *ert = p.dh_e[old] + ((size_t(b) * T + t) * H_v + h) * D + jw;
-#pragma unroll
-          for (int i = 0; i < RPL; ++i) {
-            const float f = c * ert[grp + GPW * i];
-            s[i].x = fmaf(f, kv.x, s[i].x);
-            s[i].y = fmaf(f, kv.y, s[i].y);
-            s[i].z = fmaf(f, kv.z, s[i].z);
-            s[i].w = fmaf(f, kv.w, s[i].w);
-          }
-        }
-      }
-      float *Sw = p.state_w + ((size_t(b) * H_v + h) * D + jw) * D;
-#pragma unroll
-      for (int i = 0; i < RPL; ++i) st_f4(Sw + size_t(grp + GPW * i) * D + 4 * sub, s[i]);
-    }
-    if (!active) continue;
-
     float red[2 * T];
 #pragma unroll
     for (int mvec = 0; mvec < 2 * T; ++mvec) {
@@ -366,8 +461,8 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
       }
     }
   }
+  // every warp applied its rows before the conv barrier
   if (MODE == GDN_COMMIT_DEFERRED && mark && tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
-  if (!active) return;
 
   // ---- 6. captures of the key head and decay --------------------------------
   if (MODE == GDN_COMMIT_RECOMPUTE || MODE == GDN_COMMIT_DEFERRED) {
@@ -389,7 +484,8 @@ __global__ void __launch_bounds__(2 * D, T <= 4 ? 2 : 1) verify_kernel(const Ver
 // Launch one verify instantiation, raising its dynamic shared-memory limit on
 // the first launch of that instantiation on each device.
 template <int D, int T, int MODE>
-cudaError_t launch_verify_kernel(dim3 grid, dim3 block, cudaStream_t stream, const VerifyParams &p) {
+cudaError_t launch_verify_kernel(dim3 grid, cudaStream_t stream, const VerifyParams &p) {
+  const dim3 block(VerifyShape<D, T>::kThreads);
   static bool configured[64] = {false};  // one flag set per instantiation
   constexpr int smem = int(sizeof(VerifySmem<D, T>));
   int dev = 0;
@@ -405,14 +501,14 @@ cudaError_t launch_verify_kernel(dim3 grid, dim3 block, cudaStream_t stream, con
 
 template <int D>
 cudaError_t launch_verify_d(const VerifyParams &p, int T, int mode, cudaStream_t stream) {
-  const dim3 grid(p.H_v, p.B), block(2 * D);
+  const dim3 grid(p.H_v, p.B);
 #define GDN_VERIFY_CASE(TT)                                                                   \
   case TT:                                                                                    \
     return mode == GDN_COMMIT_RECOMPUTE                                                       \
-               ? launch_verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>(grid, block, stream, p)    \
+               ? launch_verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>(grid, stream, p)    \
                : mode == GDN_COMMIT_SNAPSHOT                                                  \
-                     ? launch_verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>(grid, block, stream, p) \
-                     : launch_verify_kernel<D, TT, GDN_COMMIT_DEFERRED>(grid, block, stream, p);
+                     ? launch_verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>(grid, stream, p) \
+                     : launch_verify_kernel<D, TT, GDN_COMMIT_DEFERRED>(grid, stream, p);
   switch (T) {
     GDN_VERIFY_CASE(1)
     GDN_VERIFY_CASE(2)
