@@ -173,16 +173,13 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
     p.ws_snap = reinterpret_cast<float *>(ws);
   } else {
     const DeferredWs w = deferred_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);
-    const RecomputeWs r = recompute_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);
+    const RecomputeWs r = recompute_ws(dims->B, dims->T, dims->H_v, dims->H_v, dims->d_k);
     p.ws_epoch = reinterpret_cast<const int *>(ws);
     p.ws_pend = reinterpret_cast<const int *>(ws + w.pend);
     p.ws_applied = reinterpret_cast<int *>(ws + w.applied);
-    for (int hf = 0; hf < 2; ++hf) {
-      char *half = ws + w.half0 + size_t(hf) * w.half_bytes;
-      p.dh_e[hf] = reinterpret_cast<float *>(half + r.e);
-      p.dh_k[hf] = reinterpret_cast<float *>(half + r.k);
-      p.dh_G[hf] = reinterpret_cast<float *>(half + r.G);
-    }
+    p.ws_e = reinterpret_cast<float *>(ws + w.cap + r.e);
+    p.ws_k = reinterpret_cast<float *>(ws + w.cap + r.k);
+    p.ws_G = reinterpret_cast<float *>(ws + w.cap + r.G);
     p.state_w = const_cast<float *>(state);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -41,29 +41,61 @@ __device__ __forceinline__ int effective_keep(const CommitParams &p, int b) {
 
 // S_keep of 8 state rows (this warp's), in place on the lane's float4
 // segments: S <- gamma_{K-1} S + sum_{t<K} exp(G_{K-1} - G_t) e_t k_t^T with the
-// captures e [B][T][H_v][D], k [B][T][H_k][D], G [B][T][H_v] of one verify.
+// captures e [B][H_v][T][D], k [B][KH][T][D], G [B][H_v][kMaxT] of one verify;
+// kh is the head's index among the KH copies of k.  Every capture load of the
+// first kPre positions is issued before any arithmetic, so they are in flight
+// together with the caller's state loads.
 template <int D>
 __device__ __forceinline__ void rebuild_rows(float4 (&s)[RowLanes<D>::RPL], const float *we, const float *wk,
-                                             const float *wG, int b, int h, int hk, int row0, int K, int T, int H_k,
+                                             const float *wG, int b, int h, int kh, int KH, int row0, int K, int T,
                                              int H_v, int sub, int grp) {
   using G = RowLanes<D>;
-  const float GK = wG[(size_t(b) * T + (K - 1)) * H_v + h];
+  constexpr int kPre = 4;
+  const size_t bh = size_t(b) * H_v + h, bk = size_t(b) * KH + kh;
+  const float4 g0 = *reinterpret_cast<const float4 *>(wG + bh * kMaxT);
+  const float4 g1 = *reinterpret_cast<const float4 *>(wG + bh * kMaxT + 4);
+  float4 kv[kPre];
+  float ev[kPre][G::RPL];
+#pragma unroll
+  for (int t = 0; t < kPre; ++t) {
+    if (t < K) {
+      kv[t] = *reinterpret_cast<const float4 *>(wk + (bk * T + t) * D + 4 * sub);
+      const float *ert = we + (bh * T + t) * D + row0;
+#pragma unroll
+      for (int i = 0; i < G::RPL; ++i) ev[t][i] = ert[grp + G::GPW * i];
+    }
+  }
+  const float gv[kMaxT] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  float GK = gv[0];
+#pragma unroll
+  for (int t = 1; t < kMaxT; ++t)
+    if (t == K - 1) GK = gv[t];
   const float gam = expf(GK);
 #pragma unroll
   for (int i = 0; i < G::RPL; ++i) s[i] = make_float4(gam * s[i].x, gam * s[i].y, gam * s[i].z, gam * s[i].w);
 #pragma unroll
   for (int t = 0; t < kMaxT; ++t) {
     if (t < K) {
-      const float c = expf(GK - wG[(size_t(b) * T + t) * H_v + h]);
-      const float4 kv = *reinterpret_cast<const float4 *>(wk + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub);
-      const float *ert = we + ((size_t(b) * T + t) * H_v + h) * D + row0;
+      const float c = expf(GK - gv[t]);
+      float4 k4;
+      float e8[G::RPL];
+      if (t < kPre) {
+        k4 = kv[t];
+#pragma unroll
+        for (int i = 0; i < G::RPL; ++i) e8[i] = ev[t][i];
+      } else {
+        k4 = *reinterpret_cast<const float4 *>(wk + (bk * T + t) * D + 4 * sub);
+        const float *ert = we + (bh * T + t) * D + row0;
+#pragma unroll
+        for (int i = 0; i < G::RPL; ++i) e8[i] = ert[grp + G::GPW * i];
+      }
 #pragma unroll
       for (int i = 0; i < G::RPL; ++i) {
-        const float f = c * ert[grp + G::GPW * i];
-        s[i].x = fmaf(f, kv.x, s[i].x);
-        s[i].y = fmaf(f, kv.y, s[i].y);
-        s[i].z = fmaf(f, kv.z, s[i].z);
-        s[i].w = fmaf(f, kv.w, s[i].w);
+        const float f = c * e8[i];
+        s[i].x = fmaf(f, k4.x, s[i].x);
+        s[i].y = fmaf(f, k4.y, s[i].y);
+        s[i].z = fmaf(f, k4.z, s[i].z);
+        s[i].w = fmaf(f, k4.w, s[i].w);
       }
     }
   }
@@ -124,7 +156,6 @@ __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
   }
 
   const int H_v = p.H_v, T = p.T;
-  const int rep = H_v / p.H_k;
   const long long per_layer = (long long)p.B * H_v * TILES;
   const long long total = MODE == GDN_COMMIT_DEFERRED ? 0 : per_layer * p.n_layers;
   for (long long u = blockIdx.x; u < total; u += gridDim.x) {
@@ -147,11 +178,12 @@ __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
       for (int i = 0; i < RPL; ++i) s[i] = ld_stream_f4(src + size_t(grp + GPW * i) * D + 4 * sub);
     } else {
       const RecomputeWs wl = recompute_ws(p.B, T, p.H_k, H_v, D);
+      const int rep = H_v / p.H_k;
       const char *base = reinterpret_cast<const char *>(p.ws[layer]);
 #pragma unroll
       for (int i = 0; i < RPL; ++i) s[i] = ld_stream_f4(S + size_t(grp + GPW * i) * D + 4 * sub);
       rebuild_rows<D>(s, reinterpret_cast<const float *>(base + wl.e), reinterpret_cast<const float *>(base + wl.k),
-                      reinterpret_cast<const float *>(base + wl.G), b, h, h / rep, row0, K, T, p.H_k, H_v, sub,
+                      reinterpret_cast<const float *>(base + wl.G), b, h, h / rep, p.H_k, row0, K, T, H_v, sub,
                       grp);
     }
 #pragma unroll
@@ -173,7 +205,7 @@ __global__ void __launch_bounds__(128) flush_kernel(const CommitParams p) {
   pdl_trigger();
   const int H_v = p.H_v, T = p.T;
   const DeferredWs dl = deferred_ws(p.B, T, p.H_k, H_v, D);
-  const RecomputeWs rl = recompute_ws(p.B, T, p.H_k, H_v, D);
+  const RecomputeWs rl = recompute_ws(p.B, T, H_v, H_v, D);
   const long long total = (long long)p.n_layers * p.B * H_v;
   for (long long u = blockIdx.x; u < total; u += gridDim.x) {
     const int layer = int(u / ((long long)p.B * H_v));
@@ -185,15 +217,14 @@ __global__ void __launch_bounds__(128) flush_kernel(const CommitParams p) {
     const int K = reinterpret_cast<const int *>(ws + dl.pend)[b];
     const int A = *applied;
     if (E > A && K >= 1) {
-      const char *half = ws + dl.half0 + size_t((E - 1) & 1) * dl.half_bytes;
+      const char *cap = ws + dl.cap;
       for (int row0 = warp * 8; row0 < D; row0 += 32) {
         float *S = p.state[layer] + ((size_t(b) * H_v + h) * D + row0) * D;
         float4 s[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) s[i] = ld_stream_f4(S + size_t(grp + GPW * i) * D + 4 * sub);
-        rebuild_rows<D>(s, reinterpret_cast<const float *>(half + rl.e), reinterpret_cast<const float *>(half + rl.k),
-                        reinterpret_cast<const float *>(half + rl.G), b, h, h / (H_v / p.H_k), row0, K, T, p.H_k,
-                        H_v, sub, grp);
+        rebuild_rows<D>(s, reinterpret_cast<const float *>(cap + rl.e), reinterpret_cast<const float *>(cap + rl.k),
+                        reinterpret_cast<const float *>(cap + rl.G), b, h, h, H_v, row0, K, T, H_v, sub, grp);
 #pragma unroll
         for (int i = 0; i < RPL; ++i) st_f4(S + size_t(grp + GPW * i) * D + 4 * sub, s[i]);
       }

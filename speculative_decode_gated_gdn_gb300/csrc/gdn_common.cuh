@@ -76,6 +76,26 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Contiguous shared -> global copy on the bulk-copy engine, tracked as a bulk
+// group of the issuing thread.  src, dst 16-byte aligned; bytes a multiple of
+// 16.  Writes of the generic proxy to `src` must be fenced with
+// fence_proxy_async_shared() and a barrier before the copy is issued.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk group of this thread has finished reading shared
+// memory (the global writes complete on their own; kernel completion makes
+// them visible).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -275,16 +295,16 @@ struct VerifyParams {
   uint16_t *ring;
   const uint8_t *active;
   uint16_t *out;
-  float *ws_e;    // RECOMPUTE: [B][T][H_v][D]
-  float *ws_k;    // RECOMPUTE: [B][T][H_k][D]
-  float *ws_G;    // RECOMPUTE: [B][T][H_v]
+  // captures of this verify for the commit (RECOMPUTE and DEFERRED)
+  float *ws_e;    // [B][H_v][T][D]   e_t of each state row
+  float *ws_k;    // [B][H_v][T][D]   normalised k_t of the head's key head
+  float *ws_G;    // [B][H_v][kMaxT]  cumulative log-decay G_t
   float *ws_snap; // SNAPSHOT:  [T][B][H_v][D][D]
-  // DEFERRED: header + two capture halves (e, k, G as in RECOMPUTE) used in
-  // turn by consecutive cycles; half[(epoch - 1) & 1] holds the pending commit
+  // DEFERRED: the captures above still hold the previous verify's until this
+  // verify has applied them
   const int *ws_epoch;  // commits recorded so far
   const int *ws_pend;   // [B] keep' of the last commit
   int *ws_applied;      // [B][H_v] epoch up to which the state is materialised
-  float *dh_e[2], *dh_k[2], *dh_G[2];
   float *state_w;       // DEFERRED: the state, written where a commit is applied
   uint32_t *status; // sticky device status word
   int B, T, H_k, H_v, C, R, act;
@@ -304,19 +324,24 @@ struct CommitParams {
   int n_layers, B, T, H_k, H_v, C, R;
 };
 
-// Byte offsets of the RECOMPUTE workspace regions (each 256-byte aligned).
+// Byte offsets of the capture regions of a verify (each 256-byte aligned):
+// e [B][H_v][T][D], normalised k [B][KH][T][D], G [B][H_v][kMaxT].  KH = H_k
+// (one copy per key head, written by one CTA of the key head) in RECOMPUTE
+// mode; KH = H_v in DEFERRED mode, where every (row, value head) owns its
+// copy so that it can fetch its captures before the PDL wait.  A (row, head)'s
+// captures are contiguous per region, one bulk copy each.
 struct RecomputeWs {
   size_t e, k, G, total;
 };
 
 __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-__host__ __device__ inline RecomputeWs recompute_ws(int B, int T, int H_k, int H_v, int D) {
+__host__ __device__ inline RecomputeWs recompute_ws(int B, int T, int KH, int H_v, int D) {
   RecomputeWs w;
   w.e = 0;
-  w.k = w.e + align256(sizeof(float) * size_t(B) * T * H_v * D);
-  w.G = w.k + align256(sizeof(float) * size_t(B) * T * H_k * D);
-  w.total = w.G + align256(sizeof(float) * size_t(B) * T * H_v);
+  w.k = w.e + align256(sizeof(float) * size_t(B) * H_v * T * D);
+  w.G = w.k + align256(sizeof(float) * size_t(B) * KH * T * D);
+  w.total = w.G + align256(sizeof(float) * size_t(B) * H_v * kMaxT);
   return w;
 }
 
@@ -325,18 +350,18 @@ __host__ __device__ inline size_t snapshot_ws(int B, int T, int H_v, int D) {
 }
 
 // DEFERRED workspace: epoch at byte 0, pending keep [B], applied epochs
-// [B][H_v], then two RECOMPUTE-layout capture halves.
+// [B][H_v], then the captures in the RECOMPUTE layout.
 struct DeferredWs {
-  size_t pend, applied, half0, half_bytes, total;
+  size_t pend, applied, cap, total;
 };
 
 __host__ __device__ inline DeferredWs deferred_ws(int B, int T, int H_k, int H_v, int D) {
   DeferredWs w;
   w.pend = 256;
   w.applied = w.pend + align256(sizeof(int) * size_t(B));
-  w.half0 = w.applied + align256(sizeof(int) * size_t(B) * H_v);
-  w.half_bytes = recompute_ws(B, T, H_k, H_v, D).total;
-  w.total = w.half0 + 2 * w.half_bytes;
+  w.cap = w.applied + align256(sizeof(int) * size_t(B) * H_v);
+  (void)H_k;
+  w.total = w.cap + recompute_ws(B, T, H_v, H_v, D).total;
   return w;
 }
 

@@ -98,8 +98,8 @@ __device__ __forceinline__ void conv_store_ring(const VerifyParams &p, int b, in
 }
 
 // Shared memory of one verify CTA: the (row, head) state tile, the conv
-// outputs of its key head and, in DEFERRED mode, the captures of the commit
-// still to be applied (e_t of the head, normalised k_t of the key head).
+// outputs of its key head and, in DEFERRED mode, the captures of the previous
+// verify (e_t, normalised k_t, G_t) for the commit that may still be pending.
 template <int D, int T>
 struct VerifySmem {
   float S[D * D];
@@ -107,6 +107,7 @@ struct VerifySmem {
   float k[T][D];
   float ce[T][D];
   float ck[T][D];
+  float cG[kMaxT];
   uint64_t bar[D / kTileRows];
   uint64_t cbar;
 };
@@ -161,12 +162,24 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   const bool active = p.active[b] != 0;
   constexpr uint32_t kTileBytes = kTileRows * D * sizeof(float);
   const float *Sg = p.state + (size_t(b) * H_v + h) * D * D;
+  const size_t bh = size_t(b) * H_v + h;
+  // DEFERRED: this (row, head)'s captures of the previous verify, one bulk
+  // copy per region.  Only this CTA writes them (at its end), and the
+  // previous verify of the layer finished before the last unflagged call, so
+  // they may be fetched before the PDL wait like the state.
   auto stage_state = [&]() {
     if (tid == 0) {
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
         mbar_arrive_expect_tx(&sm.bar[i], kTileBytes);
         bulk_g2s(sm.S + i * kTileRows * D, Sg + size_t(i) * kTileRows * D, kTileBytes, &sm.bar[i]);
+      }
+      if (MODE == GDN_COMMIT_DEFERRED) {
+        constexpr uint32_t kCap = T * D * sizeof(float);
+        mbar_arrive_expect_tx(&sm.cbar, 2 * kCap + kMaxT * sizeof(float));
+        bulk_g2s(&sm.ce[0][0], p.ws_e + bh * T * D, kCap, &sm.cbar);
+        bulk_g2s(&sm.ck[0][0], p.ws_k + bh * T * D, kCap, &sm.cbar);
+        bulk_g2s(sm.cG, p.ws_G + bh * kMaxT, kMaxT * sizeof(float), &sm.cbar);
       }
     }
   };
@@ -181,9 +194,8 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   __syncthreads();  // initialised barriers are visible to every waiter
   if (p.overlap) pdl_wait();
 
-  // DEFERRED: is a commit of this (row, head) still to be applied?  If so its
-  // captures (written by this layer's previous verify, half (E-1) & 1) are
-  // fetched at once, and it is applied while the conv inputs are in flight.
+  // DEFERRED: is a commit of this (row, head) still to be applied?  If so it
+  // is applied while the conv inputs are in flight.
   int E = 0, K = 0;
   bool pending = false, mark = false;
   if (MODE == GDN_COMMIT_DEFERRED) {
@@ -193,36 +205,27 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     mark = E > A;
     pending = mark && K >= 1;
   }
-  const int old = (E - 1) & 1, cur = E & 1;
-  if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) {
-    constexpr uint32_t kRow = D * sizeof(float);
-    mbar_arrive_expect_tx(&sm.cbar, 2u * kRow * uint32_t(K));
-    for (int t = 0; t < K; ++t) {
-      bulk_g2s(sm.ce[t], p.dh_e[old] + ((size_t(b) * T + t) * H_v + h) * D, kRow, &sm.cbar);
-      bulk_g2s(sm.ck[t], p.dh_k[old] + ((size_t(b) * T + t) * H_k + hk) * D, kRow, &sm.cbar);
-    }
-  }
   auto give_up = [&]() {
     // A staged copy never arrived: flag it, give the copies one more bounded
     // wait so they do not land in a retired CTA's shared memory, and write
-    // nothing more.
+    // nothing more.  (Called only before any write-back was issued.)
     if (lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
 #pragma unroll
     for (int i = 0; i < NT; ++i) mbar_wait_bounded(&sm.bar[i], 0);
-    if (MODE == GDN_COMMIT_DEFERRED && pending) mbar_wait_bounded(&sm.cbar, 0);
+    if (MODE == GDN_COMMIT_DEFERRED && (active || pending)) mbar_wait_bounded(&sm.cbar, 0);
   };
   const int jw0 = warp * ROWS_W;
   // DEFERRED: S <- gamma S + sum_{s<K} c_s e_s k_s^T on this warp's rows (the
-  // arithmetic of the eager RECOMPUTE commit), in shared memory and written
-  // back as the committed state.  Returns false if a staged copy timed out.
+  // arithmetic of the eager RECOMPUTE commit), in place in shared memory;
+  // write_back() then stores the tile as the committed state.  Returns false
+  // if a staged copy timed out.
   auto apply_pending = [&]() -> bool {
-    const float *Gp = p.dh_G[old] + size_t(b) * T * H_v + h;
-    const float GK = Gp[size_t(K - 1) * H_v];
+    if (!mbar_wait_bounded(&sm.cbar, 0)) return false;
+    const float GK = sm.cG[K - 1];
     const float pc_gam = expf(GK);
     float pc_c[T];
 #pragma unroll
-    for (int t = 0; t < T; ++t) pc_c[t] = t < K ? expf(GK - Gp[size_t(t) * H_v]) : 0.f;
-    if (!mbar_wait_bounded(&sm.cbar, 0)) return false;
+    for (int t = 0; t < T; ++t) pc_c[t] = t < K ? expf(GK - sm.cG[t]) : 0.f;
 #pragma unroll
     for (int grp8 = 0; grp8 < NGRP; ++grp8) {
       const int jw = jw0 + 8 * grp8;
@@ -248,14 +251,24 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
           }
         }
       }
-      float *Sw = p.state_w + ((size_t(b) * H_v + h) * D + jw) * D;
 #pragma unroll
-      for (int i = 0; i < RPL; ++i) {
-        *reinterpret_cast<float4 *>(&sm.S[(jw + grp + GPW * i) * D + 4 * sub]) = sv[i];
-        st_f4(Sw + size_t(grp + GPW * i) * D + 4 * sub, sv[i]);
-      }
+      for (int i = 0; i < RPL; ++i) *reinterpret_cast<float4 *>(&sm.S[(jw + grp + GPW * i) * D + 4 * sub]) = sv[i];
     }
+    fence_proxy_async_shared();  // the bulk copies of write_back read these rows
     return true;
+  };
+  // After a barrier that follows every warp's apply: the updated tile goes
+  // back to the state buffer on the bulk-copy engine while the warps carry
+  // on; the issuing thread waits for the reads of shared memory before it
+  // leaves.
+  auto write_back = [&]() {
+    if (tid == 0) {
+      float *Sw = p.state_w + bh * D * D;
+#pragma unroll
+      for (int i = 0; i < NT; ++i)
+        bulk_s2g(Sw + size_t(i) * kTileRows * D, sm.S + i * kTileRows * D, kTileBytes);
+      bulk_commit_group();
+    }
   };
   if (!active) {
     // Inactive / padding / finished rows are inert: zero output, no ring
@@ -273,7 +286,11 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
         give_up();
         return;
       }
-      if (tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
+      if (pending) write_back();
+      if (tid == 0) {
+        p.ws_applied[size_t(b) * H_v + h] = E;
+        bulk_wait_read_all();
+      }
     }
     return;
   }
@@ -300,7 +317,10 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
       gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
       bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
     }
-    const bool failed = MODE == GDN_COMMIT_DEFERRED && pending && !apply_pending();
+    // (DEFERRED: the staged captures are waited for even when nothing is
+    // pending, so no copy lands after the CTA has left)
+    const bool failed = MODE == GDN_COMMIT_DEFERRED &&
+                        (pending ? !apply_pending() : !mbar_wait_bounded(&sm.cbar, 0));
 #pragma unroll
     for (int r = 0; r < NQK; ++r) {
       const int c2 = tid + r * NTHR;
@@ -330,6 +350,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
       give_up();
       return;
     }
+    if (MODE == GDN_COMMIT_DEFERRED && pending) write_back();
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
@@ -391,6 +412,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     const int jrow = jw + grp + GPW * istar;
     if ((grp8 * 8) % kTileRows == 0 && !mbar_wait_bounded(&sm.bar[jw / kTileRows], 0)) {
       give_up();
+      if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) bulk_wait_read_all();
       return;
     }
     float4 s[RPL];
@@ -434,10 +456,8 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     if (leader) {
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        const size_t idx = ((size_t(b) * T + t) * H_v + h) * D + jrow;
-        p.out[idx] = f2bf(o[t]);
-        if (MODE == GDN_COMMIT_RECOMPUTE) p.ws_e[idx] = e[t];
-        if (MODE == GDN_COMMIT_DEFERRED) p.dh_e[cur][idx] = e[t];
+        p.out[((size_t(b) * T + t) * H_v + h) * D + jrow] = f2bf(o[t]);
+        if (MODE != GDN_COMMIT_SNAPSHOT) p.ws_e[(bh * T + t) * D + jrow] = e[t];
       }
     }
     if (MODE == GDN_COMMIT_SNAPSHOT) {
@@ -465,20 +485,22 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   if (MODE == GDN_COMMIT_DEFERRED && mark && tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
 
   // ---- 6. captures of the key head and decay --------------------------------
-  if (MODE == GDN_COMMIT_RECOMPUTE || MODE == GDN_COMMIT_DEFERRED) {
-    float *wk = MODE == GDN_COMMIT_RECOMPUTE ? p.ws_k : p.dh_k[cur];
-    float *wG = MODE == GDN_COMMIT_RECOMPUTE ? p.ws_G : p.dh_G[cur];
-    if (qk_writer && warp == 0 && grp == 0)
+  if (MODE != GDN_COMMIT_SNAPSHOT) {
+    // k: one copy per key head in RECOMPUTE mode, one per (row, value head)
+    // in DEFERRED mode
+    const size_t bk = MODE == GDN_COMMIT_DEFERRED ? bh : size_t(b) * H_k + hk;
+    if ((MODE == GDN_COMMIT_DEFERRED || qk_writer) && warp == 0 && grp == 0)
 #pragma unroll
       for (int t = 0; t < T; ++t)
-        st_f4(wk + ((size_t(b) * T + t) * H_k + hk) * D + 4 * sub,
+        st_f4(p.ws_k + (bk * T + t) * D + 4 * sub,
               make_float4(k[t][0] * inv_k[t], k[t][1] * inv_k[t], k[t][2] * inv_k[t], k[t][3] * inv_k[t]));
     if (warp == 0 && lane < T) {
 #pragma unroll
       for (int t = 0; t < T; ++t)
-        if (lane == t) wG[(size_t(b) * T + t) * H_v + h] = Gc[t];
+        if (lane == t) p.ws_G[bh * kMaxT + t] = Gc[t];
     }
   }
+  if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) bulk_wait_read_all();
 }
 
 // Launch one verify instantiation, raising its dynamic shared-memory limit on
