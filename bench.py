@@ -3,7 +3,10 @@
 One step = one MTP verify cycle of the whole stack: gdn_conv_verify for each of
 the 30 GDN layers, then one grouped gdn_commit for all layers with keep[]
 re-drawn every cycle (B=8 rows, T=2 positions, H_k=16, H_v=32, d=128, rows 6-7
-inactive).  The metric is row-tokens/s (B*T verified positions per cycle
+inactive).  The commit strategy defaults to DEFERRED: the commit records keep
+and shifts the conv windows, and each layer's next verify applies the state
+update while it holds the state anyway (--mode recompute|snapshot for the
+eager strategies).  The metric is row-tokens/s (B*T verified positions per cycle
 divided by the cycle time) together with the achieved HBM bandwidth against
 the measured GB300 copy peak.
 
@@ -57,7 +60,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1024)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="recompute", choices=list(MODES))
+    ap.add_argument("--mode", default="deferred", choices=list(MODES))
     ap.add_argument("--B", type=int, default=8)
     ap.add_argument("--T", type=int, default=2)
     ap.add_argument("--layers", type=int, default=30)
@@ -444,7 +447,8 @@ def run_gpu(args, rank, world, local):
     n_keep_all = (kp_all >= 1).sum(axis=1)
     n_keep = n_keep_all[W:W + K]
     # DEFERRED: the verify of cycle c applies the commit of cycle c - 1
-    n_apply = n_keep_all[W - 1:W + K - 1] if args.mode == "deferred" else np.zeros(K, np.int64)
+    prev_keep = np.concatenate([[0], n_keep_all])  # [c] = kept rows of cycle c - 1 (none before cycle 0)
+    n_apply = prev_keep[W:W + K] if args.mode == "deferred" else np.zeros(K, np.int64)
     commit_alg = np.array([commit_bytes(geom, int(nk), n_layers, args.mode) for nk in n_keep], dtype=np.float64)
     verify_alg = np.array([verify_bytes(geom, n_active, args.mode, int(na)) for na in n_apply], dtype=np.float64)
     step_bytes = commit_alg + n_layers * verify_alg

@@ -250,8 +250,12 @@ static int sm_count() {
 template <int D>
 static cudaError_t launch_commit_d(const CommitParams &p, int mode, cudaStream_t stream) {
   long long units = (long long)p.n_layers * p.B * p.H_v * (D / kTileRows);
-  if (mode == GDN_COMMIT_DEFERRED) units = (long long)p.n_layers * p.B * ((p.C / 8 + 127) / 128);
   long long grid = (long long)sm_count() * 8;
+  if (mode == GDN_COMMIT_DEFERRED) {
+    // only window shifts: small units, one wave of up to 16 CTAs per SM
+    units = (long long)p.n_layers * p.B * ((p.C / 8 + 127) / 128);
+    grid = (long long)sm_count() * 16;
+  }
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
   if (mode == GDN_COMMIT_RECOMPUTE)
