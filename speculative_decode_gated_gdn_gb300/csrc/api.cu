@@ -174,9 +174,7 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
   } else {
     const DeferredWs w = deferred_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);
     const RecomputeWs r = recompute_ws(dims->B, dims->T, dims->H_v, dims->H_v, dims->d_k);
-    p.ws_epoch = reinterpret_cast<const int *>(ws);
-    p.ws_pend = reinterpret_cast<const int *>(ws + w.pend);
-    p.ws_applied = reinterpret_cast<int *>(ws + w.applied);
+    p.ws_pend = reinterpret_cast<int *>(ws + w.pend);
     p.ws_e = reinterpret_cast<float *>(ws + w.cap + r.e);
     p.ws_k = reinterpret_cast<float *>(ws + w.cap + r.k);
     p.ws_G = reinterpret_cast<float *>(ws + w.cap + r.G);

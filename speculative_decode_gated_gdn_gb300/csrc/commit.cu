@@ -145,14 +145,18 @@ __global__ void __launch_bounds__(128) commit_kernel(const CommitParams p) {
         else atomicOr(p.status, GDN_STATUS_BAD_KEEP);
       }
       p.offsets[b] += kp;
-      if (MODE == GDN_COMMIT_DEFERRED) {
-        const DeferredWs dl = deferred_ws(p.B, p.T, p.H_k, p.H_v, D);
-        for (int l = 0; l < p.n_layers; ++l)
-          reinterpret_cast<int *>(reinterpret_cast<char *>(p.ws[l]) + dl.pend)[b] = kp;
-      }
     }
-    if (MODE == GDN_COMMIT_DEFERRED)
-      for (int l = tid; l < p.n_layers; l += blockDim.x) *reinterpret_cast<int *>(p.ws[l]) += 1;
+  }
+  if (MODE == GDN_COMMIT_DEFERRED) {
+    // record keep' for every (layer, row, head); the next verify of each
+    // (or a flush) applies it and resets it to 0
+    const DeferredWs dl = deferred_ws(p.B, p.T, p.H_k, p.H_v, D);
+    const long long n = (long long)p.n_layers * p.B * p.H_v;
+    for (long long i = (long long)blockIdx.x * blockDim.x + tid; i < n; i += (long long)gridDim.x * blockDim.x) {
+      const int l = int(i / ((long long)p.B * p.H_v));
+      const int bh = int(i % ((long long)p.B * p.H_v));
+      reinterpret_cast<int *>(reinterpret_cast<char *>(p.ws[l]) + dl.pend)[bh] = effective_keep(p, bh / p.H_v);
+    }
   }
 
   const int H_v = p.H_v, T = p.T;
@@ -212,11 +216,9 @@ __global__ void __launch_bounds__(128) flush_kernel(const CommitParams p) {
     const int r = int(u % ((long long)p.B * H_v));
     const int b = r / H_v, h = r % H_v;
     char *ws = reinterpret_cast<char *>(p.ws[layer]);
-    const int E = *reinterpret_cast<const int *>(ws);
-    int *applied = reinterpret_cast<int *>(ws + dl.applied) + size_t(b) * H_v + h;
-    const int K = reinterpret_cast<const int *>(ws + dl.pend)[b];
-    const int A = *applied;
-    if (E > A && K >= 1) {
+    int *pend = reinterpret_cast<int *>(ws + dl.pend) + size_t(b) * H_v + h;
+    const int K = min(*pend, T);
+    if (K >= 1) {
       const char *cap = ws + dl.cap;
       for (int row0 = warp * 8; row0 < D; row0 += 32) {
         float *S = p.state[layer] + ((size_t(b) * H_v + h) * D + row0) * D;
@@ -229,8 +231,8 @@ __global__ void __launch_bounds__(128) flush_kernel(const CommitParams p) {
         for (int i = 0; i < RPL; ++i) st_f4(S + size_t(grp + GPW * i) * D + 4 * sub, s[i]);
       }
     }
-    __syncthreads();  // every CTA thread has read A before it changes
-    if (E > A && tid == 0) *applied = E;
+    __syncthreads();  // every CTA thread has read the pending keep before it is reset
+    if (K >= 1 && tid == 0) *pend = 0;
   }
 }
 

@@ -302,9 +302,7 @@ struct VerifyParams {
   float *ws_snap; // SNAPSHOT:  [T][B][H_v][D][D]
   // DEFERRED: the captures above still hold the previous verify's until this
   // verify has applied them
-  const int *ws_epoch;  // commits recorded so far
-  const int *ws_pend;   // [B] keep' of the last commit
-  int *ws_applied;      // [B][H_v] epoch up to which the state is materialised
+  int *ws_pend;         // [B][H_v] keep' of a commit not yet applied (0: none)
   float *state_w;       // DEFERRED: the state, written where a commit is applied
   uint32_t *status; // sticky device status word
   int B, T, H_k, H_v, C, R, act;
@@ -349,17 +347,17 @@ __host__ __device__ inline size_t snapshot_ws(int B, int T, int H_v, int D) {
   return sizeof(float) * size_t(T) * B * H_v * D * D;
 }
 
-// DEFERRED workspace: epoch at byte 0, pending keep [B], applied epochs
-// [B][H_v], then the captures in the RECOMPUTE layout.
+// DEFERRED workspace: the pending keep' [B][H_v] of each (row, head) (set by
+// the commit, reset to 0 by whichever verify or flush applies it), then the
+// captures in the RECOMPUTE layout.
 struct DeferredWs {
-  size_t pend, applied, cap, total;
+  size_t pend, cap, total;
 };
 
 __host__ __device__ inline DeferredWs deferred_ws(int B, int T, int H_k, int H_v, int D) {
   DeferredWs w;
-  w.pend = 256;
-  w.applied = w.pend + align256(sizeof(int) * size_t(B));
-  w.cap = w.applied + align256(sizeof(int) * size_t(B) * H_v);
+  w.pend = 0;
+  w.cap = w.pend + align256(sizeof(int) * size_t(B) * H_v);
   (void)H_k;
   w.total = w.cap + recompute_ws(B, T, H_v, H_v, D).total;
   return w;

@@ -196,14 +196,11 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
 
   // DEFERRED: is a commit of this (row, head) still to be applied?  If so it
   // is applied while the conv inputs are in flight.
-  int E = 0, K = 0;
-  bool pending = false, mark = false;
+  int K = 0;
+  bool pending = false;
   if (MODE == GDN_COMMIT_DEFERRED) {
-    E = *p.ws_epoch;
-    const int A = p.ws_applied[size_t(b) * H_v + h];
-    K = p.ws_pend[b];
-    mark = E > A;
-    pending = mark && K >= 1;
+    K = min(p.ws_pend[bh], T);
+    pending = K >= 1;
   }
   auto give_up = [&]() {
     // A staged copy never arrived: flag it, give the copies one more bounded
@@ -274,21 +271,18 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     // Inactive / padding / finished rows are inert: zero output, no ring
     // access.  A commit still pending from an earlier cycle is applied.
     for (int i = tid; i < T * D; i += NTHR) p.out[((size_t(b) * T + i / D) * H_v + h) * D + i % D] = 0;
-    if (MODE == GDN_COMMIT_DEFERRED && mark) {  // (pending implies mark)
-      bool failed = false;
-      if (pending) {
-        stage_state();
-        failed = !apply_pending();
-      }
-      // every warp has applied (or given up) before the epoch is recorded;
-      // no thread leaves before this barrier
+    if (MODE == GDN_COMMIT_DEFERRED && pending) {
+      stage_state();
+      const bool failed = !apply_pending();
+      // every warp has applied (or given up) before the pending keep is
+      // reset; no thread leaves before this barrier
       if (__syncthreads_or(failed)) {
         give_up();
         return;
       }
-      if (pending) write_back();
+      write_back();
       if (tid == 0) {
-        p.ws_applied[size_t(b) * H_v + h] = E;
+        p.ws_pend[bh] = 0;
         bulk_wait_read_all();
       }
     }
@@ -482,7 +476,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     }
   }
   // every warp applied its rows before the conv barrier
-  if (MODE == GDN_COMMIT_DEFERRED && mark && tid == 0) p.ws_applied[size_t(b) * H_v + h] = E;
+  if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) p.ws_pend[bh] = 0;
 
   // ---- 6. captures of the key head and decay --------------------------------
   if (MODE != GDN_COMMIT_SNAPSHOT) {

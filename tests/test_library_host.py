@@ -127,8 +127,9 @@ def test_deferred_workspace_size(lib):
     d = L.dims(8, 2, 16, 32, 128)
     rec = lib.gdn_layer_workspace_bytes(ctypes.byref(d), L.GDN_COMMIT_RECOMPUTE)
     dfr = lib.gdn_layer_workspace_bytes(ctypes.byref(d), L.GDN_COMMIT_DEFERRED)
-    # the RECOMPUTE captures plus the epoch, keep and applied-epoch words
-    assert dfr >= rec + 4 + 8 * 4 + 8 * 32 * 4
+    # the pending keep of every (row, head), then the captures with k kept
+    # per value head
+    assert dfr == 8 * 32 * 4 + 2 * 8 * 32 * 2 * 128 * 4 + 8 * 32 * 8 * 4
     # captures: e per (row, value head, position), normalised k per (row, key
     # head, position), G padded to 8 positions per (row, value head)
     assert rec == 8 * 32 * 2 * 128 * 4 + 8 * 16 * 2 * 128 * 4 + 8 * 32 * 8 * 4
