@@ -54,35 +54,48 @@ struct PrefillParams {
   uint16_t *kn_hi, *kn_lo;  // [B][H_k][NCp] tiles of k  as [t][i]
   uint16_t *kt_hi, *kt_lo;  // [B][H_k][NCp] tiles of k^T as [i][t] (K dim = 64 tokens)
   uint16_t *vt_hi, *vt_lo;  // [B][H_v][NCp] tiles of v^T as [j][t]
+  // d = 128: the chunk kernel hands W and Pm to the tensor-core state pass
+  // as bf16 tiles instead of fp32 rows
+  uint16_t *w_hi, *w_lo;    // [B][H_v][NCp] tiles of W as [t][i] (K dim = d)
+  uint16_t *pm_hi;          // [B][H_v][NCp] tiles of Pm as [t][s] (K dim = 64)
   uint32_t *status;         // sticky device status word
   int B, L, NC, NCp, H_k, H_v, C, R, act;
 };
 
 struct PrefillWs {
-  size_t q, k, v, W, U, Gc, Pm, qn_hi, qn_lo, kn_hi, kn_lo, kt_hi, kt_lo, vt_hi, vt_lo, total;
+  size_t q, k, v, W, U, Gc, Pm, qn_hi, qn_lo, kn_hi, kn_lo, kt_hi, kt_lo, vt_hi, vt_lo, w_hi, w_lo, pm_hi, total;
 };
+
+// The sequential pass runs on the tensor cores at d = 128 (one TMEM lane per
+// state row) and on the CUDA cores at d = 32, 64.
+__host__ __device__ constexpr bool state_pass_tc(int D) { return D == 128; }
 
 inline PrefillWs prefill_ws(int B, int L, int H_k, int H_v, int D) {
   const int NC = (L + kChunk - 1) / kChunk;
   const size_t Lp = size_t(NC) * kChunk;  // padded so every chunk tile is whole
+  const bool tc = state_pass_tc(D);
+  const int NCp = (NC + 1) & ~1;  // the tensor-core kernels work on chunk pairs
   PrefillWs w;
   size_t o = 0;
   w.q = o, o += align256(sizeof(float) * size_t(B) * H_k * Lp * D);
   w.k = o, o += align256(sizeof(float) * size_t(B) * H_k * Lp * D);
   w.v = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp * D);
-  w.W = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp * D);
+  w.W = o, o += tc ? 0 : align256(sizeof(float) * size_t(B) * H_v * Lp * D);
   w.U = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp * D);
   w.Gc = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp);
-  w.Pm = o, o += align256(sizeof(float) * size_t(B) * H_v * NC * kChunk * kChunk);
-  const int NCp = (NC + 1) & ~1;  // the tensor-core kernel works on chunk pairs
+  w.Pm = o, o += tc ? 0 : align256(sizeof(float) * size_t(B) * H_v * NC * kChunk * kChunk);
   const size_t tile = size_t(kChunk) * D * sizeof(uint16_t);
   size_t *hk_tiles[6] = {&w.qn_hi, &w.qn_lo, &w.kn_hi, &w.kn_lo, &w.kt_hi, &w.kt_lo};
   for (size_t *f : hk_tiles) *f = o, o += align256(tile * B * H_k * NCp);
   w.vt_hi = o, o += align256(tile * B * H_v * NCp);
   w.vt_lo = o, o += align256(tile * B * H_v * NCp);
+  w.w_hi = o, o += tc ? align256(tile * B * H_v * NCp) : 0;
+  w.w_lo = o, o += tc ? align256(tile * B * H_v * NCp) : 0;
+  w.pm_hi = o, o += tc ? align256(size_t(kChunk) * kChunk * sizeof(uint16_t) * B * H_v * NCp) : 0;
   w.total = o;
   return w;
 }
+
 
 // Byte offset of element (row, k) in a K-major no-swizzle canonical tile whose
 // K extent is Kd bf16 elements: core matrix (row/8, k/8) at
@@ -95,6 +108,21 @@ __device__ __forceinline__ void split_bf16(float y, uint16_t &hi, uint16_t &lo) 
   const __nv_bfloat16 h = __float2bfloat16_rn(y);
   hi = __bfloat16_as_ushort(h);
   lo = __bfloat16_as_ushort(__float2bfloat16_rn(y - __bfloat162float(h)));
+}
+
+// Split 8 fp32 values into bf16 hi/lo and store them as two 16-byte runs.
+__device__ __forceinline__ void store8_split(const float *v, uint16_t *hi, uint16_t *lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint16_t h0, l0, h1, l1;
+    split_bf16(v[2 * q], h0, l0);
+    split_bf16(v[2 * q + 1], h1, l1);
+    h[q] = uint32_t(h0) | (uint32_t(h1) << 16);
+    l[q] = uint32_t(l0) | (uint32_t(l1) << 16);
+  }
+  *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  if (lo) *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // Write one channel's 64 values into a natural tile ([t][i], K dim D) and,
@@ -355,9 +383,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
     const float Gt = sG[tid], bq = sBeta[tid];
     const int cb = q * kChunk;
     float *Pg = p.Pm + (((size_t(b) * H_v + h) * p.NC + chunk) * kChunk + tl) * kChunk;
+    uint16_t *Pt = p.pm_hi + ((size_t(b) * H_v + h) * p.NCp + chunk) * kChunk * kChunk;
 #pragma unroll
     for (int cc = 0; cc < kChunk; cc += 32) {
-      float kk[32], qk[32];
+      float kk[32], qk[32], pm[32];
       tmem_ld32(tmem + lane_base + cb + cc, kk);
       tmem_ld32(tmem + lane_base + 128 + cb + cc, qk);
 #pragma unroll
@@ -365,7 +394,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
         const int sl = cc + j;
         const float decay = sl <= tl ? expf(Gt - sG[cb + sl]) : 0.f;
         As[q][tl][sl] = sl < tl ? bq * decay * kk[j] : 0.f;
-        if (chunk < p.NC) Pg[sl] = decay * qk[j];
+        pm[j] = decay * qk[j];
+      }
+      if (chunk < p.NC) {
+        if constexpr (state_pass_tc(D)) {
+#pragma unroll
+          for (int s8 = 0; s8 < 32; s8 += 8)
+            store8_split(pm + s8, Pt + canon_off(tl, cc + s8, kChunk) / 2, nullptr);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) Pg[cc + j] = pm[j];
+        }
       }
     }
   }
@@ -462,12 +501,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   tc_fence_after();
   if (okw && chunk < p.NC) {
     float *Wg = p.W + ((size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl) * D;
+    const size_t wt = ((size_t(b) * H_v + h) * p.NCp + chunk) * tile_el;
 #pragma unroll
     for (int cc = 0; cc < D; cc += 32) {
       float v[32];
       tmem_ld32(tmem + lane_base + cc, v);
+      if constexpr (state_pass_tc(D)) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) st_f4(Wg + cc + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+        for (int i8 = 0; i8 < 32; i8 += 8) {
+          const uint32_t o = canon_off(tl, cc + i8, D) / 2;
+          store8_split(v + i8, p.w_hi + wt + o, p.w_lo + wt + o);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) st_f4(Wg + cc + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+      }
     }
     p.Gc[(size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl] = sG[tid];
   }
@@ -607,6 +655,286 @@ __global__ void __launch_bounds__(kStateThreads) prefill_state_kernel(const Pref
 }
 
 // ---------------------------------------------------------------------------
+// 3b. the sequential pass over chunks on the tensor cores (d = 128).  One CTA
+//     per (row, value head); state row j <-> TMEM lane j.  The fp32 state
+//     stays in TMEM for the whole prompt; per chunk of n tokens (t, s index
+//     tokens, i, j state columns and rows):
+//       E'^T = S W^T,   QS^T = S Q^T       M = 128 rows j, N = 64 tokens, K = d
+//       E = U - E',  E~_t = exp(G_n - G_t) E_t,  S <- gamma_n S   (epilogue)
+//       O^T = E^T Pm^T                     N = 64 tokens, K = 64 tokens
+//       S += E~^T K                        N = d columns, K = 64 tokens
+//       o_t = gamma_t QS^T + O^T,  then the bf16 hi/lo tiles of the new S
+//     The products that feed the state (E', S += ...) take three bf16 passes
+//     (hi hi, hi lo, lo hi); those that only feed the bf16 output take two
+//     (A split, B rounded once).  Operand tiles of the next chunk are fetched
+//     as soon as the products of this chunk that read them are done.  The
+//     epilogues are spread over 16 warps: warp w reads TMEM lane quarter
+//     w % 4 and takes column group w / 4 (16 tokens or 32 state columns);
+//     the per-token decay factors are computed once per chunk.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kStCols = 512;
+constexpr uint32_t kColE = 0, kColQS = 64, kColEP = 128, kColS = 256;
+constexpr int kStThreads = 512;
+
+struct StLayout {  // d = 128, byte offsets in dynamic shared memory
+  static constexpr uint32_t S_hi = 0, S_lo = 32768;          // S [j][i], K = 128: A operand
+  static constexpr uint32_t W_hi = 65536, W_lo = 81920;      // W [t][i], K = 128: B operand
+  static constexpr uint32_t Q_hi = 98304;                    // Q [t][i], K = 128: B operand
+  static constexpr uint32_t Kt_hi = 114688, Kt_lo = 131072;  // K^T [i][t], K = 64: B operand
+  static constexpr uint32_t Pm_hi = 147456;                  // Pm [t][s], K = 64: B operand
+  static constexpr uint32_t E_hi = 155648, E_lo = 172032;    // E^T [j][s], K = 64: A operand
+  static constexpr uint32_t Et_hi = 188416, Et_lo = 204800;  // decayed E^T [j][t], K = 64: A operand
+  static constexpr uint32_t G = 221184;                      // [2][64] within-chunk G, by chunk parity
+  static constexpr uint32_t Dec = G + 2 * kChunk * 4;        // [64] exp(G_n - G_t), 0 past n
+  static constexpr uint32_t Gam = Dec + kChunk * 4;          // [64] exp(G_t)
+  static constexpr uint32_t total = Gam + kChunk * 4;
+};
+
+__global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const PrefillParams p) {
+  constexpr int D = 128;
+  using Lay = StLayout;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bars[4];  // W+Q tiles, K^T+Pm tiles, products 1, products 2
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  float *sG = reinterpret_cast<float *>(smem + Lay::G);
+  float *sDec = reinterpret_cast<float *>(smem + Lay::Dec);
+  float *sGam = reinterpret_cast<float *>(smem + Lay::Gam);
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group
+  const int j = 32 * quarter + lane;             // this thread's state row
+  const int H_v = p.H_v, H_k = p.H_k, L = p.L, NC = p.NC;
+  const int hk = h / (H_v / H_k);
+  const size_t Lp = size_t(NC) * kChunk;
+  const size_t bh = size_t(b) * H_v + h;
+  const uint32_t sbase = smem_u32(smem);
+  constexpr uint32_t kT128 = kChunk * D * sizeof(uint16_t);     // a 64 x 128 bf16 tile
+  constexpr uint32_t kT64 = kChunk * kChunk * sizeof(uint16_t);  // a 64 x 64 bf16 tile
+  const int tc0 = 16 * cg;  // this thread's 16 tokens of a chunk
+  const int ic0 = 32 * cg;  // this thread's 32 state columns
+
+  if (tid == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    s_fail = 0;
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, kStCols);
+  pdl_wait();
+  pdl_trigger();
+
+  auto load_wq = [&](int c) {
+    const size_t wq = (bh * p.NCp + c) * (kChunk * D);
+    const size_t qq = ((size_t(b) * H_k + hk) * p.NCp + c) * (kChunk * D);
+    mbar_arrive_expect_tx(&bars[0], 3 * kT128);
+    bulk_g2s(smem + Lay::W_hi, p.w_hi + wq, kT128, &bars[0]);
+    bulk_g2s(smem + Lay::W_lo, p.w_lo + wq, kT128, &bars[0]);
+    bulk_g2s(smem + Lay::Q_hi, p.qn_hi + qq, kT128, &bars[0]);
+  };
+  auto load_kp = [&](int c) {
+    const size_t kq = ((size_t(b) * H_k + hk) * p.NCp + c) * (kChunk * D);
+    const size_t pq = (bh * p.NCp + c) * (kChunk * kChunk);
+    mbar_arrive_expect_tx(&bars[1], 2 * kT128 + kT64);
+    bulk_g2s(smem + Lay::Kt_hi, p.kt_hi + kq, kT128, &bars[1]);
+    bulk_g2s(smem + Lay::Kt_lo, p.kt_lo + kq, kT128, &bars[1]);
+    bulk_g2s(smem + Lay::Pm_hi, p.pm_hi + pq, kT64, &bars[1]);
+  };
+  // bf16 hi/lo of this thread's 32 state columns of row j into the A tiles of S
+  auto put_row = [&](const float (&v)[32]) {
+#pragma unroll
+    for (int i8 = 0; i8 < 32; i8 += 8) {
+      const uint32_t o = canon_off(j, ic0 + i8, D);
+      store8_split(v + i8, reinterpret_cast<uint16_t *>(smem + Lay::S_hi + o),
+                   reinterpret_cast<uint16_t *>(smem + Lay::S_lo + o));
+    }
+  };
+  int pend_wq = -1, pend_kp = -1;  // (thread 0) chunk whose operand copies are in flight
+  if (tid == 0 && NC > 0) {
+    load_wq(0);
+    load_kp(0);
+    pend_wq = pend_kp = 0;
+  }
+  if (tid < kChunk) sG[tid] = tid < L ? p.Gc[bh * Lp + tid] : 0.f;
+  tc_fence_before();
+  __syncthreads();  // barriers, TMEM address, first gates
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t trow = tm + (uint32_t(32 * quarter) << 16);
+
+  // the initial state: this thread's columns of row j into TMEM and the A tiles
+  float *Sg = p.state + (bh * D + j) * D + ic0;
+  {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float4 f = *reinterpret_cast<const float4 *>(Sg + i);
+      v[i] = f.x, v[i + 1] = f.y, v[i + 2] = f.z, v[i + 3] = f.w;
+    }
+    tmem_st32(trow + kColS + ic0, v);
+    put_row(v);
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  constexpr int pa[3] = {0, 0, 1}, pb[3] = {0, 1, 0};  // (hi,hi), (hi,lo), (lo,hi)
+  constexpr uint32_t sbo128 = (D / 8) * 128, sbo64 = (kChunk / 8) * 128;
+  constexpr uint32_t idesc64 = umma_idesc_bf16(128, kChunk), idesc128 = umma_idesc_bf16(128, D);
+  for (int c = 0; c < NC; ++c) {
+    const int t0 = c * kChunk, n = min(kChunk, L - t0);
+    const uint32_t ph = uint32_t(c) & 1u;
+    const float *Gs = sG + (c & 1) * kChunk;
+    // this thread's U of the chunk, issued before the products
+    float u[16];
+    {
+      const float *Ug = p.U + (bh * Lp + t0 + tc0) * D + j;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) u[t] = Ug[size_t(t) * D];
+    }
+    // ---- products 1: E'^T = S W^T, QS^T = S Q^T ----
+    bool ok1 = true;
+    if (tid == 0) {
+      ok1 = mbar_wait_bounded(&bars[0], ph);
+      if (ok1) {
+        pend_wq = -1;
+        tc_fence_after();
+        const uint32_t aS[2] = {sbase + Lay::S_hi, sbase + Lay::S_lo};
+        const uint32_t bW[2] = {sbase + Lay::W_hi, sbase + Lay::W_lo};
+#pragma unroll
+        for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            umma_bf16(tm + kColE, umma_desc(aS[pa[ps]] + k * 256, 128, sbo128),
+                      umma_desc(bW[pb[ps]] + k * 256, 128, sbo128), idesc64, ps | k);
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            umma_bf16(tm + kColQS, umma_desc(aS[ps] + k * 256, 128, sbo128),
+                      umma_desc(sbase + Lay::Q_hi + k * 256, 128, sbo128), idesc64, ps | k);
+      }
+      umma_commit(&bars[2]);  // also arrives when nothing was issued
+    }
+    // per-token factors of this chunk, once
+    if (tid < kChunk) {
+      const float Gn = Gs[n - 1];
+      sDec[tid] = tid < n ? expf(Gn - Gs[tid]) : 0.f;
+      sGam[tid] = expf(Gs[tid]);
+    }
+    __syncthreads();
+    ok1 = mbar_wait_bounded(&bars[2], ph) && ok1;
+    tc_fence_after();
+    if (!ok1) s_fail = 1;
+    if (tid == 0 && ok1 && c + 1 < NC) {  // W and Q tiles are free
+      load_wq(c + 1);
+      pend_wq = c + 1;
+    }
+    // ---- epilogue 1: E^T and decayed E^T tiles; S <- gamma_n S ----
+    {
+      float ep[16], ev[16], et[16];
+      tmem_ld16(trow + kColE + tc0, ep);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int t = tc0 + k;
+        ev[k] = t < n ? u[k] - ep[k] : 0.f;
+        et[k] = ev[k] * sDec[t];
+      }
+#pragma unroll
+      for (int t8 = 0; t8 < 16; t8 += 8) {
+        const uint32_t o = canon_off(j, tc0 + t8, kChunk);
+        store8_split(ev + t8, reinterpret_cast<uint16_t *>(smem + Lay::E_hi + o),
+                     reinterpret_cast<uint16_t *>(smem + Lay::E_lo + o));
+        store8_split(et + t8, reinterpret_cast<uint16_t *>(smem + Lay::Et_hi + o),
+                     reinterpret_cast<uint16_t *>(smem + Lay::Et_lo + o));
+      }
+      const float gn = sGam[n - 1];
+      float v[32];
+      tmem_ld32(trow + kColS + ic0, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= gn;
+      tmem_st32(trow + kColS + ic0, v);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (s_fail) break;
+    // ---- products 2: O^T = E^T Pm^T, S += E~^T K ----
+    bool ok2 = true;
+    if (tid == 0) {
+      ok2 = mbar_wait_bounded(&bars[1], ph);
+      if (ok2) {
+        pend_kp = -1;
+        tc_fence_after();
+        const uint32_t aE[2] = {sbase + Lay::E_hi, sbase + Lay::E_lo};
+        const uint32_t aEt[2] = {sbase + Lay::Et_hi, sbase + Lay::Et_lo};
+        const uint32_t bK[2] = {sbase + Lay::Kt_hi, sbase + Lay::Kt_lo};
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+          for (int k = 0; k < kChunk / 16; ++k)
+            umma_bf16(tm + kColEP, umma_desc(aE[ps] + k * 256, 128, sbo64),
+                      umma_desc(sbase + Lay::Pm_hi + k * 256, 128, sbo64), idesc64, ps | k);
+#pragma unroll
+        for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+          for (int k = 0; k < kChunk / 16; ++k)
+            umma_bf16(tm + kColS, umma_desc(aEt[pa[ps]] + k * 256, 128, sbo64),
+                      umma_desc(bK[pb[ps]] + k * 256, 128, sbo64), idesc128, true);
+      }
+      umma_commit(&bars[3]);
+    }
+    ok2 = mbar_wait_bounded(&bars[3], ph) && ok2;
+    tc_fence_after();
+    if (!ok2) s_fail = 1;
+    if (tid == 0 && ok2 && c + 1 < NC) {  // K^T and Pm tiles are free
+      load_kp(c + 1);
+      pend_kp = c + 1;
+    }
+    // ---- epilogue 2: outputs, then the A tiles of the updated state ----
+    {
+      float qs[16], ep[16];
+      tmem_ld16(trow + kColQS + tc0, qs);
+      tmem_ld16(trow + kColEP + tc0, ep);
+      uint16_t *o = p.out + ((size_t(b) * L + t0 + tc0) * H_v + h) * D + j;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (tc0 + k < n) o[size_t(k) * H_v * D] = f2bf(fmaf(sGam[tc0 + k], qs[k], ep[k]));
+      float v[32];
+      tmem_ld32(trow + kColS + ic0, v);
+      put_row(v);
+    }
+    if (tid < kChunk && c + 1 < NC) {
+      const int t = (c + 1) * kChunk + tid;
+      sG[((c + 1) & 1) * kChunk + tid] = t < L ? p.Gc[bh * Lp + t] : 0.f;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (s_fail) break;
+  }
+  if (!s_fail) {
+    float v[32];
+    tmem_ld32(trow + kColS + ic0, v);
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) st_f4(Sg + i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+  } else if (tid == 0) {
+    atomicOr(p.status, GDN_STATUS_TIMEOUT);
+    // copies still in flight must land before the CTA leaves
+    if (pend_wq >= 0) mbar_wait_bounded(&bars[0], uint32_t(pend_wq) & 1u);
+    if (pend_kp >= 0) mbar_wait_bounded(&bars[1], uint32_t(pend_kp) & 1u);
+  }
+  if (h == 0 && tid == 0) p.offsets[b] += L;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, kStCols);
+}
+
+// ---------------------------------------------------------------------------
 // 4. ring: slots 0..2 become the raw inputs of the last three positions of
 //    window ++ prompt (for L < 3 partly the old window, read before any
 //    write by the same thread).  Runs after the conv kernel has read the old
@@ -655,6 +983,22 @@ static cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
     e = cudaLaunchKernelEx(&cfg, prefill_chunk_tc_kernel<D>, p);
     if (e != cudaSuccess) return e;
   }
+  if constexpr (state_pass_tc(D)) {
+    e = cudaFuncSetAttribute(prefill_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(StLayout::total));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.H_v, p.B);
+    cfg.blockDim = dim3(kStThreads);
+    cfg.dynamicSmemBytes = StLayout::total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_state_tc_kernel, p);
+  }
   const size_t state_smem = sizeof(StateSmem<D>);
   e = cudaFuncSetAttribute(prefill_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(state_smem));
   if (e != cudaSuccess) return e;
@@ -700,6 +1044,9 @@ cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g,
   p.kt_lo = reinterpret_cast<uint16_t *>(base + l.kt_lo);
   p.vt_hi = reinterpret_cast<uint16_t *>(base + l.vt_hi);
   p.vt_lo = reinterpret_cast<uint16_t *>(base + l.vt_lo);
+  p.w_hi = reinterpret_cast<uint16_t *>(base + l.w_hi);
+  p.w_lo = reinterpret_cast<uint16_t *>(base + l.w_lo);
+  p.pm_hi = reinterpret_cast<uint16_t *>(base + l.pm_hi);
   p.B = B, p.L = L, p.NC = (L + kChunk - 1) / kChunk, p.H_k = H_k, p.H_v = H_v;
   p.NCp = (p.NC + 1) & ~1;
   p.status = status_word_address();
