@@ -40,9 +40,8 @@ struct PrefillParams {
   int32_t *offsets;   // [B]
   uint16_t *out;      // [B][L][H_v][D]
   // workspace
-  float *q;   // [B][H_k][L][D]  normalised q / sqrt(D)
-  float *k;   // [B][H_k][L][D]  normalised k
-  float *v;   // [B][H_v][L][D]
+  float *q;   // [B][H_k][L][D]  normalised q / sqrt(D)   (CUDA-core state pass only)
+  float *k;   // [B][H_k][L][D]  normalised k             (CUDA-core state pass only)
   float *W;   // [B][H_v][L][D]
   float *U;   // [B][H_v][L][D]
   float *Gc;  // [B][H_v][L]     within-chunk cumulative log-decay
@@ -63,7 +62,7 @@ struct PrefillParams {
 };
 
 struct PrefillWs {
-  size_t q, k, v, W, U, Gc, Pm, qn_hi, qn_lo, kn_hi, kn_lo, kt_hi, kt_lo, vt_hi, vt_lo, w_hi, w_lo, pm_hi, total;
+  size_t q, k, W, U, Gc, Pm, qn_hi, qn_lo, kn_hi, kn_lo, kt_hi, kt_lo, vt_hi, vt_lo, w_hi, w_lo, pm_hi, total;
 };
 
 // The sequential pass runs on the tensor cores at d = 128 (one TMEM lane per
@@ -77,9 +76,8 @@ inline PrefillWs prefill_ws(int B, int L, int H_k, int H_v, int D) {
   const int NCp = (NC + 1) & ~1;  // the tensor-core kernels work on chunk pairs
   PrefillWs w;
   size_t o = 0;
-  w.q = o, o += align256(sizeof(float) * size_t(B) * H_k * Lp * D);
-  w.k = o, o += align256(sizeof(float) * size_t(B) * H_k * Lp * D);
-  w.v = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp * D);
+  w.q = o, o += tc ? 0 : align256(sizeof(float) * size_t(B) * H_k * Lp * D);
+  w.k = o, o += tc ? 0 : align256(sizeof(float) * size_t(B) * H_k * Lp * D);
   w.W = o, o += tc ? 0 : align256(sizeof(float) * size_t(B) * H_v * Lp * D);
   w.U = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp * D);
   w.Gc = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp);
@@ -212,10 +210,6 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
     const int hv = head - 2 * H_k;
     const size_t tbase = ((size_t(b) * p.H_v + hv) * p.NCp + chunk) * tile;
     store_tiles<D>(y, tid, nullptr, nullptr, p.vt_hi + tbase, p.vt_lo + tbase);
-    if (chunk >= p.NC) return;
-    float *dst = p.v + ((size_t(b) * p.H_v + hv) * Lp + t0) * D + tid;
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) dst[size_t(i) * D] = y[i];
     return;
   }
 #pragma unroll
@@ -243,7 +237,7 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
     store_tiles<D>(y, tid, p.qn_hi + tbase, p.qn_lo + tbase, nullptr, nullptr);
   else
     store_tiles<D>(y, tid, p.kn_hi + tbase, p.kn_lo + tbase, p.kt_hi + tbase, p.kt_lo + tbase);
-  if (chunk >= p.NC) return;
+  if (state_pass_tc(D) || chunk >= p.NC) return;
   float *dst = (kind == 0 ? p.q : p.k) + ((size_t(b) * H_k + hk) * Lp + t0) * D + tid;
 #pragma unroll
   for (int i = 0; i < kChunk; ++i) dst[size_t(i) * D] = y[i];
@@ -275,7 +269,8 @@ struct TcLayout {
   static constexpr uint32_t tr_tile = uint32_t(D) * kChunk * 2;    // one [i][t] tile
   static constexpr uint32_t sq_op = kPairRows * kPairRows * 2;     // a 128 x 128 bf16 operand
   static constexpr uint32_t R0 = 0, R1 = 65536, R2 = 131072, R3 = 196608;
-  static constexpr uint32_t solve_bytes = 2 * kChunk * (kChunk + 1) * 4;
+  static constexpr int kAStride = kChunk + 1;  // odd stride: the epilogue's row writes hit distinct banks
+  static constexpr uint32_t solve_bytes = 2 * kChunk * kAStride * 4;
   static constexpr uint32_t misc = R3 + solve_bytes;              // G[128], beta[128]
   static constexpr uint32_t total = misc + 2 * kPairRows * 4;
   static_assert(2 * nat_pair <= 65536 && 4 * tr_tile <= 65536 && 2 * sq_op <= 65536, "regions");
@@ -288,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   __shared__ __align__(8) uint64_t bars[6];
   __shared__ uint32_t s_tmem;
   __shared__ float s_wsum[4];
-  float(*As)[kChunk][kChunk + 1] = reinterpret_cast<float(*)[kChunk][kChunk + 1]>(smem + Lay::R3);
+  float(*As)[kChunk][Lay::kAStride] = reinterpret_cast<float(*)[kChunk][Lay::kAStride]>(smem + Lay::R3);
   float *sG = reinterpret_cast<float *>(smem + Lay::misc);
   float *sBeta = sG + kPairRows;
 
@@ -440,12 +435,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
     for (int r = 0; r < kChunk; ++r) {
       const int tr = q * kChunk + r;
       uint16_t hi, lo;
-      const uint32_t o = canon_off(tr, ks, kPairRows) / 2, oz = canon_off(tr, kz, kPairRows) / 2;
+      const uint32_t o = canon_off(tr, ks, kPairRows) / 2;
       split_bf16(x[r] * bgs, hi, lo);
       awh[o] = hi, awl[o] = lo;
       split_bf16(x[r] * bs, hi, lo);
       auh[o] = hi, aul[o] = lo;
-      awh[oz] = 0, awl[oz] = 0, auh[oz] = 0, aul[oz] = 0;
+    }
+    // the off-diagonal 64 x 64 quadrants are zero: in the canonical layout
+    // each 8-row group of a quadrant is one contiguous kilobyte
+    (void)kz;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    constexpr int kQuadU4 = kChunk / 8 * 1024 / 16;  // uint4 per quadrant
+#pragma unroll
+    for (int i = tid; i < 2 * kQuadU4; i += kTcThreads) {
+      const int quad = i / kQuadU4, w = i % kQuadU4;  // quad 0: rows 0..63 x cols 64..127; 1: the mirror
+      const int g = w / 64, c16 = w % 64;             // 8-row group, 16-byte unit within its kilobyte
+      const uint32_t byte = uint32_t((quad * 8 + g) * (kPairRows / 8) * 128 + (1 - quad) * 1024 + c16 * 16);
+      *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(awh) + byte) = z;
+      *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(awl) + byte) = z;
+      *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(auh) + byte) = z;
+      *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(aul) + byte) = z;
     }
   }
   fence_async_smem();  // generic-proxy writes above -> tensor-core reads below
@@ -1031,7 +1040,6 @@ cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g,
   char *base = static_cast<char *>(ws);
   p.q = reinterpret_cast<float *>(base + l.q);
   p.k = reinterpret_cast<float *>(base + l.k);
-  p.v = reinterpret_cast<float *>(base + l.v);
   p.W = reinterpret_cast<float *>(base + l.W);
   p.U = reinterpret_cast<float *>(base + l.U);
   p.Gc = reinterpret_cast<float *>(base + l.Gc);
