@@ -108,16 +108,19 @@ __device__ __forceinline__ void split_bf16(float y, uint16_t &hi, uint16_t &lo) 
   lo = __bfloat16_as_ushort(__float2bfloat16_rn(y - __bfloat162float(h)));
 }
 
-// Split 8 fp32 values into bf16 hi/lo and store them as two 16-byte runs.
+// Split 8 fp32 values into bf16 hi/lo (x_hi = bf16(x), x_lo = bf16(x - x_hi),
+// the same rounding as split_bf16, two values per conversion) and store them
+// as two 16-byte runs.
 __device__ __forceinline__ void store8_split(const float *v, uint16_t *hi, uint16_t *lo) {
   uint32_t h[4], l[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint16_t h0, l0, h1, l1;
-    split_bf16(v[2 * q], h0, l0);
-    split_bf16(v[2 * q + 1], h1, l1);
-    h[q] = uint32_t(h0) | (uint32_t(h1) << 16);
-    l[q] = uint32_t(l0) | (uint32_t(l1) << 16);
+    const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+    h[q] = *reinterpret_cast<const uint32_t *>(&hv);
+    if (lo) {
+      const __nv_bfloat162 lv = __floats2bfloat162_rn(v[2 * q] - __low2float(hv), v[2 * q + 1] - __high2float(hv));
+      l[q] = *reinterpret_cast<const uint32_t *>(&lv);
+    }
   }
   *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
   if (lo) *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
@@ -687,8 +690,9 @@ constexpr int kStThreads = 512;
 
 struct StLayout {  // d = 128, byte offsets in dynamic shared memory
   static constexpr uint32_t S_hi = 0, S_lo = 32768;          // S [j][i], K = 128: A operand
-  static constexpr uint32_t W_hi = 65536, W_lo = 81920;      // W [t][i], K = 128: B operand
-  static constexpr uint32_t Q_hi = 98304;                    // Q [t][i], K = 128: B operand
+  static constexpr uint32_t W_lo = 65536, W_hi = 81920;      // W [t][i], K = 128: B operand
+  static constexpr uint32_t Q_hi = 98304;                    // Q [t][i] right after W_hi: [W; Q] is
+                                                             // one 128-row B operand
   static constexpr uint32_t Kt_hi = 114688, Kt_lo = 131072;  // K^T [i][t], K = 64: B operand
   static constexpr uint32_t Pm_hi = 147456;                  // Pm [t][s], K = 64: B operand
   static constexpr uint32_t E_hi = 155648, E_lo = 172032;    // E^T [j][s], K = 64: A operand
@@ -795,7 +799,13 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     const int t0 = c * kChunk, n = min(kChunk, L - t0);
     const uint32_t ph = uint32_t(c) & 1u;
     const float *Gs = sG + (c & 1) * kChunk;
-    // this thread's U of the chunk, issued before the products
+    // the next chunk's gate (threads < 64) and this thread's U of the chunk,
+    // issued before the products
+    float g_next = 0.f;
+    if (tid < kChunk && c + 1 < NC) {
+      const int t = (c + 1) * kChunk + tid;
+      g_next = t < L ? p.Gc[bh * Lp + t] : 0.f;
+    }
     float u[16];
     {
       const float *Ug = p.U + (bh * Lp + t0 + tc0) * D + j;
@@ -809,20 +819,20 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       if (ok1) {
         pend_wq = -1;
         tc_fence_after();
+        // [E'^T | QS^T] = S [W; Q]^T over the hi parts (N = 128, columns
+        // kColE..kColE+127 = E' then QS), then E'^T += S_hi W_lo^T
+        static_assert(Lay::Q_hi == Lay::W_hi + kT128 && kColQS == kColE + kChunk, "[W; Q] operand");
         const uint32_t aS[2] = {sbase + Lay::S_hi, sbase + Lay::S_lo};
-        const uint32_t bW[2] = {sbase + Lay::W_hi, sbase + Lay::W_lo};
-#pragma unroll
-        for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            umma_bf16(tm + kColE, umma_desc(aS[pa[ps]] + k * 256, 128, sbo128),
-                      umma_desc(bW[pb[ps]] + k * 256, 128, sbo128), idesc64, ps | k);
 #pragma unroll
         for (int ps = 0; ps < 2; ++ps)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            umma_bf16(tm + kColQS, umma_desc(aS[ps] + k * 256, 128, sbo128),
-                      umma_desc(sbase + Lay::Q_hi + k * 256, 128, sbo128), idesc64, ps | k);
+            umma_bf16(tm + kColE, umma_desc(aS[ps] + k * 256, 128, sbo128),
+                      umma_desc(sbase + Lay::W_hi + k * 256, 128, sbo128), idesc128, ps | k);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_bf16(tm + kColE, umma_desc(aS[0] + k * 256, 128, sbo128),
+                    umma_desc(sbase + Lay::W_lo + k * 256, 128, sbo128), idesc64, true);
       }
       umma_commit(&bars[2]);  // also arrives when nothing was issued
     }
@@ -915,10 +925,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       tmem_ld32(trow + kColS + ic0, v);
       put_row(v);
     }
-    if (tid < kChunk && c + 1 < NC) {
-      const int t = (c + 1) * kChunk + tid;
-      sG[((c + 1) & 1) * kChunk + tid] = t < L ? p.Gc[bh * Lp + t] : 0.f;
-    }
+    if (tid < kChunk && c + 1 < NC) sG[((c + 1) & 1) * kChunk + tid] = g_next;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
