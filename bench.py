@@ -338,11 +338,11 @@ def timing_event():
 
 def verify_mode(mode, layer):
     """Layers after the first follow another layer's verify, which writes none of
-    their buffers, so they may stage state before that verify finishes.  In
-    DEFERRED mode the commit before layer 0 writes no state either."""
+    their buffers, so they may stage state (and in DEFERRED mode apply their
+    pending commit) before that verify finishes.  Layer 0 follows the commit,
+    which writes every layer's state or workspace."""
     from speculative_decode_gated_gdn_gb300 import lib as L
-    flag = layer > 0 or mode == L.GDN_COMMIT_DEFERRED
-    return mode | (L.GDN_VERIFY_OVERLAP if flag else 0)
+    return mode | (L.GDN_VERIFY_OVERLAP if layer > 0 else 0)
 
 
 def run_gpu(args, rank, world, local):

@@ -122,16 +122,16 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
  * With GDN_VERIFY_OVERLAP the call's kernel also lets the next kernel on the
  * stream start as soon as it has started, and stages its own state tiles
  * before waiting for its predecessor, so consecutive flagged verifies stream
- * their state ahead of one another (in DEFERRED mode also the captures of
- * the layer's previous verify).  The caller guarantees that no work issued
- * since the last library call made WITHOUT the flag writes this call's
- * `state` or `active`, and that the previous verify of this layer was issued
- * before that call.  In a verify cycle over a layer stack that
- * means: flag every layer but the first one after an eager gdn_commit
- * (RECOMPUTE or SNAPSHOT), gdn_prefill_chunked, gdn_flush or any other write
- * of these buffers; a DEFERRED gdn_commit writes no state, so every layer of
- * a DEFERRED cycle may be flagged.  Never flag a repeated verify of the same
- * layer.  It is always safe to omit. */
+ * their state ahead of one another; in DEFERRED mode it also fetches the
+ * captures of the layer's previous verify and applies a pending commit (and
+ * writes it back) before that wait.  The caller guarantees that no work
+ * issued since the last library call made WITHOUT the flag writes this
+ * call's `state`, `active` or `layer_ws`, and that the previous verify of
+ * this layer was issued before that call.  In a verify cycle over a layer
+ * stack that means: flag every layer but the first one after a gdn_commit
+ * (any mode), gdn_prefill_chunked, gdn_flush or any other write of these
+ * buffers.  Never flag a repeated verify of the same layer.  It is always
+ * safe to omit. */
 #define GDN_VERIFY_OVERLAP 0x100
 
 /* sticky device status bits (gdn_get_status) */

@@ -192,24 +192,19 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   }
   if (active) stage_state();
   __syncthreads();  // initialised barriers are visible to every waiter
-  if (p.overlap) pdl_wait();
 
-  // DEFERRED: is a commit of this (row, head) still to be applied?  If so it
-  // is applied while the conv inputs are in flight.
+  // DEFERRED: K = keep' of a commit of this (row, head) not yet applied.
   int K = 0;
-  bool pending = false;
-  if (MODE == GDN_COMMIT_DEFERRED) {
-    K = min(p.ws_pend[bh], T);
-    pending = K >= 1;
-  }
+  bool pending = false, applied = false;
   auto give_up = [&]() {
     // A staged copy never arrived: flag it, give the copies one more bounded
     // wait so they do not land in a retired CTA's shared memory, and write
-    // nothing more.  (Called only before any write-back was issued.)
+    // nothing more.
     if (lane == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
 #pragma unroll
     for (int i = 0; i < NT; ++i) mbar_wait_bounded(&sm.bar[i], 0);
     if (MODE == GDN_COMMIT_DEFERRED && (active || pending)) mbar_wait_bounded(&sm.cbar, 0);
+    if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
   };
   const int jw0 = warp * ROWS_W;
   // DEFERRED: S <- gamma S + sum_{s<K} c_s e_s k_s^T on this warp's rows (the
@@ -267,25 +262,47 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
       bulk_commit_group();
     }
   };
+  // Stage (if the row is inactive), apply, write back and retire a pending
+  // commit; CTA-uniform, so its barrier is safe.  False if a copy timed out.
+  auto apply_and_write = [&]() -> bool {
+    if (!active) stage_state();
+    const bool failed = !apply_pending();
+    // every warp has applied (or given up) before the write-back and the
+    // reset; no thread leaves before this barrier
+    if (__syncthreads_or(failed)) return false;
+    write_back();
+    if (tid == 0) p.ws_pend[bh] = 0;
+    applied = true;
+    return true;
+  };
+  // DEFERRED with GDN_VERIFY_OVERLAP: nothing issued since the last call
+  // without the flag wrote this layer's workspace (a commit is followed by an
+  // unflagged call), so the pending keep is final before the PDL wait and the
+  // commit is applied and written back while the preceding kernel still runs.
+  // Without the flag it is read after the wait and applied while the conv
+  // inputs are in flight.
+  if (MODE == GDN_COMMIT_DEFERRED && p.overlap) {
+    K = min(p.ws_pend[bh], T);
+    pending = K >= 1;
+    if (pending && !apply_and_write()) {
+      give_up();
+      return;
+    }
+  }
+  if (p.overlap) pdl_wait();
+  if (MODE == GDN_COMMIT_DEFERRED && !p.overlap) {
+    K = min(p.ws_pend[bh], T);
+    pending = K >= 1;
+  }
   if (!active) {
     // Inactive / padding / finished rows are inert: zero output, no ring
     // access.  A commit still pending from an earlier cycle is applied.
     for (int i = tid; i < T * D; i += NTHR) p.out[((size_t(b) * T + i / D) * H_v + h) * D + i % D] = 0;
-    if (MODE == GDN_COMMIT_DEFERRED && pending) {
-      stage_state();
-      const bool failed = !apply_pending();
-      // every warp has applied (or given up) before the pending keep is
-      // reset; no thread leaves before this barrier
-      if (__syncthreads_or(failed)) {
-        give_up();
-        return;
-      }
-      write_back();
-      if (tid == 0) {
-        p.ws_pend[bh] = 0;
-        bulk_wait_read_all();
-      }
+    if (MODE == GDN_COMMIT_DEFERRED && pending && !applied && !apply_and_write()) {
+      give_up();
+      return;
     }
+    if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
     return;
   }
 
@@ -314,7 +331,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     // (DEFERRED: the staged captures are waited for even when nothing is
     // pending, so no copy lands after the CTA has left)
     const bool failed = MODE == GDN_COMMIT_DEFERRED &&
-                        (pending ? !apply_pending() : !mbar_wait_bounded(&sm.cbar, 0));
+                        (pending && !applied ? !apply_pending() : !mbar_wait_bounded(&sm.cbar, 0));
 #pragma unroll
     for (int r = 0; r < NQK; ++r) {
       const int c2 = tid + r * NTHR;
@@ -344,7 +361,10 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
       give_up();
       return;
     }
-    if (MODE == GDN_COMMIT_DEFERRED && pending) write_back();
+    if (MODE == GDN_COMMIT_DEFERRED && pending && !applied) {
+      write_back();
+      applied = true;
+    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
@@ -406,7 +426,6 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     const int jrow = jw + grp + GPW * istar;
     if ((grp8 * 8) % kTileRows == 0 && !mbar_wait_bounded(&sm.bar[jw / kTileRows], 0)) {
       give_up();
-      if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) bulk_wait_read_all();
       return;
     }
     float4 s[RPL];
@@ -476,7 +495,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     }
   }
   // every warp applied its rows before the conv barrier
-  if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) p.ws_pend[bh] = 0;
+  if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) p.ws_pend[bh] = 0;  // (a repeat if applied before the wait)
 
   // ---- 6. captures of the key head and decay --------------------------------
   if (MODE != GDN_COMMIT_SNAPSHOT) {
@@ -494,7 +513,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
         if (lane == t) p.ws_G[bh * kMaxT + t] = Gc[t];
     }
   }
-  if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) bulk_wait_read_all();
+  if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
 }
 
 // Launch one verify instantiation, raising its dynamic shared-memory limit on

@@ -217,17 +217,19 @@ def test_guard_regions_untouched(gdn):
         assert torch.all(big[:pad] == 0xA5) and torch.all(big[-pad:] == 0xA5)
 
 
-def test_stack_30_layers_256_cycles_sampled(gdn):
+@pytest.mark.parametrize("mode", [L.GDN_COMMIT_RECOMPUTE, L.GDN_COMMIT_DEFERRED], ids=["recompute", "deferred"])
+def test_stack_30_layers_256_cycles_sampled(gdn, mode):
     """The B8/T2 cohort over a 30-layer stack for 256 consecutive cycles, keep
     re-drawn every cycle and offsets tracked, checked on sampled (layer, row,
-    head) units every cycle (the oracle recomputes each unit on its own)."""
+    head) units every cycle (the oracle recomputes each unit on its own), in
+    the launch configuration the benchmark times."""
     geom = synth.COHORT
     n_layers, n_cycles, pool = 30, 256, 16
     seed = 2
     active = synth.active_mask(8, (6, 7))
     st = synth.layer_state(geom, seed, n_layers)
     keeps = synth.keep_draws(geom, seed, n_cycles)
-    gpu = GpuStack(geom, st, active, L.GDN_COMMIT_RECOMPUTE, n_layers)
+    gpu = GpuStack(geom, st, active, mode, n_layers)
     units = [OracleUnit(geom, st, l, b, h) for (l, b, h) in
              [(0, 0, 0), (7, 1, 31), (13, 2, 5), (29, 5, 17), (21, 3, 10), (4, 6, 3), (29, 4, 30), (16, 5, 1)]]
     pool_in = [synth.cycle_inputs(geom, seed, p, n_layers) for p in range(pool)]
@@ -240,8 +242,8 @@ def test_stack_30_layers_256_cycles_sampled(gdn):
         for l in range(n_layers):
             # the launch configuration the benchmark times: layers after the
             # first stage their state while the previous layer's verify ends
-            mode = gpu.mode | (L.GDN_VERIFY_OVERLAP if l > 0 else 0)
-            L.gdn_conv_verify(gpu.dims, mode, xd[l], gpu.w[l], gd[l], bd[l], gpu.state[l], gpu.ring[l],
+            vmode = gpu.mode | (L.GDN_VERIFY_OVERLAP if l > 0 else 0)
+            L.gdn_conv_verify(gpu.dims, vmode, xd[l], gpu.w[l], gd[l], bd[l], gpu.state[l], gpu.ring[l],
                               gpu.offsets, gpu.active, gpu.out[l], gpu.ws[l])
         o_units = [u.verify(cy["x"][u.layer], cy["g"][u.layer], cy["beta"][u.layer], active[u.b]) for u in units]
         out = gpu.out
@@ -253,6 +255,8 @@ def test_stack_30_layers_256_cycles_sampled(gdn):
         offsets += np.where(active == 1, keeps[c], 0).astype(np.int32)
         assert np.array_equal(gpu.offsets.cpu().numpy(), offsets), f"cycle {c} offsets"
         if c % 32 == 31 or c == n_cycles - 1:
+            if mode == L.GDN_COMMIT_DEFERRED:
+                gpu.flush()
             for u in units:
                 check_state(gpu.state[u.layer, u.b, u.h].cpu().numpy()[None], u.S[0], f"cycle {c} unit state")
                 ring = host_bits(gpu.ring[u.layer, u.b:u.b + 1])
@@ -300,11 +304,10 @@ def _cycle_runs(geom, st, masks, keeps, n_layers, mode, overlap_all=False, repea
         gpu.active.copy_(torch.from_numpy(masks[c]))
         cy = synth.cycle_inputs(geom, 30, c, n_layers)
         for l in range(n_layers):
-            # flagged unless this layer's verify repeats (its first pass may
-            # have written the state) or the active mask was just rewritten
-            same_mask = c > 0 and np.array_equal(masks[c], masks[c - 1])
+            # flagged except after the commit (layer 0) and on a repeated
+            # verify of a layer (its first pass may have written the state)
             for rep in range(2 if repeat_verify else 1):
-                flag = overlap_all and rep == 0 and (l > 0 or same_mask)
+                flag = overlap_all and rep == 0 and l > 0
                 gpu.verify(l, cy["x"][l], cy["g"][l], cy["beta"][l], overlap=flag)
         outs.append(gpu.out.clone())
         gpu.commit(np.asarray(keep, np.int32))
@@ -319,7 +322,8 @@ def test_deferred_bit_identical_to_recompute(gdn, repeat_verify):
     """DEFERRED applies a commit inside the next verify with the arithmetic of
     the eager commit: every output, and the flushed state, equals RECOMPUTE bit
     for bit.  Rows switch between active and inactive with commits pending, and
-    every layer's verify is flagged GDN_VERIFY_OVERLAP in DEFERRED mode."""
+    every layer's verify after the first is flagged GDN_VERIFY_OVERLAP in
+    DEFERRED mode, so those apply their pending commit before the PDL wait."""
     geom = synth.Geometry(B=4, T=3, H_k=2, H_v=4, d=128, T_max=4)
     st = synth.layer_state(geom, 30, 3)
     masks = [synth.active_mask(4), synth.active_mask(4, (1,)), synth.active_mask(4, (1,)),
