@@ -61,7 +61,7 @@ def _f64(a):
 
 
 class Oracle:
-    """The oracle's four entry points bound to one compiled library."""
+    """The oracle's entry points bound to one compiled library."""
 
     def __init__(self, lib_path: str):
         lib = ctypes.CDLL(lib_path)
@@ -73,6 +73,8 @@ class Oracle:
         lib.oracle_commit.restype = None
         lib.oracle_prefill.argtypes = [_int] * 7 + [_D, _D, _D, _D, _D, _F, _D, _I]
         lib.oracle_prefill.restype = _int
+        lib.oracle_accept.argtypes = [_int] * 3 + [_D, _I, _U8, _I, _I]
+        lib.oracle_accept.restype = _int
         self.lib = lib
         self.path = lib_path
 
@@ -142,6 +144,21 @@ class Oracle:
         return o
 
 
+    def accept(self, logits, draft, active):
+        """Greedy acceptance: logits [B][T][V] (values as given), draft [B][T]
+        int32, active [B] -> (keep [B], next [B]) int32."""
+        logits = _f64(logits)
+        B, T, V = logits.shape
+        draft = np.ascontiguousarray(draft, dtype=np.int32)
+        active = np.ascontiguousarray(active, dtype=np.uint8)
+        keep = np.empty(B, dtype=np.int32)
+        nxt = np.empty(B, dtype=np.int32)
+        if self.lib.oracle_accept(B, T, V, _p(logits, _D), _p(draft, _I), _p(active, _U8), _p(keep, _I),
+                                  _p(nxt, _I)):
+            raise MemoryError("oracle_accept allocation failed")
+        return keep, nxt
+
+
 _default = None
 
 
@@ -170,3 +187,7 @@ def commit(*a, **k):
 
 def prefill(*a, **k):
     return default().prefill(*a, **k)
+
+
+def accept(*a, **k):
+    return default().accept(*a, **k)

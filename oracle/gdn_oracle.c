@@ -246,3 +246,49 @@ OR_EXPORT int oracle_prefill(int B, int L, int Hk, int Hv, int dk, int dv, int a
   free(Sd);
   return 0;
 }
+
+/*
+ * Greedy acceptance of one verify cycle, the decision that "Add request-owned
+ * eight-way MTP serving for Qwen 35B" takes off the host so that a decode
+ * cycle needs no host synchronisation.  Position 0 of a row's verify holds the
+ * last accepted token; positions 1..T-1 hold the draft tokens.  For an active
+ * row b:
+ *   target_t = argmax_v logits[b][t][v]   (the first index of the maximum;
+ *                                          NaN never wins; an all-NaN row gives 0)
+ *   keep[b]  = 1 + the number of leading t in 1..T-1 with draft[b][t] == target_{t-1}
+ *   next[b]  = target_{keep[b] - 1}       (the token the next cycle feeds)
+ * Inactive rows: keep 0, next -1.  logits [B][T][V] as fp64 (the bf16 values,
+ * exactly); draft [B][T] (draft[b][0] is not read).
+ */
+OR_EXPORT int oracle_accept(int B, int T, int V, const double *logits, const int32_t *draft,
+                            const uint8_t *active, int32_t *keep, int32_t *next) {
+  int32_t *target = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  if (!target) return -1;
+  for (int b = 0; b < B; ++b) {
+    if (!active[b]) {
+      keep[b] = 0;
+      next[b] = -1;
+      continue;
+    }
+    for (int t = 0; t < T; ++t) {
+      const double *row = logits + ((size_t)b * T + t) * V;
+      int best = -1;
+      double best_v = 0.0;
+      for (int v = 0; v < V; ++v) {
+        const double x = row[v];
+        if (x != x) continue; /* NaN */
+        if (best < 0 || x > best_v) {
+          best = v;
+          best_v = x;
+        }
+      }
+      target[t] = best < 0 ? 0 : best;
+    }
+    int k = 1;
+    while (k < T && draft[(size_t)b * T + k] == target[k - 1]) ++k;
+    keep[b] = k;
+    next[b] = target[k - 1];
+  }
+  free(target);
+  return 0;
+}

@@ -18,7 +18,10 @@ when the oracle disagrees with:
   recurrence (the chunked form that "MTP inference: review and commit
   structure", Verification and limits, says differs from the sequential one
   only in rounding),
-* a hand-worked example stored under tests/golden/.
+* a hand-worked example stored under tests/golden/,
+* for greedy acceptance: numpy's argmax (the first index of the maximum),
+  hand-built drafts whose accepted prefix is known by construction, and the
+  defining properties of the accepted prefix.
 
 They are plain functions (not tests) so that ``test_oracle_pins.py`` can also
 run them against builds of the oracle with planted mistakes and show that each
@@ -353,6 +356,63 @@ def pin_row_separable(orc):
         assert np.array_equal(o[b], ob[0]) and np.array_equal(Sall[b], Sb[0]), f"row {b} separable"
 
 
+def pin_accept_hand(orc):
+    """Greedy acceptance on a hand-built case: targets are planted maxima, so
+    the accepted prefix is known without running any argmax."""
+    B, T, V = 4, 4, 7
+    logits = np.zeros((B, T, V))
+    targets = np.array([[3, 1, 6, 0], [2, 2, 5, 4], [0, 6, 1, 3], [5, 5, 5, 5]])
+    for b in range(B):
+        for t in range(T):
+            logits[b, t, targets[b, t]] = 2.0 + t
+    draft = np.full((B, T), -7, np.int32)
+    draft[0, 1:] = [3, 1, 6]      # every draft accepted: keep = T
+    draft[1, 1:] = [2, 9, 5]      # second draft rejected: keep = 2
+    draft[2, 1:] = [4, 6, 1]      # first draft rejected: keep = 1
+    draft[3, 1:] = [5, 5, 5]      # all accepted, but the row is inactive
+    active = np.array([1, 1, 1, 0], np.uint8)
+    keep, nxt = orc.accept(logits, draft, active)
+    assert list(keep) == [4, 2, 1, 0], keep
+    assert list(nxt) == [0, 2, 0, -1], nxt
+
+
+def pin_accept_ties_and_nan(orc):
+    """Ties go to the first index; NaN never wins; an all-NaN row gives 0."""
+    logits = np.array([[[1.0, 5.0, 5.0, -2.0], [np.nan, 0.5, np.nan, 0.5]],
+                       [[np.nan] * 4, [3.0, 3.0, 3.0, 3.0]]])
+    draft = np.array([[0, 1], [0, 0]], np.int32)
+    keep, nxt = orc.accept(logits, draft, np.ones(2, np.uint8))
+    # row 0: target_0 = 1 (first of the tied 5.0s) == draft[0][1] -> keep 2, next = target_1 = 1
+    # row 1: target_0 = 0 (all NaN) == draft[1][1] -> keep 2, next = target_1 = 0 (first of ties)
+    assert list(keep) == [2, 2] and list(nxt) == [1, 0], (keep, nxt)
+
+
+def pin_accept_random(orc):
+    """Random logits against numpy's argmax and the defining properties of the
+    accepted prefix (every accepted draft equals the previous target; the
+    first rejected one does not)."""
+    rng = np.random.default_rng(7)
+    B, T, V = 24, 6, 97
+    logits = rng.integers(-20, 20, size=(B, T, V)).astype(np.float64)  # many ties
+    tgt = np.argmax(logits, axis=2)
+    draft = rng.integers(0, V, size=(B, T)).astype(np.int32)
+    for b in range(B):  # plant an accepted prefix of random length
+        n = int(rng.integers(0, T))
+        draft[b, 1:1 + n] = tgt[b, :n]
+    active = (rng.random(B) < 0.8).astype(np.uint8)
+    keep, nxt = orc.accept(logits, draft, active)
+    for b in range(B):
+        if not active[b]:
+            assert keep[b] == 0 and nxt[b] == -1
+            continue
+        k = int(keep[b])
+        assert 1 <= k <= T
+        assert all(draft[b, t] == tgt[b, t - 1] for t in range(1, k))
+        assert k == T or draft[b, k] != tgt[b, k - 1]
+        assert nxt[b] == tgt[b, k - 1]
+
+
 ALL_PINS = [pin_conv_numpy, pin_conv_taps, pin_dense_product, pin_beta_zero, pin_orthonormal_store,
             pin_one_step_store, pin_key_head_sharing, pin_commit_prefix, pin_restore_and_inert,
-            pin_prefill_is_verify_commit, pin_chunked_wy, pin_golden_hand, pin_row_separable]
+            pin_prefill_is_verify_commit, pin_chunked_wy, pin_golden_hand, pin_row_separable,
+            pin_accept_hand, pin_accept_ties_and_nan, pin_accept_random]

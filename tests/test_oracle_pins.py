@@ -48,6 +48,10 @@ MUTANTS = {
     "inactive_commits": ("    if (active[b]) {\n      if (keep[b] >= 0", "    if (1) {\n      if (keep[b] >= 0"),
     "window_not_advanced": ("      for (int i = 0; i < OR_HIST; ++i) wc[i] = tail[i];", "      (void)tail;"),
     "decay_missing_on_state": ("row[i] = a * row[i] + e * k[i];", "row[i] = row[i] + e * k[i];"),
+    "accept_ties_last": ("if (best < 0 || x > best_v) {", "if (best < 0 || x >= best_v) {"),
+    "accept_wrong_target": ("draft[(size_t)b * T + k] == target[k - 1]", "draft[(size_t)b * T + k] == target[k]"),
+    "accept_next_from_last": ("    next[b] = target[k - 1];", "    next[b] = target[T - 1];"),
+    "accept_inactive_kept": ("    if (!active[b]) {\n      keep[b] = 0;", "    if (0) {\n      keep[b] = 0;"),
 }
 
 
