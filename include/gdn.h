@@ -295,6 +295,32 @@ int gdn_conv_verify_noalloc(const gdn_dims *dims, int mode, const gdn_bf16 *x, c
  */
 int gdn_get_status(int clear, uint32_t *status);
 
+/* ---- on-device greedy acceptance ---------------------------------------------
+ * "Add request-owned eight-way MTP serving for Qwen 35B" takes the acceptance
+ * decision of the batched decode cycle off the host, so a cycle needs no host
+ * synchronisation.  Position 0 of a row's verify holds the last accepted
+ * token, positions 1..T-1 the draft tokens.  For every active row b:
+ *   target_t = argmax_v logits[b][t][v]   first index of the maximum; NaN never
+ *                                          wins; an all-NaN position gives 0
+ *   keep[b]  = 1 + the number of leading t in 1..T-1 with
+ *              draft[b][t] == target_{t-1}
+ *   next[b]  = target_{keep[b]-1}          the token the next cycle feeds
+ * Inactive rows get keep 0 and next -1.  keep is what gdn_commit takes, so
+ * verify -> accept -> commit runs on one stream with no host round trip.
+ *
+ *  logits [B][T][V]  bf16   device, read only
+ *  draft  [B][T]     int32  device; draft[b][0] is not read
+ *  active [B]        uint8  device
+ *  keep, next [B]    int32  device, written
+ *  ws                device scratch of gdn_accept_workspace_bytes(B, T, V)
+ *                    bytes, zero-filled once before its first use (each call
+ *                    leaves it ready for the next)
+ * Supported: 1 <= T <= 64, V >= 1, B*T <= 65535.  Errors as for every call.
+ */
+size_t gdn_accept_workspace_bytes(int B, int T, int V);
+int gdn_accept_greedy(int B, int T, int V, const gdn_bf16 *logits, const int32_t *draft, const uint8_t *active,
+                      int32_t *keep, int32_t *next, void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -286,6 +286,32 @@ __attribute__((visibility("default"))) int gdn_get_status(int clear, uint32_t *s
   return ok();
 }
 
+__attribute__((visibility("default"))) size_t gdn_accept_workspace_bytes(int B, int T, int V) {
+  if (B < 0 || T < 1 || T > kMaxAcceptT || V < 1) return 0;
+  return accept_workspace_bytes(B, T, V);
+}
+
+__attribute__((visibility("default"))) int gdn_accept_greedy(int B, int T, int V, const gdn_bf16 *logits,
+                                                             const int32_t *draft, const uint8_t *active,
+                                                             int32_t *keep, int32_t *next, void *ws,
+                                                             size_t ws_bytes, void *stream) {
+  if (B < 0 || T < 1 || V < 1) return fail(GDN_ERR_INVALID_ARG, "accept: B=%d T=%d V=%d", B, T, V);
+  if (T > kMaxAcceptT) return fail(GDN_ERR_UNSUPPORTED, "accept: T=%d above %d", T, kMaxAcceptT);
+  if ((long long)B * T > 65535) return fail(GDN_ERR_UNSUPPORTED, "accept: B*T=%lld above 65535", (long long)B * T);
+  if (B == 0) return ok();
+  GDN_NEED_PTR(logits, 16);
+  GDN_NEED_PTR(draft, 16);
+  GDN_NEED_PTR(active, 16);
+  GDN_NEED_PTR(keep, 16);
+  GDN_NEED_PTR(next, 16);
+  GDN_NEED_PTR(ws, 256);
+  const size_t need = accept_workspace_bytes(B, T, V);
+  if (ws_bytes < need) return fail(GDN_ERR_WORKSPACE, "accept workspace has %zu bytes, needs %zu", ws_bytes, need);
+  cudaError_t e = launch_accept(logits, draft, active, keep, next, ws, B, T, V, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_accept_greedy launch");
+  return ok();
+}
+
 // ---- verify without caller-provided workspace ---------------------------------
 // Scratch for gdn_conv_verify_noalloc: one layer's verify captures.  It lives
 // in the library's own device memory, so every GPU that loads the library

@@ -406,5 +406,9 @@ cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g,
                            uint16_t *ring, int32_t *offsets, uint16_t *out, void *ws, int B, int L, int H_k,
                            int H_v, int D, int R, int act, cudaStream_t stream);
 uint32_t *status_word_address();  // device address of the sticky status word
+constexpr int kMaxAcceptT = 64;   // positions per row the acceptance kernel handles
+size_t accept_workspace_bytes(int B, int T, int V);
+cudaError_t launch_accept(const uint16_t *logits, const int32_t *draft, const uint8_t *active, int32_t *keep,
+                          int32_t *next, void *ws, int B, int T, int V, cudaStream_t stream);
 
 }  // namespace gdn

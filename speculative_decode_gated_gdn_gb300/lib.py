@@ -33,7 +33,7 @@ GDN_NOALLOC_WS_BYTES = 4 << 20
 
 EXPORTS = ("gdn_version", "gdn_last_error", "gdn_layer_workspace_bytes", "gdn_conv_verify",
            "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status",
-           "gdn_conv_verify_noalloc", "gdn_flush")
+           "gdn_conv_verify_noalloc", "gdn_flush", "gdn_accept_workspace_bytes", "gdn_accept_greedy")
 
 
 class GdnError(RuntimeError):
@@ -83,6 +83,10 @@ def _declare(lib):
     lib.gdn_conv_verify_noalloc.argtypes = [D, ctypes.c_int] + [_P] * 9 + [ctypes.POINTER(_P), _P]
     lib.gdn_get_status.restype = ctypes.c_int
     lib.gdn_get_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)]
+    lib.gdn_accept_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_accept_workspace_bytes.argtypes = [ctypes.c_int] * 3
+    lib.gdn_accept_greedy.restype = ctypes.c_int
+    lib.gdn_accept_greedy.argtypes = [ctypes.c_int] * 3 + [_P] * 6 + [ctypes.c_size_t, _P]
 
 
 def library_path() -> str:
@@ -229,6 +233,23 @@ def gdn_prefill_chunked(d: gdn_dims, L, x, conv_w, g, beta, state, ring, offsets
         _ptr(ring, "ring", torch.bfloat16), _ptr(offsets, "offsets", torch.int32),
         _ptr(out, "out", torch.bfloat16), _ptr(ws, "ws"), int(ws_bytes), _stream(stream))
     _check(rc, "gdn_prefill_chunked")
+
+
+def gdn_accept_workspace_bytes(B: int, T: int, V: int) -> int:
+    return int(load().gdn_accept_workspace_bytes(B, T, V))
+
+
+def gdn_accept_greedy(logits, draft, active, keep, nxt, ws, stream=None):
+    """Greedy acceptance on the device: logits [B][T][V] bf16, draft [B][T]
+    int32, active [B] uint8 -> keep [B], nxt [B] int32 (written in place).
+    ws: gdn_accept_workspace_bytes(B, T, V) bytes, zero-filled once."""
+    torch = _t()
+    B, T, V = logits.shape
+    rc = load().gdn_accept_greedy(B, T, V, _ptr(logits, "logits", torch.bfloat16), _ptr(draft, "draft", torch.int32),
+                                  _ptr(active, "active", torch.uint8), _ptr(keep, "keep", torch.int32),
+                                  _ptr(nxt, "next", torch.int32), _ptr(ws, "ws"),
+                                  ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "gdn_accept_greedy")
 
 
 def gdn_get_status(clear: bool = False) -> int:

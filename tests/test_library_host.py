@@ -136,6 +136,19 @@ def test_deferred_workspace_size(lib):
     assert dfr % 256 == 0
 
 
+def test_accept_argument_checks(lib):
+    assert lib.gdn_accept_workspace_bytes(8, 2, 151936) > 0
+    assert lib.gdn_accept_workspace_bytes(8, 0, 10) == 0 and lib.gdn_accept_workspace_bytes(8, 65, 10) == 0
+    g = 1 << 20
+    ws = lib.gdn_accept_workspace_bytes(8, 2, 1000)
+    assert lib.gdn_accept_greedy(8, 2, 1000, None, g, g, g, g, g, ws, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_accept_greedy(8, 2, 1000, g + 2, g, g, g, g, g, ws, None) == L.GDN_ERR_MISALIGNED
+    assert lib.gdn_accept_greedy(8, 2, 1000, g, g, g, g, g, g, ws - 1, None) == L.GDN_ERR_WORKSPACE
+    assert lib.gdn_accept_greedy(8, 65, 1000, g, g, g, g, g, g, 1 << 30, None) == L.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_accept_greedy(8, 0, 1000, g, g, g, g, g, g, 1 << 30, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_accept_greedy(0, 2, 1000, None, None, None, None, None, None, 0, None) == L.GDN_OK
+
+
 def test_empty_batch_is_a_no_op(lib):
     d = L.dims(0, 2, 16, 32, 128)
     assert lib.gdn_conv_verify(ctypes.byref(d), 0, *([None] * 10), 0, None) == L.GDN_OK
