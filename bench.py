@@ -70,8 +70,13 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--workload", default="cycle", choices=["cycle", "prefill"],
-                    help="cycle: the verify+commit headline; prefill: chunked state priming of one row")
+    ap.add_argument("--workload", default="cycle", choices=["cycle", "prefill", "accept"],
+                    help="cycle: the verify+commit headline; prefill: chunked state priming of one row; "
+                         "accept: the on-device greedy acceptance kernel alone")
+    ap.add_argument("--accept", action="store_true",
+                    help="cycle: take keep from gdn_accept_greedy on synthetic logits (verify + accept + commit "
+                         "per graph) instead of drawing it")
+    ap.add_argument("--V", type=int, default=151936, help="vocabulary size for acceptance")
     ap.add_argument("--L", type=int, default=4096, help="prompt length for --workload prefill")
     return ap.parse_args()
 
@@ -90,10 +95,14 @@ def workload(args):
 
 
 def config_dict(args, geom, inactive):
+    acc = getattr(args, "accept", False)
+    keep_txt = (f"keep from on-device greedy acceptance over V={args.V} (drafts planted so keep~U{{1..{geom.T}}}), "
+                f"verify+accept+commit per graph" if acc else f"keep~U{{0..{geom.T}}} per cycle")
     return {
         "workload": (f"GDN verify+commit cycle: B={geom.B} T={geom.T} H_k={geom.H_k} H_v={geom.H_v} "
-                     f"d={geom.d} x {args.layers} layers, keep~U{{0..{geom.T}}} per cycle, "
+                     f"d={geom.d} x {args.layers} layers, {keep_txt}, "
                      f"inactive rows {list(inactive)}"),
+        "keep_source": "gdn_accept_greedy" if acc else "drawn",
         "B": geom.B, "T": geom.T, "H_k": geom.H_k, "H_v": geom.H_v, "d": geom.d,
         "layers": args.layers, "commit_mode": args.mode, "inactive_rows": list(inactive),
         "l2": f"no flush: state stack {args.layers * geom.B * geom.H_v * geom.d * geom.d * 4 / 2**20:.0f} MiB "
@@ -365,6 +374,23 @@ def run_gpu(args, rank, world, local):
     active_np = synth.active_mask(geom.B, inactive)
     keeps_np = synth.keep_draws(geom, seed, K + W)
     inp = [synth.cycle_inputs(geom, seed, p, n_layers) for p in range(pool)]
+    if args.accept:
+        # synthetic logits per pool entry, and per cycle drafts that repeat the
+        # targets for the drawn number of positions: greedy acceptance then
+        # reproduces the draw (at least 1: position 0 is always kept)
+        V = args.V
+        lg_bits = [synth.normal_bf16(seed + 7, f"logits{p}", geom.B * geom.T * V).reshape(geom.B, geom.T, V)
+                   for p in range(pool)]
+        tg = [np.argmax(synth.bf16_to_f32(bb), axis=2) for bb in lg_bits]
+        keeps_np = np.maximum(keeps_np, 1).astype(np.int32)
+        drafts_np = np.zeros((K + W, geom.B, geom.T), np.int32)
+        for c in range(K + W):
+            t_p = tg[c % pool]
+            for b in range(geom.B):
+                k = int(keeps_np[c, b])
+                drafts_np[c, b, 1:k] = t_p[b, :k - 1]
+                if k < geom.T:
+                    drafts_np[c, b, k] = (t_p[b, k - 1] + 1) % V
 
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -383,11 +409,20 @@ def run_gpu(args, rank, world, local):
     bs = [torch.from_numpy(c["beta"]).to(dev) for c in inp]
     states = [state[l] for l in range(n_layers)]
     rings = [ring[l] for l in range(n_layers)]
+    if args.accept:
+        lgs = [bf(bb) for bb in lg_bits]
+        drafts = torch.from_numpy(drafts_np).to(dev)
+        keep_dev = torch.zeros(geom.B, dtype=torch.int32, device=dev)
+        next_dev = torch.zeros(geom.B, dtype=torch.int32, device=dev)
+        ws_acc = torch.zeros(L.gdn_accept_workspace_bytes(geom.B, geom.T, args.V), dtype=torch.uint8, device=dev)
 
     def cycle(c, x, g, beta, keep, ev=None):
         for l in range(n_layers):
             L.gdn_conv_verify(d, verify_mode(mode, l), x[l], conv_w[l], g[l], beta[l], state[l], ring[l],
                               offsets, active, out[l], ws[l], ws_bytes)
+        if args.accept:
+            L.gdn_accept_greedy(lgs[c % pool], drafts[c], active, keep_dev, next_dev, ws_acc)
+            keep = keep_dev
         if ev is not None:
             ev[0].record()
         L.gdn_commit(d, mode, states, rings, ws, keep, active, offsets)
@@ -486,7 +521,7 @@ def run_gpu(args, rank, world, local):
                 "verify_gbs": round(verify_gbs, 1), "verify_avg_ms_incl_gaps": round(verify_avg_ms, 5),
                 "commit_gbs": round(commit_gbs, 1), "commit_avg_ms": round(commit_avg_ms, 5)},
         "roofline": roof,
-        "gpu_launches": K * (n_layers + 1),
+        "gpu_launches": K * (n_layers + 1 + int(args.accept)),
         "clocks": clk.summary(),
     }
 
@@ -574,6 +609,59 @@ def prefill_flops(L, H_v, d, chunk=64):
         n = min(chunk, L - c0)
         total += H_v * (4 * 2 * n * n * d + 3 * 2 * n * d * d + 2 * n * n * d + n ** 3 // 3)
     return total
+
+
+def run_accept_bench(args, rank, world, local):
+    """Time gdn_accept_greedy alone: B x T positions over a V-entry vocabulary
+    per launch, logits rotated over more distinct buffers than L2 holds."""
+    import torch
+    from speculative_decode_gated_gdn_gb300 import lib as L
+    from speculative_decode_gated_gdn_gb300 import synth
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, T, V, K, W = args.B, args.T, args.V, args.steps, args.warmup
+    seed = rank_seed(args.seed, rank)
+    base = [synth.normal_bf16(seed, f"logits{i}", B * T * V).reshape(B, T, V) for i in range(4)]
+    per = B * T * V * 2
+    n_buf = max(8, int(3 * 129e6 // per) + 1)  # three times L2 between reuses
+    lgs = [torch.from_numpy(base[i % 4].view(np.int16)).to(dev).view(torch.bfloat16) for i in range(n_buf)]
+    draft = torch.zeros((B, T), dtype=torch.int32, device=dev)
+    active = torch.from_numpy(synth.active_mask(B, workload(args)[1])).to(dev)
+    keep = torch.zeros(B, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(B, dtype=torch.int32, device=dev)
+    ws = torch.zeros(L.gdn_accept_workspace_bytes(B, T, V), dtype=torch.uint8, device=dev)
+    # K launches in one CUDA graph, so the device time is measured, not the
+    # host's launch rate
+    side = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(side):
+        for i in range(W):
+            L.gdn_accept_greedy(lgs[i % n_buf], draft, active, keep, nxt, ws)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=side):
+        for i in range(K):
+            L.gdn_accept_greedy(lgs[i % n_buf], draft, active, keep, nxt, ws)
+    gr.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    gr.replay()
+    end.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), dev, world) / K
+    n_active = int(active.sum().item())
+    alg = n_active * T * V * 2
+    peak, peak_kind = measured_peak()
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"metric": "greedy acceptance positions/s", "value": job_rate(world, B * T, ms), "unit": "positions/s",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"gdn_accept_greedy B={B} T={T} V={V}, {n_active} active rows, "
+                                   f"{n_buf} logits buffers in rotation", "B": B, "T": T, "V": V},
+            "roofline": {"kernel": "accept_kernel", "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None, "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": alg, "avg_launch_ms": round(ms, 5)},
+            "gpu_launches": K}
 
 
 def run_prefill_bench(args, rank, world, local):
@@ -684,8 +772,8 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
-    if args.workload == "prefill":
-        res = run_prefill_bench(args, rank, world, local)
+    if args.workload in ("prefill", "accept"):
+        res = (run_prefill_bench if args.workload == "prefill" else run_accept_bench)(args, rank, world, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

@@ -77,14 +77,25 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
     const uint16_t *row = p.logits + size_t(bt) * p.V;
     AccBest best{0.f, -1};
     if ((p.V & 7) == 0) {
-      // 8 entries per 16-byte load; a thread's entries arrive in increasing order
-      for (int v = v0 + 8 * tid; v < v1; v += 8 * kAccThreads) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(row + v);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      // 8 entries per 16-byte load, all of a thread's loads issued before
+      // any comparison; its entries arrive in increasing order
+      constexpr int kLoads = kAccSlice / (8 * kAccThreads);
+      uint4 q[kLoads];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc_take(best, bf2f(uint16_t(w[j] & 0xffff)), v + 2 * j);
-          acc_take(best, bf2f(uint16_t(w[j] >> 16)), v + 2 * j + 1);
+      for (int r = 0; r < kLoads; ++r) {
+        const int v = v0 + 8 * (tid + r * kAccThreads);
+        q[r] = v < v1 ? *reinterpret_cast<const uint4 *>(row + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int r = 0; r < kLoads; ++r) {
+        const int v = v0 + 8 * (tid + r * kAccThreads);
+        if (v < v1) {
+          const uint32_t w[4] = {q[r].x, q[r].y, q[r].z, q[r].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc_take(best, bf2f(uint16_t(w[j] & 0xffff)), v + 2 * j);
+            acc_take(best, bf2f(uint16_t(w[j] >> 16)), v + 2 * j + 1);
+          }
         }
       }
     } else {
@@ -119,14 +130,16 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
     }
     return;
   }
-  if (tid < p.T) {
+  // one warp per position: the lanes read the slices' results in parallel
+  for (int t = warp; t < p.T; t += kAccThreads / 32) {
     AccBest r{0.f, -1};
-    const size_t base = (size_t(b) * p.T + tid) * p.NB;
-    for (int s = 0; s < p.NB; ++s) {
+    const size_t base = (size_t(b) * p.T + t) * p.NB;
+    for (int s = lane; s < p.NB; s += 32) {
       const AccBest o{__ldcg(p.pmax + base + s), __ldcg(p.pidx + base + s)};
       if (acc_better(o, r)) r = o;
     }
-    s_target[tid] = r.i < 0 ? 0 : r.i;
+    r = acc_warp_reduce(r);
+    if (lane == 0) s_target[t] = r.i < 0 ? 0 : r.i;
   }
   __syncthreads();
   if (tid == 0) {
