@@ -75,6 +75,8 @@ class Oracle:
         lib.oracle_prefill.restype = _int
         lib.oracle_accept.argtypes = [_int] * 3 + [_D, _I, _U8, _I, _I]
         lib.oracle_accept.restype = _int
+        lib.oracle_gated_rmsnorm.argtypes = [_int, _int, _D, _D, _D, ctypes.c_double, _D]
+        lib.oracle_gated_rmsnorm.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -159,6 +161,15 @@ class Oracle:
         return keep, nxt
 
 
+    def gated_rmsnorm(self, o, z, w, eps=1e-6):
+        """y = o / sqrt(mean(o^2) + eps) * w * silu(z) over the last axis (fp64)."""
+        o, z, w = _f64(o), _f64(z), _f64(w)
+        d = o.shape[-1]
+        y = np.empty_like(o)
+        self.lib.oracle_gated_rmsnorm(int(o.size // d), d, _p(o, _D), _p(z, _D), _p(w, _D), float(eps), _p(y, _D))
+        return y
+
+
 _default = None
 
 
@@ -191,3 +202,7 @@ def prefill(*a, **k):
 
 def accept(*a, **k):
     return default().accept(*a, **k)
+
+
+def gated_rmsnorm(*a, **k):
+    return default().gated_rmsnorm(*a, **k)

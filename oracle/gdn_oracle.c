@@ -292,3 +292,26 @@ OR_EXPORT int oracle_accept(int B, int T, int V, const double *logits, const int
   free(target);
   return 0;
 }
+
+/*
+ * Gated RMSNorm of the GDN output, the step that follows the mixer in the
+ * hybrid-Qwen GDN layer ("MTP inference: review and commit structure",
+ * Functional commits item 4, names it beside the conv-cache mutation as a
+ * custom-operator boundary).  Per (row, position, value head) vector o of d
+ * values with gate z and weight w [d]:
+ *   y[j] = o[j] / sqrt(mean_j o[j]^2 + eps) * w[j] * silu(z[j]),  silu(z) = z / (1 + e^-z)
+ * o, z, y [n][d]; w [d].
+ */
+OR_EXPORT void oracle_gated_rmsnorm(int n, int d, const double *o, const double *z, const double *w, double eps,
+                                    double *y) {
+  for (int r = 0; r < n; ++r) {
+    const double *orow = o + (size_t)r * d, *zrow = z + (size_t)r * d;
+    double ss = 0.0;
+    for (int j = 0; j < d; ++j) ss += orow[j] * orow[j];
+    const double inv = 1.0 / sqrt(ss / d + eps);
+    for (int j = 0; j < d; ++j) {
+      const double gate = zrow[j] / (1.0 + exp(-zrow[j]));
+      y[(size_t)r * d + j] = orow[j] * inv * w[j] * gate;
+    }
+  }
+}

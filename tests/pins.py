@@ -21,7 +21,9 @@ when the oracle disagrees with:
 * a hand-worked example stored under tests/golden/,
 * for greedy acceptance: numpy's argmax (the first index of the maximum),
   hand-built drafts whose accepted prefix is known by construction, and the
-  defining properties of the accepted prefix.
+  defining properties of the accepted prefix,
+* for the gated RMSNorm: torch's rms_norm and silu (double precision, CPU),
+  and the unit root-mean-square of the normalised vector.
 
 They are plain functions (not tests) so that ``test_oracle_pins.py`` can also
 run them against builds of the oracle with planted mistakes and show that each
@@ -412,7 +414,26 @@ def pin_accept_random(orc):
         assert nxt[b] == tgt[b, k - 1]
 
 
+def pin_gated_rmsnorm(orc):
+    """Gated RMSNorm against torch's library rms_norm and silu in float64, and
+    its defining property: with w = 1 and the gate divided out, the vector has
+    unit root mean square (up to eps)."""
+    import torch
+    rng = np.random.default_rng(11)
+    o = rng.normal(size=(5, 3, 64)) * rng.uniform(0.01, 3.0, size=(5, 3, 1))
+    z = rng.normal(size=o.shape) * 2.0
+    w = rng.normal(size=64)
+    eps = 1e-6
+    y = orc.gated_rmsnorm(o, z, w, eps)
+    to = torch.from_numpy(o)
+    ref = torch.nn.functional.rms_norm(to, (64,), weight=torch.from_numpy(w), eps=eps) * \
+        torch.nn.functional.silu(torch.from_numpy(z))
+    assert np.allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
+    u = orc.gated_rmsnorm(o, np.full(o.shape, 30.0), np.ones(64), 0.0) / (30.0 / (1.0 + np.exp(-30.0)))
+    assert np.allclose(np.sqrt((u ** 2).mean(axis=-1)), 1.0, rtol=1e-12)
+
+
 ALL_PINS = [pin_conv_numpy, pin_conv_taps, pin_dense_product, pin_beta_zero, pin_orthonormal_store,
             pin_one_step_store, pin_key_head_sharing, pin_commit_prefix, pin_restore_and_inert,
             pin_prefill_is_verify_commit, pin_chunked_wy, pin_golden_hand, pin_row_separable,
-            pin_accept_hand, pin_accept_ties_and_nan, pin_accept_random]
+            pin_accept_hand, pin_accept_ties_and_nan, pin_accept_random, pin_gated_rmsnorm]

@@ -52,6 +52,9 @@ MUTANTS = {
     "accept_wrong_target": ("draft[(size_t)b * T + k] == target[k - 1]", "draft[(size_t)b * T + k] == target[k]"),
     "accept_next_from_last": ("    next[b] = target[k - 1];", "    next[b] = target[T - 1];"),
     "accept_inactive_kept": ("    if (!active[b]) {\n      keep[b] = 0;", "    if (0) {\n      keep[b] = 0;"),
+    "norm_sum_not_mean": ("const double inv = 1.0 / sqrt(ss / d + eps);", "const double inv = 1.0 / sqrt(ss + eps);"),
+    "gate_sigmoid": ("const double gate = zrow[j] / (1.0 + exp(-zrow[j]));", "const double gate = 1.0 / (1.0 + exp(-zrow[j]));"),
+    "norm_weight_dropped": ("y[(size_t)r * d + j] = orow[j] * inv * w[j] * gate;", "y[(size_t)r * d + j] = orow[j] * inv * gate;"),
 }
 
 
