@@ -192,6 +192,25 @@ int gdn_conv_verify(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn
                     void *layer_ws, size_t layer_ws_bytes, void *stream);
 
 /*
+ * gdn_conv_verify followed, in the same kernel, by the gated RMSNorm that
+ * comes after the GDN mixer in the hybrid-Qwen layer ("MTP inference: review
+ * and commit structure", Functional commits item 4, keeps it behind its own
+ * operator boundary): per (row, position, value head)
+ *   out[j] = o[j] / sqrt(mean_j o[j]^2 + eps) * norm_w[j] * silu(gate_z[j])
+ * with o the verify output (fp32 inside the kernel, never rounded).
+ *  gate_z  [B][T][H_v][d_v] bf16  device, read only
+ *  norm_w  [d_v]            bf16  device, read only (shared by all heads)
+ *  eps     finite, >= 0
+ * Everything else, including the captures for gdn_commit, is as for
+ * gdn_conv_verify; inactive rows get out = 0.
+ */
+int gdn_conv_verify_gated(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w,
+                          const float *g, const float *beta, const float *state, gdn_bf16 *ring,
+                          const int32_t *offsets, const uint8_t *active, const gdn_bf16 *gate_z,
+                          const gdn_bf16 *norm_w, float eps, gdn_bf16 *out, void *layer_ws,
+                          size_t layer_ws_bytes, void *stream);
+
+/*
  * Commit the accepted prefix of every row for n_layers layers in one launch
  * (grouped across layers).  keep'[b] = keep[b] if active[b] and
  * 0 <= keep[b] <= T, else 0 (an active row with keep outside [0, T] also sets

@@ -9,6 +9,7 @@
 // layers).
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <mutex>
 #include <string>
 
@@ -118,10 +119,12 @@ __attribute__((visibility("default"))) size_t gdn_layer_workspace_bytes(const gd
   return layer_ws_bytes(dims, mode);
 }
 
-__attribute__((visibility("default"))) int gdn_conv_verify(
-    const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
-    const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
-    const uint8_t *active, gdn_bf16 *out, void *layer_ws, size_t layer_ws_bytes_given, void *stream) {
+namespace {
+
+int verify_impl(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
+                const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
+                const uint8_t *active, const gdn_bf16 *gate_z, const gdn_bf16 *norm_w, float eps, gdn_bf16 *out,
+                void *layer_ws, size_t layer_ws_bytes_given, void *stream) {
   int rc = check_dims(dims);
   if (rc) return rc;
   if (mode & ~(GDN_VERIFY_OVERLAP | 0xff))
@@ -161,6 +164,9 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
   p.R = kHist + dims->T_max;
   p.act = dims->act;
   p.overlap = overlap;
+  p.gz = gate_z;
+  p.gw = norm_w;
+  p.geps = eps;
   p.status = status_word_address();
   if (!p.status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
   char *ws = static_cast<char *>(layer_ws);
@@ -189,6 +195,30 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
   }
   if (e != cudaSuccess) return cuda_fail(e, "gdn_conv_verify launch");
   return ok();
+}
+
+}  // namespace
+
+__attribute__((visibility("default"))) int gdn_conv_verify(
+    const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
+    const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
+    const uint8_t *active, gdn_bf16 *out, void *layer_ws, size_t layer_ws_bytes_given, void *stream) {
+  return verify_impl(dims, mode, x, conv_w, g, beta, state, ring, offsets, active, nullptr, nullptr, 0.f, out,
+                     layer_ws, layer_ws_bytes_given, stream);
+}
+
+__attribute__((visibility("default"))) int gdn_conv_verify_gated(
+    const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
+    const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
+    const uint8_t *active, const gdn_bf16 *gate_z, const gdn_bf16 *norm_w, float eps, gdn_bf16 *out,
+    void *layer_ws, size_t layer_ws_bytes_given, void *stream) {
+  if (check_dims(dims) == GDN_OK && dims->B > 0) {
+    GDN_NEED_PTR(gate_z, 16);
+    GDN_NEED_PTR(norm_w, 16);
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(GDN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  }
+  return verify_impl(dims, mode, x, conv_w, g, beta, state, ring, offsets, active, gate_z, norm_w, eps, out,
+                     layer_ws, layer_ws_bytes_given, stream);
 }
 
 __attribute__((visibility("default"))) int gdn_commit(const gdn_dims *dims, int mode, int n_layers,

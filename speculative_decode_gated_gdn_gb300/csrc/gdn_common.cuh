@@ -339,6 +339,10 @@ struct VerifyParams {
   uint32_t *status; // sticky device status word
   int B, T, H_k, H_v, C, R, act;
   int overlap;      // GDN_VERIFY_OVERLAP: stage the state tile before the PDL wait
+  // optional gated RMSNorm of the output: out = o / rms(o) * w * silu(z)
+  const uint16_t *gz;  // [B][T][H_v][d_v] bf16 gate, or nullptr (plain o)
+  const uint16_t *gw;  // [d_v] bf16 weight
+  float geps;
 };
 
 constexpr int kMaxLayers = GDN_MAX_LAYERS;

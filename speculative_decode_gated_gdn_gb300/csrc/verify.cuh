@@ -108,6 +108,7 @@ struct VerifySmem {
   float ce[T][D];
   float ck[T][D];
   float cG[kMaxT];
+  float gsq[T][8];  // gated RMSNorm: per-warp sums of o_t^2 (at most 8 warps)
   uint64_t bar[D / kTileRows];
   uint64_t cbar;
 };
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   constexpr int ROWS_W = D / NWARP;   // state rows per warp, in groups of 8
   constexpr int NGRP = ROWS_W / 8;
   static_assert(ROWS_W % 8 == 0 && NWARP * ROWS_W == D, "rows must split evenly over warps");
+  static_assert(NWARP <= 8, "the gated-norm partial sums hold 8 warps");
   constexpr int NT = D / kTileRows;   // 32-row tiles, one bulk copy and barrier each
   // per-head reductions: |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t)
   constexpr int NKK = T * (T - 1) / 2, NKQ = T * (T + 1) / 2, NV = 2 * T + NKK + NKQ;
@@ -420,13 +422,26 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   // ---- 5. this warp's rows, in groups of 8 (the state is already staged,
   // and in DEFERRED mode already brought up to date) -------------------------
   const size_t plane = size_t(p.B) * H_v * D * D;
+  const bool gated = p.gz != nullptr;
+  float og[NGRP][T];           // gated: o of the rows this lane leads, until the norm is known
+  uint16_t zg[NGRP][T], wg[NGRP];
+  if (gated && leader) {       // the gate and weight of those rows, loaded now
+#pragma unroll
+    for (int grp8 = 0; grp8 < NGRP; ++grp8) {
+      const int jrow = jw0 + 8 * grp8 + grp + GPW * istar;
+      wg[grp8] = p.gw[jrow];
+#pragma unroll
+      for (int t = 0; t < T; ++t) zg[grp8][t] = p.gz[((size_t(b) * T + t) * H_v + h) * D + jrow];
+    }
+  }
+  bool bad = false;
 #pragma unroll
   for (int grp8 = 0; grp8 < NGRP; ++grp8) {
     const int jw = jw0 + 8 * grp8;  // first state row of this group
     const int jrow = jw + grp + GPW * istar;
     if ((grp8 * 8) % kTileRows == 0 && !mbar_wait_bounded(&sm.bar[jw / kTileRows], 0)) {
-      give_up();
-      return;
+      bad = true;
+      break;
     }
     float4 s[RPL];
 #pragma unroll
@@ -469,7 +484,10 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     if (leader) {
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        p.out[((size_t(b) * T + t) * H_v + h) * D + jrow] = f2bf(o[t]);
+        if (gated)
+          og[grp8][t] = o[t];
+        else
+          p.out[((size_t(b) * T + t) * H_v + h) * D + jrow] = f2bf(o[t]);
         if (MODE != GDN_COMMIT_SNAPSHOT) p.ws_e[(bh * T + t) * D + jrow] = e[t];
       }
     }
@@ -493,6 +511,45 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
         }
       }
     }
+  }
+  if (gated) {
+    // out = o_t / sqrt(mean_j o_t[j]^2 + eps) * w[j] * silu(z_t[j]) over the
+    // head's d_v rows, which the CTA's warps share: one more block barrier
+    // (reached by every thread; a timed-out warp leaves after it)
+    if (__syncthreads_or(bad)) {
+      if (bad) give_up();
+      return;
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      float q2 = 0.f;
+      if (leader)
+#pragma unroll
+        for (int grp8 = 0; grp8 < NGRP; ++grp8) q2 = fmaf(og[grp8][t], og[grp8][t], q2);
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, m);
+      if (lane == 0) sm.gsq[t][warp] = q2;
+    }
+    __syncthreads();
+    if (leader) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        float ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) ss += sm.gsq[t][w];
+        const float rstd = rsqrtf(ss / float(D) + p.geps);
+#pragma unroll
+        for (int grp8 = 0; grp8 < NGRP; ++grp8) {
+          const int jrow = jw0 + 8 * grp8 + grp + GPW * istar;
+          const float z = bf2f(zg[grp8][t]);
+          p.out[((size_t(b) * T + t) * H_v + h) * D + jrow] =
+              f2bf(og[grp8][t] * rstd * bf2f(wg[grp8]) * silu_fast(z));
+        }
+      }
+    }
+  } else if (bad) {
+    give_up();
+    return;
   }
   // every warp applied its rows before the conv barrier
   if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) p.ws_pend[bh] = 0;  // (a repeat if applied before the wait)

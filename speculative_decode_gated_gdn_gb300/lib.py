@@ -33,7 +33,8 @@ GDN_NOALLOC_WS_BYTES = 4 << 20
 
 EXPORTS = ("gdn_version", "gdn_last_error", "gdn_layer_workspace_bytes", "gdn_conv_verify",
            "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status",
-           "gdn_conv_verify_noalloc", "gdn_flush", "gdn_accept_workspace_bytes", "gdn_accept_greedy")
+           "gdn_conv_verify_noalloc", "gdn_flush", "gdn_accept_workspace_bytes", "gdn_accept_greedy",
+           "gdn_conv_verify_gated")
 
 
 class GdnError(RuntimeError):
@@ -83,6 +84,8 @@ def _declare(lib):
     lib.gdn_conv_verify_noalloc.argtypes = [D, ctypes.c_int] + [_P] * 9 + [ctypes.POINTER(_P), _P]
     lib.gdn_get_status.restype = ctypes.c_int
     lib.gdn_get_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)]
+    lib.gdn_conv_verify_gated.restype = ctypes.c_int
+    lib.gdn_conv_verify_gated.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_float, _P, _P, ctypes.c_size_t, _P]
     lib.gdn_accept_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_accept_workspace_bytes.argtypes = [ctypes.c_int] * 3
     lib.gdn_accept_greedy.restype = ctypes.c_int
@@ -169,6 +172,23 @@ def gdn_conv_verify(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets,
         _ptr(active, "active", torch.uint8), _ptr(out, "out", torch.bfloat16), _ptr(layer_ws, "layer_ws"),
         int(layer_ws_bytes), _stream(stream))
     _check(rc, "gdn_conv_verify")
+
+
+def gdn_conv_verify_gated(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets, active, gate_z, norm_w,
+                          eps, out, layer_ws, layer_ws_bytes=None, stream=None):
+    """gdn_conv_verify with the gated RMSNorm of the output fused in:
+    out = o / sqrt(mean(o^2) + eps) * norm_w * silu(gate_z) per (row, position, head)."""
+    torch = _t()
+    if layer_ws_bytes is None:
+        layer_ws_bytes = layer_ws.numel() * layer_ws.element_size()
+    rc = load().gdn_conv_verify_gated(
+        ctypes.byref(d), mode, _ptr(x, "x", torch.bfloat16), _ptr(conv_w, "conv_w", torch.bfloat16),
+        _ptr(g, "g", torch.float32), _ptr(beta, "beta", torch.float32), _ptr(state, "state", torch.float32),
+        _ptr(ring, "ring", torch.bfloat16), _ptr(offsets, "offsets", torch.int32),
+        _ptr(active, "active", torch.uint8), _ptr(gate_z, "gate_z", torch.bfloat16),
+        _ptr(norm_w, "norm_w", torch.bfloat16), float(eps), _ptr(out, "out", torch.bfloat16),
+        _ptr(layer_ws, "layer_ws"), int(layer_ws_bytes), _stream(stream))
+    _check(rc, "gdn_conv_verify_gated")
 
 
 def gdn_conv_verify_noalloc(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets, active, out,
