@@ -77,6 +77,8 @@ def parse_args():
                     help="cycle: take keep from gdn_accept_greedy on synthetic logits (verify + accept + commit "
                          "per graph) instead of drawing it")
     ap.add_argument("--V", type=int, default=151936, help="vocabulary size for acceptance")
+    ap.add_argument("--gated", action="store_true",
+                    help="cycle: verify through gdn_conv_verify_gated (gated RMSNorm of the output fused in)")
     ap.add_argument("--L", type=int, default=4096, help="prompt length for --workload prefill")
     return ap.parse_args()
 
@@ -103,6 +105,7 @@ def config_dict(args, geom, inactive):
                      f"d={geom.d} x {args.layers} layers, {keep_txt}, "
                      f"inactive rows {list(inactive)}"),
         "keep_source": "gdn_accept_greedy" if acc else "drawn",
+        "output": "gated RMSNorm fused (gdn_conv_verify_gated)" if getattr(args, "gated", False) else "o",
         "B": geom.B, "T": geom.T, "H_k": geom.H_k, "H_v": geom.H_v, "d": geom.d,
         "layers": args.layers, "commit_mode": args.mode, "inactive_rows": list(inactive),
         "l2": f"no flush: state stack {args.layers * geom.B * geom.H_v * geom.d * geom.d * 4 / 2**20:.0f} MiB "
@@ -409,6 +412,9 @@ def run_gpu(args, rank, world, local):
     bs = [torch.from_numpy(c["beta"]).to(dev) for c in inp]
     states = [state[l] for l in range(n_layers)]
     rings = [ring[l] for l in range(n_layers)]
+    if args.gated:
+        zs = [bf(synth.normal_bf16(seed + 11, f"gate{p}", geom.B * geom.T * geom.H_v * geom.d)) for p in range(pool)]
+        norm_w = bf(synth.normal_bf16(seed, "norm_w", geom.d, std=0.5))
     if args.accept:
         lgs = [bf(bb) for bb in lg_bits]
         drafts = torch.from_numpy(drafts_np).to(dev)
@@ -418,8 +424,13 @@ def run_gpu(args, rank, world, local):
 
     def cycle(c, x, g, beta, keep, ev=None):
         for l in range(n_layers):
-            L.gdn_conv_verify(d, verify_mode(mode, l), x[l], conv_w[l], g[l], beta[l], state[l], ring[l],
-                              offsets, active, out[l], ws[l], ws_bytes)
+            if args.gated:
+                L.gdn_conv_verify_gated(d, verify_mode(mode, l), x[l], conv_w[l], g[l], beta[l], state[l], ring[l],
+                                        offsets, active, zs[c % pool].view(geom.B, geom.T, geom.H_v, geom.d), norm_w,
+                                        1e-6, out[l], ws[l], ws_bytes)
+            else:
+                L.gdn_conv_verify(d, verify_mode(mode, l), x[l], conv_w[l], g[l], beta[l], state[l], ring[l],
+                                  offsets, active, out[l], ws[l], ws_bytes)
         if args.accept:
             L.gdn_accept_greedy(lgs[c % pool], drafts[c], active, keep_dev, next_dev, ws_acc)
             keep = keep_dev

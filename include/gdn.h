@@ -140,6 +140,8 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
 #define GDN_STATUS_TIMEOUT 2u  /* a kernel gave up waiting for one of its own
                                   bulk copies (bounded wait); its outputs for
                                   that tile were not written */
+#define GDN_STATUS_BAD_ROW 4u  /* gdn_move_rows got a row index outside its
+                                  cohort; that pair was not copied */
 
 #define GDN_MAX_LAYERS 256     /* layers one gdn_commit call may group */
 
@@ -313,6 +315,30 @@ int gdn_conv_verify_noalloc(const gdn_dims *dims, int mode, const gdn_bf16 *x, c
  * device.  Returns GDN_OK or GDN_ERR_CUDA / GDN_ERR_INVALID_ARG.
  */
 int gdn_get_status(int clear, uint32_t *status);
+
+/* ---- joining rows into a cohort ------------------------------------------------
+ * Copy, for every layer, the decode state of row src_rows[i] of one cohort
+ * into row dst_rows[i] of another (or the same) cohort, i < n_rows: the fp32
+ * state, the whole conv cache row and the committed offset.  This is how a
+ * row primed by gdn_prefill_chunked (B = 1) joins a verify cohort ("Add
+ * request-owned eight-way MTP serving for Qwen 35B", sections 2 and 3: rows
+ * enter the eight-way cohort with their own committed offsets).
+ *  src_dims, dst_dims  equal H_k, H_v, d_k, T_max, width; B may differ
+ *  src_state, dst_state, src_ring, dst_ring  host arrays [n_layers] of device pointers
+ *  src_offsets, dst_offsets  [B] int32 device
+ *  dst_layer_ws  DEFERRED only: the destination cohort's layer workspaces; the
+ *                destination rows' pending keep is cleared.  The source must
+ *                have no commit pending (gdn_flush it first).
+ *  src_rows, dst_rows  [n_rows] int32 device; destination rows distinct, and
+ *                none of them a source row of another pair when the cohorts
+ *                share memory.  A pair with an index outside its cohort is
+ *                skipped and sets GDN_STATUS_BAD_ROW.
+ */
+int gdn_move_rows(const gdn_dims *src_dims, const gdn_dims *dst_dims, int mode, int n_layers,
+                  const float *const *src_state, const gdn_bf16 *const *src_ring, const int32_t *src_offsets,
+                  float *const *dst_state, gdn_bf16 *const *dst_ring, int32_t *dst_offsets,
+                  void *const *dst_layer_ws, const int32_t *src_rows, const int32_t *dst_rows, int n_rows,
+                  void *stream);
 
 /* ---- on-device greedy acceptance ---------------------------------------------
  * "Add request-owned eight-way MTP serving for Qwen 35B" takes the acceptance

@@ -342,6 +342,66 @@ __attribute__((visibility("default"))) int gdn_accept_greedy(int B, int T, int V
   return ok();
 }
 
+__attribute__((visibility("default"))) int gdn_move_rows(
+    const gdn_dims *src_dims, const gdn_dims *dst_dims, int mode, int n_layers, const float *const *src_state,
+    const gdn_bf16 *const *src_ring, const int32_t *src_offsets, float *const *dst_state, gdn_bf16 *const *dst_ring,
+    int32_t *dst_offsets, void *const *dst_layer_ws, const int32_t *src_rows, const int32_t *dst_rows, int n_rows,
+    void *stream) {
+  int rc = check_dims(src_dims);
+  if (rc) return rc;
+  if ((rc = check_dims(dst_dims))) return rc;
+  if ((rc = check_mode(mode))) return rc;
+  if (src_dims->H_k != dst_dims->H_k || src_dims->H_v != dst_dims->H_v || src_dims->d_k != dst_dims->d_k ||
+      src_dims->T_max != dst_dims->T_max || src_dims->width != dst_dims->width)
+    return fail(GDN_ERR_INVALID_ARG, "move_rows: the cohorts differ in heads, head size or T_max");
+  if (n_layers < 1 || n_layers > kMaxLayers)
+    return fail(GDN_ERR_INVALID_ARG, "n_layers=%d outside [1, %d]", n_layers, kMaxLayers);
+  if (n_rows < 0) return fail(GDN_ERR_INVALID_ARG, "n_rows=%d", n_rows);
+  if (!src_state || !src_ring || !dst_state || !dst_ring) return fail(GDN_ERR_INVALID_ARG, "NULL layer array");
+  if (mode == GDN_COMMIT_DEFERRED && !dst_layer_ws)
+    return fail(GDN_ERR_INVALID_ARG, "DEFERRED: the destination layer workspaces are needed");
+  if (n_rows == 0) return ok();
+  GDN_NEED_PTR(src_offsets, 16);
+  GDN_NEED_PTR(dst_offsets, 16);
+  GDN_NEED_PTR(src_rows, 16);
+  GDN_NEED_PTR(dst_rows, 16);
+  MoveParams p{};
+  for (int l = 0; l < n_layers; ++l) {
+    if (!src_state[l] || !src_ring[l] || !dst_state[l] || !dst_ring[l])
+      return fail(GDN_ERR_INVALID_ARG, "layer %d: NULL state or ring", l);
+    if (!aligned(src_state[l], 16) || !aligned(src_ring[l], 16) || !aligned(dst_state[l], 16) ||
+        !aligned(dst_ring[l], 16))
+      return fail(GDN_ERR_MISALIGNED, "layer %d: state or ring not 16-byte aligned", l);
+    p.src_state[l] = src_state[l];
+    p.src_ring[l] = reinterpret_cast<const uint16_t *>(src_ring[l]);
+    p.dst_state[l] = dst_state[l];
+    p.dst_ring[l] = reinterpret_cast<uint16_t *>(dst_ring[l]);
+    if (mode == GDN_COMMIT_DEFERRED) {
+      if (!dst_layer_ws[l] || !aligned(dst_layer_ws[l], 256))
+        return fail(GDN_ERR_MISALIGNED, "layer %d: NULL or misaligned destination workspace", l);
+      p.dst_ws[l] = dst_layer_ws[l];
+    }
+  }
+  const int C = (2 * src_dims->H_k + src_dims->H_v) * src_dims->d_k;
+  p.src_offsets = src_offsets;
+  p.dst_offsets = dst_offsets;
+  p.src_rows = src_rows;
+  p.dst_rows = dst_rows;
+  p.state_bytes = size_t(src_dims->H_v) * src_dims->d_v * src_dims->d_k * sizeof(float);
+  p.ring_bytes = size_t(kHist + src_dims->T_max) * C * sizeof(uint16_t);
+  p.pend_bytes = mode == GDN_COMMIT_DEFERRED ? size_t(dst_dims->H_v) * sizeof(int) : 0;
+  p.n_layers = n_layers;
+  p.n_rows = n_rows;
+  p.src_B = src_dims->B;
+  p.dst_B = dst_dims->B;
+  p.H_v = dst_dims->H_v;
+  p.status = status_word_address();
+  if (!p.status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = launch_move_rows(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_move_rows launch");
+  return ok();
+}
+
 // ---- verify without caller-provided workspace ---------------------------------
 // Scratch for gdn_conv_verify_noalloc: one layer's verify captures.  It lives
 // in the library's own device memory, so every GPU that loads the library

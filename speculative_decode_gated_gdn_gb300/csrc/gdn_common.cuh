@@ -410,6 +410,20 @@ cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g,
                            uint16_t *ring, int32_t *offsets, uint16_t *out, void *ws, int B, int L, int H_k,
                            int H_v, int D, int R, int act, cudaStream_t stream);
 uint32_t *status_word_address();  // device address of the sticky status word
+struct MoveParams {
+  const float *src_state[kMaxLayers];
+  const uint16_t *src_ring[kMaxLayers];
+  float *dst_state[kMaxLayers];
+  uint16_t *dst_ring[kMaxLayers];
+  void *dst_ws[kMaxLayers];     // DEFERRED: pending keep [B][H_v] at the start
+  const int32_t *src_offsets;
+  int32_t *dst_offsets;
+  const int32_t *src_rows, *dst_rows;
+  uint32_t *status;
+  size_t state_bytes, ring_bytes, pend_bytes;  // per row
+  int n_layers, n_rows, src_B, dst_B, H_v;
+};
+cudaError_t launch_move_rows(const MoveParams &p, cudaStream_t stream);
 constexpr int kMaxAcceptT = 64;   // positions per row the acceptance kernel handles
 size_t accept_workspace_bytes(int B, int T, int V);
 cudaError_t launch_accept(const uint16_t *logits, const int32_t *draft, const uint8_t *active, int32_t *keep,

@@ -28,13 +28,14 @@ GDN_COMMIT_DEFERRED = 2
 GDN_VERIFY_OVERLAP = 0x100
 GDN_STATUS_TIMEOUT = 2
 GDN_STATUS_BAD_KEEP = 1
+GDN_STATUS_BAD_ROW = 4
 GDN_MAX_LAYERS = 256
 GDN_NOALLOC_WS_BYTES = 4 << 20
 
 EXPORTS = ("gdn_version", "gdn_last_error", "gdn_layer_workspace_bytes", "gdn_conv_verify",
            "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status",
            "gdn_conv_verify_noalloc", "gdn_flush", "gdn_accept_workspace_bytes", "gdn_accept_greedy",
-           "gdn_conv_verify_gated")
+           "gdn_conv_verify_gated", "gdn_move_rows")
 
 
 class GdnError(RuntimeError):
@@ -86,6 +87,10 @@ def _declare(lib):
     lib.gdn_get_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)]
     lib.gdn_conv_verify_gated.restype = ctypes.c_int
     lib.gdn_conv_verify_gated.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_float, _P, _P, ctypes.c_size_t, _P]
+    PP = ctypes.POINTER(_P)
+    lib.gdn_move_rows.restype = ctypes.c_int
+    lib.gdn_move_rows.argtypes = [D, D, ctypes.c_int, ctypes.c_int, PP, PP, _P, PP, PP, _P, PP, _P, _P,
+                                  ctypes.c_int, _P]
     lib.gdn_accept_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_accept_workspace_bytes.argtypes = [ctypes.c_int] * 3
     lib.gdn_accept_greedy.restype = ctypes.c_int
@@ -253,6 +258,22 @@ def gdn_prefill_chunked(d: gdn_dims, L, x, conv_w, g, beta, state, ring, offsets
         _ptr(ring, "ring", torch.bfloat16), _ptr(offsets, "offsets", torch.int32),
         _ptr(out, "out", torch.bfloat16), _ptr(ws, "ws"), int(ws_bytes), _stream(stream))
     _check(rc, "gdn_prefill_chunked")
+
+
+def gdn_move_rows(src_d: gdn_dims, dst_d: gdn_dims, mode, src_states, src_rings, src_offsets, dst_states,
+                  dst_rings, dst_offsets, dst_layer_ws, src_rows, dst_rows, stream=None):
+    """Copy rows src_rows[i] of one cohort into rows dst_rows[i] of another,
+    every layer: state, conv cache and committed offset (device index arrays)."""
+    torch = _t()
+    n = len(src_states)
+    ws = None if dst_layer_ws is None else _layer_ptrs(dst_layer_ws, "dst_layer_ws")
+    rc = load().gdn_move_rows(
+        ctypes.byref(src_d), ctypes.byref(dst_d), mode, n, _layer_ptrs(src_states, "src_state", torch.float32),
+        _layer_ptrs(src_rings, "src_ring", torch.bfloat16), _ptr(src_offsets, "src_offsets", torch.int32),
+        _layer_ptrs(dst_states, "dst_state", torch.float32), _layer_ptrs(dst_rings, "dst_ring", torch.bfloat16),
+        _ptr(dst_offsets, "dst_offsets", torch.int32), ws, _ptr(src_rows, "src_rows", torch.int32),
+        _ptr(dst_rows, "dst_rows", torch.int32), int(src_rows.numel()), _stream(stream))
+    _check(rc, "gdn_move_rows")
 
 
 def gdn_accept_workspace_bytes(B: int, T: int, V: int) -> int:
