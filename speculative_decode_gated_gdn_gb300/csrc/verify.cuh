@@ -108,6 +108,11 @@ struct VerifySmem {
   float ce[T][D];
   float ck[T][D];
   float cG[kMaxT];
+  // T >= 4: the per-head scalars, computed once per CTA
+  float hraw[T * T + 2 * T];  // |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t) of the raw conv outputs
+  float cA[T][T];             // beta_t e^{G_t-G_s} (k^_s.k^_t), s < t: weight of e_s in e_t
+  float cQ[T][T];             // e^{G_t-G_s} (k^_s.q^_t), s <= t: weight of e_s in o_t
+  float cbk[T], cgq[T], cinvk[T], cGc[T];
   float gsq[T][8];  // gated RMSNorm: per-warp sums of o_t^2 (at most 8 warps)
   uint64_t bar[D / kTileRows];
   uint64_t cbar;
@@ -309,6 +314,10 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   }
 
   const bool qk_writer = (h % rep) == 0;  // one CTA per key head writes its q/k ring slots
+  // T >= 4: the per-head scalars are shared through shared memory and q, k
+  // are read from it per row group, instead of every lane reducing all
+  // T^2 + 2T of them and holding 2T vectors in registers
+  constexpr bool kSC = T >= 4;
   float q[T][4], k[T][4], vrow[NGRP][T];
   float gt[T], bt[T];
   {
@@ -367,12 +376,14 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
       write_back();
       applied = true;
     }
+    if constexpr (!kSC) {
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
-      const float4 kv = *reinterpret_cast<const float4 *>(&sm.k[t][4 * sub]);
-      q[t][0] = qv.x, q[t][1] = qv.y, q[t][2] = qv.z, q[t][3] = qv.w;
-      k[t][0] = kv.x, k[t][1] = kv.y, k[t][2] = kv.z, k[t][3] = kv.w;
+      for (int t = 0; t < T; ++t) {
+        const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[t][4 * sub]);
+        const float4 kv = *reinterpret_cast<const float4 *>(&sm.k[t][4 * sub]);
+        q[t][0] = qv.x, q[t][1] = qv.y, q[t][2] = qv.z, q[t][3] = qv.w;
+        k[t][0] = kv.x, k[t][1] = kv.y, k[t][2] = kv.z, k[t][3] = kv.w;
+      }
     }
   }
 
@@ -380,7 +391,60 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   float red_h[NV];
   float inv_q[T], inv_k[T], Gc[T], gam[T];
   float decay[T][T];  // exp(G_t - G_s), s < t
-  {
+  if constexpr (kSC) {
+    // ---- 3'. the T^2 + 2T dot products, spread over the warps ----------------
+    for (int n = warp; n < NV; n += NWARP) {
+      const float *u, *w;
+      if (n < 2 * T) {
+        u = w = (n & 1) ? sm.k[n >> 1] : sm.q[n >> 1];
+      } else if (n < 2 * T + NKK) {  // k_s . k_t, s < t, t-major
+        int r = n - 2 * T, t = 1;
+        while (r >= t) r -= t, ++t;
+        u = sm.k[r], w = sm.k[t];
+      } else {                        // k_s . q_t, s <= t, t-major
+        int r = n - 2 * T - NKK, t = 0;
+        while (r > t) r -= t + 1, ++t;
+        u = sm.k[r], w = sm.q[t];
+      }
+      float part = 0.f;
+      for (int i = 4 * lane; i < D; i += 128) {
+        const float4 a = *reinterpret_cast<const float4 *>(u + i), c = *reinterpret_cast<const float4 *>(w + i);
+        part += dot4(a, c);
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
+      if (lane == 0) sm.hraw[n] = part;
+    }
+    __syncthreads();
+    // ---- 4'. coefficients of the recurrence, one thread each -----------------
+    const float qs = 1.0f / sqrtf(float(D));
+    auto Gcum = [&](int t) {
+      float a = 0.f;
+      for (int u = 0; u <= t; ++u) a += gt[u];
+      return a;
+    };
+    for (int i = tid; i < T + T * T; i += NTHR) {  // (T + T^2 can exceed the CTA at d = 32)
+      if (i < T) {
+        const int t = i;
+        const float iq = rsqrtf(sm.hraw[2 * t] + kNormEps) * qs, ik = rsqrtf(sm.hraw[2 * t + 1] + kNormEps);
+        const float G = Gcum(t), gm = expf(G);
+        sm.cbk[t] = (bt[t] * gm) * ik;
+        sm.cgq[t] = gm * iq;
+        sm.cinvk[t] = ik;
+        sm.cGc[t] = G;
+        continue;
+      }
+      const int t = (i - T) / T, s0 = (i - T) % T;
+      if (s0 <= t) {
+        const float ik_s = rsqrtf(sm.hraw[2 * s0 + 1] + kNormEps), ik_t = rsqrtf(sm.hraw[2 * t + 1] + kNormEps);
+        const float iq_t = rsqrtf(sm.hraw[2 * t] + kNormEps) * qs;
+        const float dec = s0 == t ? 1.0f : expf(Gcum(t) - Gcum(s0));
+        if (s0 < t) sm.cA[t][s0] = bt[t] * dec * (sm.hraw[2 * T + t * (t - 1) / 2 + s0] * ik_s * ik_t);
+        sm.cQ[t][s0] = dec * (sm.hraw[2 * T + NKK + t * (t + 1) / 2 + s0] * ik_s * iq_t);
+      }
+    }
+    __syncthreads();
+  } else {
     int n = 0;
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -450,8 +514,13 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     float red[2 * T];
 #pragma unroll
     for (int mvec = 0; mvec < 2 * T; ++mvec) {
-      const float *vv = mvec < T ? k[mvec] : q[mvec - T];
-      const float4 vec = make_float4(vv[0], vv[1], vv[2], vv[3]);
+      float4 vec;
+      if constexpr (kSC) {
+        vec = *reinterpret_cast<const float4 *>(&(mvec < T ? sm.k[mvec] : sm.q[mvec - T])[4 * sub]);
+      } else {
+        const float *vv = mvec < T ? k[mvec] : q[mvec - T];
+        vec = make_float4(vv[0], vv[1], vv[2], vv[3]);
+      }
       float acc[RPL];
 #pragma unroll
       for (int i = 0; i < RPL; ++i) acc[i] = dot4(s[i], vec);
@@ -461,7 +530,19 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
 
     // scalar recurrence for the row this lane holds
     float e[T], o[T];
-    {
+    if constexpr (kSC) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        float acc = fmaf(bt[t], v[t], -sm.cbk[t] * red[t]);
+#pragma unroll
+        for (int s0 = 0; s0 < t; ++s0) acc = fmaf(-sm.cA[t][s0], e[s0], acc);
+        e[t] = acc;
+        float ot = sm.cgq[t] * red[T + t];
+#pragma unroll
+        for (int s0 = 0; s0 <= t; ++s0) ot = fmaf(sm.cQ[t][s0], e[s0], ot);
+        o[t] = ot;
+      }
+    } else {
       int nkk = 2 * T, nkq = 2 * T + NKK;
 #pragma unroll
       for (int t = 0; t < T; ++t) {
@@ -503,10 +584,18 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
         for (int t = 0; t < T; ++t) {
           const float et = __shfl_sync(0xffffffffu, e[t], src);
           const float a = expf(gt[t]);
-          st.x = fmaf(et, k[t][0] * inv_k[t], a * st.x);
-          st.y = fmaf(et, k[t][1] * inv_k[t], a * st.y);
-          st.z = fmaf(et, k[t][2] * inv_k[t], a * st.z);
-          st.w = fmaf(et, k[t][3] * inv_k[t], a * st.w);
+          float4 kh;
+          if constexpr (kSC) {
+            const float4 kr = *reinterpret_cast<const float4 *>(&sm.k[t][4 * sub]);
+            const float ik = sm.cinvk[t];
+            kh = make_float4(kr.x * ik, kr.y * ik, kr.z * ik, kr.w * ik);
+          } else {
+            kh = make_float4(k[t][0] * inv_k[t], k[t][1] * inv_k[t], k[t][2] * inv_k[t], k[t][3] * inv_k[t]);
+          }
+          st.x = fmaf(et, kh.x, a * st.x);
+          st.y = fmaf(et, kh.y, a * st.y);
+          st.z = fmaf(et, kh.z, a * st.z);
+          st.w = fmaf(et, kh.w, a * st.w);
           st_f4(snap + t * plane + size_t(grp + GPW * i) * D + 4 * sub, st);
         }
       }
@@ -561,13 +650,20 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     const size_t bk = MODE == GDN_COMMIT_DEFERRED ? bh : size_t(b) * H_k + hk;
     if ((MODE == GDN_COMMIT_DEFERRED || qk_writer) && warp == 0 && grp == 0)
 #pragma unroll
-      for (int t = 0; t < T; ++t)
-        st_f4(p.ws_k + (bk * T + t) * D + 4 * sub,
-              make_float4(k[t][0] * inv_k[t], k[t][1] * inv_k[t], k[t][2] * inv_k[t], k[t][3] * inv_k[t]));
+      for (int t = 0; t < T; ++t) {
+        if constexpr (kSC) {
+          const float4 kr = *reinterpret_cast<const float4 *>(&sm.k[t][4 * sub]);
+          const float ik = sm.cinvk[t];
+          st_f4(p.ws_k + (bk * T + t) * D + 4 * sub, make_float4(kr.x * ik, kr.y * ik, kr.z * ik, kr.w * ik));
+        } else {
+          st_f4(p.ws_k + (bk * T + t) * D + 4 * sub,
+                make_float4(k[t][0] * inv_k[t], k[t][1] * inv_k[t], k[t][2] * inv_k[t], k[t][3] * inv_k[t]));
+        }
+      }
     if (warp == 0 && lane < T) {
 #pragma unroll
       for (int t = 0; t < T; ++t)
-        if (lane == t) p.ws_G[bh * kMaxT + t] = Gc[t];
+        if (lane == t) p.ws_G[bh * kMaxT + t] = kSC ? sm.cGc[t] : Gc[t];
     }
   }
   if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
