@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
   constexpr int NW = D / 32;
   __shared__ float s_part[kChunk][NW];
   __shared__ float s_inv[kChunk];
+  __shared__ __align__(16) float s_y[kChunk][D + 4];  // q/k of the chunk, to store the [t][i] tile 16 bytes at a time
   pdl_wait();
   pdl_trigger();
   const int H_k = p.H_k, C = p.C, R = p.R, L = p.L;
@@ -236,10 +237,20 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
 #pragma unroll
   for (int i = 0; i < kChunk; ++i) y[i] *= s_inv[i];
   const size_t tbase = ((size_t(b) * H_k + hk) * p.NCp + chunk) * tile;
-  if (kind == 0)
-    store_tiles<D>(y, tid, p.qn_hi + tbase, p.qn_lo + tbase, nullptr, nullptr);
-  else
-    store_tiles<D>(y, tid, p.kn_hi + tbase, p.kn_lo + tbase, p.kt_hi + tbase, p.kt_lo + tbase);
+  // the [t][i] tile: a 16-byte run is 8 channels of one token, so the chunk
+  // goes through shared memory and every thread stores whole runs
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) s_y[i][tid] = y[i];
+  if (kind == 1) store_tiles<D>(y, tid, nullptr, nullptr, p.kt_hi + tbase, p.kt_lo + tbase);
+  __syncthreads();
+  {
+    uint16_t *nh = (kind == 0 ? p.qn_hi : p.kn_hi) + tbase, *nl = (kind == 0 ? p.qn_lo : p.kn_lo) + tbase;
+    for (int u = tid; u < kChunk * (D / 8); u += D) {
+      const int t = u / (D / 8), i8 = (u % (D / 8)) * 8;
+      const uint32_t o = canon_off(t, i8, D) / 2;
+      store8_split(&s_y[t][i8], nh + o, nl + o);
+    }
+  }
   if (state_pass_tc(D) || chunk >= p.NC) return;
   float *dst = (kind == 0 ? p.q : p.k) + ((size_t(b) * H_k + hk) * Lp + t0) * D + tid;
 #pragma unroll
