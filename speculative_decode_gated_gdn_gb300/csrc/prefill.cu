@@ -95,37 +95,6 @@ inline PrefillWs prefill_ws(int B, int L, int H_k, int H_v, int D) {
 }
 
 
-// Byte offset of element (row, k) in a K-major no-swizzle canonical tile whose
-// K extent is Kd bf16 elements: core matrix (row/8, k/8) at
-// (row/8) * (Kd/8)*128 + (k/8) * 128, then row%8 * 16 + k%8 * 2 inside it.
-__host__ __device__ constexpr uint32_t canon_off(int row, int k, int Kd) {
-  return uint32_t((row / 8) * (Kd / 8) * 128 + (k / 8) * 128 + (row % 8) * 16 + (k % 8) * 2);
-}
-
-__device__ __forceinline__ void split_bf16(float y, uint16_t &hi, uint16_t &lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(y);
-  hi = __bfloat16_as_ushort(h);
-  lo = __bfloat16_as_ushort(__float2bfloat16_rn(y - __bfloat162float(h)));
-}
-
-// Split 8 fp32 values into bf16 hi/lo (x_hi = bf16(x), x_lo = bf16(x - x_hi),
-// the same rounding as split_bf16, two values per conversion) and store them
-// as two 16-byte runs.
-__device__ __forceinline__ void store8_split(const float *v, uint16_t *hi, uint16_t *lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
-    h[q] = *reinterpret_cast<const uint32_t *>(&hv);
-    if (lo) {
-      const __nv_bfloat162 lv = __floats2bfloat162_rn(v[2 * q] - __low2float(hv), v[2 * q + 1] - __high2float(hv));
-      l[q] = *reinterpret_cast<const uint32_t *>(&lv);
-    }
-  }
-  *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-  if (lo) *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
 // Write one channel's 64 values into a natural tile ([t][i], K dim D) and,
 // when `transposed` is set, into a transposed tile ([i][t], K dim 64).
 template <int D>
@@ -315,9 +284,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
     for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
   pdl_wait();
   pdl_trigger();
+  // tensor memory is taken only after the wait: no CTA holds it while it
+  // waits for another grid, so an allocation never waits on a CTA that is
+  // itself waiting for the allocating grid
+  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
 
   const size_t tile_el = size_t(kChunk) * D;
   if (tid == 0) {
@@ -744,9 +716,12 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     fence_mbar_init();
     s_fail = 0;
   }
-  if (warp == 0) tmem_alloc(&s_tmem, kStCols);
   pdl_wait();
   pdl_trigger();
+  // tensor memory is taken only after the wait: no CTA holds it while it
+  // waits for another grid, so an allocation never waits on a CTA that is
+  // itself waiting for the allocating grid
+  if (warp == 0) tmem_alloc(&s_tmem, kStCols);
 
   auto load_wq = [&](int c) {
     const size_t wq = (bh * p.NCp + c) * (kChunk * D);

@@ -11,6 +11,14 @@
 // GDN_VERIFY_OVERLAP part of the next layer's CTAs fit beside it and stream
 // their state while this one computes.
 //
+// Deep drafts at d = 128 (T >= kTcMinT, RECOMPUTE and DEFERRED) take the
+// state dot products on the tensor cores instead: after the conv barrier the
+// staged fp32 state is split in place into bf16 hi/lo operand tiles, one
+// thread issues the products into TMEM, and thread i < d reads the 2T dot
+// products of state row i from TMEM lane i and runs the row's recurrence.
+// The fixed cost of the split and the products (about 2 us per CTA) beats
+// the SIMT row loop, whose shuffles and registers grow with T, from T = 5 on.
+//
 // The pre-verification state S_0 is only read ("MTP inference: review and
 // commit structure", Functional commits item 2: speculative transactions with
 // verifier buffers; "Add request-owned eight-way MTP serving for Qwen 35B",
@@ -97,12 +105,45 @@ __device__ __forceinline__ void conv_store_ring(const VerifyParams &p, int b, in
   for (int t = 0; t < T; ++t) ringb[size_t(kNewSlot + t) * p.C] = in.x[t];
 }
 
+// Tensor-core dot products (d = 128, T >= kTcMinT, not SNAPSHOT): the 2T
+// dot products of every state row with the raw k_t and q_t are one
+// 128 x 16 x 128 product, D[i][n] = sum_j S_0[i][j] B[n][j] with B's rows
+// k_0..k_{T-1}, q_0..q_{T-1} and zero rows up to kTcN, taken in bf16 pieces
+// as S_hi [B_hi; B_lo]^T (N = 32, TMEM columns 0..31) and S_lo B_hi^T
+// (N = 16, columns 32..47), summed per row afterwards; the SIMT row loop and
+// its butterflies are gone.
+constexpr int kTcMinT = 5;
+constexpr int kTcN = 2 * kMaxT;   // the 2T vectors, zero-padded
+constexpr int kTcCols = 64;       // TMEM columns allocated (48 used)
+
+// Split 8 fp32 values by truncation: x_hi = the upper 16 bits of x (a bf16),
+// x_lo = the upper 16 bits of x - x_hi (exact in fp32), so that
+// |x - x_hi - x_lo| < 2^-14 |x|; byte permutes and one subtraction per
+// value, no conversion instructions.  Stored as two 16-byte runs.
+__device__ __forceinline__ void store8_split_trunc(const float *v, uint16_t *hi, uint16_t *lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t a = __float_as_uint(v[2 * q]), c = __float_as_uint(v[2 * q + 1]);
+    h[q] = __byte_perm(a, c, 0x7632);
+    const float ra = v[2 * q] - __uint_as_float(a & 0xffff0000u);
+    const float rc = v[2 * q + 1] - __uint_as_float(c & 0xffff0000u);
+    l[q] = __byte_perm(__float_as_uint(ra), __float_as_uint(rc), 0x7632);
+  }
+  *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 // Shared memory of one verify CTA: the (row, head) state tile, the conv
 // outputs of its key head and, in DEFERRED mode, the captures of the previous
 // verify (e_t, normalised k_t, G_t) for the commit that may still be pending.
 template <int D, int T>
 struct VerifySmem {
-  float S[D * D];
+  static constexpr bool kTc = D == 128 && T >= kTcMinT;
+  // fp32 state; on the tensor-core path, once every thread holds its part in
+  // registers, the same bytes take the bf16 hi and lo A tiles (K-major,
+  // no-swizzle canonical layout, 32 KiB each)
+  alignas(128) float S[D * D];
   float q[T][D];
   float k[T][D];
   float ce[T][D];
@@ -114,26 +155,32 @@ struct VerifySmem {
   float cQ[T][T];             // e^{G_t-G_s} (k^_s.q^_t), s <= t: weight of e_s in o_t
   float cbk[T], cgq[T], cinvk[T], cGc[T];
   float gsq[T][8];  // gated RMSNorm: per-warp sums of o_t^2 (at most 8 warps)
+  alignas(128) uint16_t bqk[kTc ? 2 * kTcN * D : 8];  // tensor-core B operand: hi tile, then lo tile
   uint64_t bar[D / kTileRows];
   uint64_t cbar;
+  uint64_t mbar;  // tensor-core products done
+  uint32_t tmem;  // TMEM accumulator address
 };
 
 // Threads per verify CTA: 2d (8 warps at d = 128, 16 state rows per warp).
 // Measured at B = 8, T = 2: d threads (3 CTAs per SM, 32 rows per warp) make
 // a layer about 1 us slower, the longer per-warp row loop costing more than
 // the deeper residency gains.
-template <int D, int T>
+// Two CTAs per SM for T <= 4 and on the tensor-core path; the SIMT path at
+// T > 4 needs more registers than that leaves (spills measured).
+template <int D, int T, int MODE>
 struct VerifyShape {
+  static constexpr bool kTc = VerifySmem<D, T>::kTc && MODE != GDN_COMMIT_SNAPSHOT;
   static constexpr int kThreads = 2 * D;
-  static constexpr int kMinBlocks = T <= 4 ? 2 : 1;
+  static constexpr int kMinBlocks = (T <= 4 || kTc) ? 2 : 1;
 };
 
 template <int D, int T, int MODE>
-__global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>::kMinBlocks)
+__global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape<D, T, MODE>::kMinBlocks)
     verify_kernel(const VerifyParams p) {
   using G = RowLanes<D>;
   constexpr int RPL = G::RPL, GPW = G::GPW, LPR = G::LPR;
-  constexpr int NTHR = VerifyShape<D, T>::kThreads, NWARP = NTHR / 32;
+  constexpr int NTHR = VerifyShape<D, T, MODE>::kThreads, NWARP = NTHR / 32;
   constexpr int ROWS_W = D / NWARP;   // state rows per warp, in groups of 8
   constexpr int NGRP = ROWS_W / 8;
   static_assert(ROWS_W % 8 == 0 && NWARP * ROWS_W == D, "rows must split evenly over warps");
@@ -141,6 +188,9 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   constexpr int NT = D / kTileRows;   // 32-row tiles, one bulk copy and barrier each
   // per-head reductions: |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t)
   constexpr int NKK = T * (T - 1) / 2, NKQ = T * (T + 1) / 2, NV = 2 * T + NKK + NKQ;
+  constexpr bool kTC = VerifyShape<D, T, MODE>::kTc;
+  static_assert(!kTC || (T >= 4 && 2 * T <= kTcN && NTHR == kTcN * D / 8 && NWARP == 8),
+                "tensor-core path: one B-tile chunk per thread, 16 rows per warp");
 
   extern __shared__ __align__(128) unsigned char vsm_raw[];
   VerifySmem<D, T> &sm = *reinterpret_cast<VerifySmem<D, T> *>(vsm_raw);
@@ -195,6 +245,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
 #pragma unroll
     for (int i = 0; i < NT; ++i) mbar_init(&sm.bar[i], 1);
     mbar_init(&sm.cbar, 1);
+    if (kTC) mbar_init(&sm.mbar, 1);
     fence_mbar_init();
   }
   if (active) stage_state();
@@ -325,15 +376,20 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     // the CTA) and the v channels of the rows this lane will hold; every load
     // is issued before the first use
     constexpr int NQK = (2 * D + NTHR - 1) / NTHR;
-    ConvIn<T> inqk[NQK], inv[NGRP];
+    // (tensor-core path: thread i < d takes the v channel of state row i)
+    ConvIn<T> inqk[NQK], inv[kTC ? 1 : NGRP];
 #pragma unroll
     for (int r = 0; r < NQK; ++r) {
       const int c2 = tid + r * NTHR;
       if (c2 < 2 * D) conv_load<T>(p, b, (c2 >= D ? H_k * D + c2 - D : c2) + hk * D, inqk[r]);
     }
+    if constexpr (kTC) {
+      if (tid < D) conv_load<T>(p, b, 2 * H_k * D + h * D + tid, inv[0]);
+    } else {
 #pragma unroll
-    for (int grp8 = 0; grp8 < NGRP; ++grp8)
-      conv_load<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
+      for (int grp8 = 0; grp8 < NGRP; ++grp8)
+        conv_load<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
+    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
@@ -353,8 +409,12 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
         for (int t = 0; t < T; ++t) (c2 >= D ? sm.k : sm.q)[t][c2 >= D ? c2 - D : c2] = y[t];
       }
     }
+    if constexpr (kTC) {
+      if (tid < D) conv_eval<T>(inv[0], p.act, vrow[0]);
+    } else {
 #pragma unroll
-    for (int grp8 = 0; grp8 < NGRP; ++grp8) conv_eval<T>(inv[grp8], p.act, vrow[grp8]);
+      for (int grp8 = 0; grp8 < NGRP; ++grp8) conv_eval<T>(inv[grp8], p.act, vrow[grp8]);
+    }
     // new raw inputs into the ring: q/k channels by one CTA of the key head,
     // v channels by one lane of the four sharing a row
 #pragma unroll
@@ -362,10 +422,13 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
       const int c2 = tid + r * NTHR;
       if (qk_writer && c2 < 2 * D) conv_store_ring<T>(p, b, (c2 >= D ? H_k * D + c2 - D : c2) + hk * D, inqk[r]);
     }
-    if (leader)
+    if constexpr (kTC) {
+      if (tid < D) conv_store_ring<T>(p, b, 2 * H_k * D + h * D + tid, inv[0]);
+    } else if (leader) {
 #pragma unroll
       for (int grp8 = 0; grp8 < NGRP; ++grp8)
         conv_store_ring<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
+    }
     // conv outputs (and applied state rows) are visible; a timed-out staged
     // copy stops the CTA here, where no thread has left yet
     if (__syncthreads_or(failed)) {
@@ -391,54 +454,131 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   float red_h[NV];
   float inv_q[T], inv_k[T], Gc[T], gam[T];
   float decay[T][T];  // exp(G_t - G_s), s < t
+  // tensor-core path: thread (warp w, lane l) converts 64 state values of row
+  // i = 16w + 8(l/16) + l % 8, columns [64 hf, +64) with hf = (l/8) % 2,
+  // one 8-column chunk per step, starting at chunk (l % 8) so that the eight
+  // lanes of a quarter-warp read distinct banks and, holding distinct i % 8,
+  // write distinct banks of the canonical tile; fsw swaps the two 16-byte
+  // halves of a chunk for the upper four lanes of each eight
+  const int tc_r = lane & 7, tc_q = warp * 4 + (lane >> 3);
+  const int tc_i = (tc_q >> 1) * 8 + tc_r, tc_hf = tc_q & 1, tc_fsw = (tc_r >> 2) & 1;
   if constexpr (kSC) {
-    // ---- 3'. the T^2 + 2T dot products, spread over the warps ----------------
-    for (int n = warp; n < NV; n += NWARP) {
-      const float *u, *w;
+    float4 sv[kTC ? 16 : 1];
+    if constexpr (kTC) {
+      // the B operand: row n < T is the raw k_n, T <= n < 2T the raw q_{n-T},
+      // the rest zero; one 8-element chunk per thread
+      const int n = tid >> 4, c8 = 8 * (tid & 15);
+      float bv[8];
       if (n < 2 * T) {
-        u = w = (n & 1) ? sm.k[n >> 1] : sm.q[n >> 1];
-      } else if (n < 2 * T + NKK) {  // k_s . k_t, s < t, t-major
-        int r = n - 2 * T, t = 1;
-        while (r >= t) r -= t, ++t;
-        u = sm.k[r], w = sm.k[t];
-      } else {                        // k_s . q_t, s <= t, t-major
-        int r = n - 2 * T - NKK, t = 0;
-        while (r > t) r -= t + 1, ++t;
-        u = sm.k[r], w = sm.q[t];
-      }
-      float part = 0.f;
-      for (int i = 4 * lane; i < D; i += 128) {
-        const float4 a = *reinterpret_cast<const float4 *>(u + i), c = *reinterpret_cast<const float4 *>(w + i);
-        part += dot4(a, c);
-      }
+        const float *src = (n < T ? sm.k[n] : sm.q[n - T]) + c8;
+        const float4 lo4 = *reinterpret_cast<const float4 *>(src), hi4 = *reinterpret_cast<const float4 *>(src + 4);
+        bv[0] = lo4.x, bv[1] = lo4.y, bv[2] = lo4.z, bv[3] = lo4.w;
+        bv[4] = hi4.x, bv[5] = hi4.y, bv[6] = hi4.z, bv[7] = hi4.w;
+      } else {
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
-      if (lane == 0) sm.hraw[n] = part;
+        for (int u = 0; u < 8; ++u) bv[u] = 0.f;
+      }
+      const uint32_t o = canon_off(n, c8, D) / 2;
+      store8_split(bv, sm.bqk + o, sm.bqk + kTcN * D + o);
+      // the accumulators; taken only now, after the PDL wait (no CTA holds
+      // tensor memory while it waits for another grid), by the last warp,
+      // which has no rows, so that its release overlaps the captures
+      if (warp == NWARP - 1) tmem_alloc(&sm.tmem, kTcCols);
     }
-    __syncthreads();
+    // ---- 3'. the T^2 + 2T dot products, four lanes each ----------------------
+    // Lane l of quad qd sums float4 columns l, l+4, ... of its pair, starting
+    // 4*qd columns in, so the two quads of a quarter-warp read different banks.
+    constexpr int NQ4 = NTHR / 4, F4 = D / 4;
+    {
+      const int qd = tid >> 2, ql = tid & 3;
+      for (int r0 = 0; r0 < NV; r0 += NQ4) {  // the same trip count in every lane
+        const int n = r0 + qd;
+        float part = 0.f;
+        if (n < NV) {
+          const float *u, *w;
+          if (n < 2 * T) {
+            u = w = (n & 1) ? sm.k[n >> 1] : sm.q[n >> 1];
+          } else if (n < 2 * T + NKK) {  // k_s . k_t, s < t, t-major
+            int r = n - 2 * T, t = 1;
+            while (r >= t) r -= t, ++t;
+            u = sm.k[r], w = sm.k[t];
+          } else {                        // k_s . q_t, s <= t, t-major
+            int r = n - 2 * T - NKK, t = 0;
+            while (r > t) r -= t + 1, ++t;
+            u = sm.k[r], w = sm.q[t];
+          }
+#pragma unroll
+          for (int j = 0; j < F4 / 4; ++j) {
+            const int f = (ql + 4 * (j + qd)) % F4;
+            part += dot4(*reinterpret_cast<const float4 *>(u + 4 * f), *reinterpret_cast<const float4 *>(w + 4 * f));
+          }
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (n < NV && ql == 0) sm.hraw[n] = part;
+      }
+      // cumulative log-decay G_t = g_0 + ... + g_t, in order
+      if (tid < T) {
+        float a = 0.f;
+#pragma unroll
+        for (int u = 0; u < T; ++u)
+          if (u <= tid) a += gt[u];
+        sm.cGc[tid] = a;
+      }
+    }
+    if constexpr (kTC) {
+      // this thread's 64 state values into registers (the warp's rows arrive
+      // with one bulk copy); the A tiles overwrite them after the barrier, so
+      // the write-back copy of an applied commit must have read them too
+      const bool late = !mbar_wait_bounded(&sm.bar[(16 * warp) / kTileRows], 0);
+      if (!late) {
+        const float *row = sm.S + tc_i * D + 64 * tc_hf;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = (j + tc_r) & 7;
+          sv[2 * j] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 * tc_fsw);
+          sv[2 * j + 1] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 - 4 * tc_fsw);
+        }
+      }
+      if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
+      tc_fence_before();
+      const bool failed = __syncthreads_or(late);
+      tc_fence_after();
+      if (failed) {
+        if (warp == NWARP - 1) tmem_dealloc(sm.tmem, kTcCols);
+        give_up();
+        return;
+      }
+      uint16_t *ahi = reinterpret_cast<uint16_t *>(sm.S), *alo = ahi + D * D;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = 8 * tc_hf + ((j + tc_r) & 7);
+        const float4 a = tc_fsw ? sv[2 * j + 1] : sv[2 * j], z = tc_fsw ? sv[2 * j] : sv[2 * j + 1];
+        const float v8[8] = {a.x, a.y, a.z, a.w, z.x, z.y, z.z, z.w};
+        const uint32_t o = canon_off(tc_i, 8 * c, D) / 2;
+        store8_split_trunc(v8, ahi + o, alo + o);
+      }
+      fence_async_smem();  // the tiles (and the B operand) are read by the tensor cores
+    } else {
+      __syncthreads();
+    }
     // ---- 4'. coefficients of the recurrence, one thread each -----------------
     const float qs = 1.0f / sqrtf(float(D));
-    auto Gcum = [&](int t) {
-      float a = 0.f;
-      for (int u = 0; u <= t; ++u) a += gt[u];
-      return a;
-    };
     for (int i = tid; i < T + T * T; i += NTHR) {  // (T + T^2 can exceed the CTA at d = 32)
       if (i < T) {
         const int t = i;
         const float iq = rsqrtf(sm.hraw[2 * t] + kNormEps) * qs, ik = rsqrtf(sm.hraw[2 * t + 1] + kNormEps);
-        const float G = Gcum(t), gm = expf(G);
+        const float gm = expf(sm.cGc[t]);
         sm.cbk[t] = (bt[t] * gm) * ik;
         sm.cgq[t] = gm * iq;
         sm.cinvk[t] = ik;
-        sm.cGc[t] = G;
         continue;
       }
       const int t = (i - T) / T, s0 = (i - T) % T;
       if (s0 <= t) {
         const float ik_s = rsqrtf(sm.hraw[2 * s0 + 1] + kNormEps), ik_t = rsqrtf(sm.hraw[2 * t + 1] + kNormEps);
         const float iq_t = rsqrtf(sm.hraw[2 * t] + kNormEps) * qs;
-        const float dec = s0 == t ? 1.0f : expf(Gcum(t) - Gcum(s0));
+        const float dec = s0 == t ? 1.0f : expf(sm.cGc[t] - sm.cGc[s0]);
         if (s0 < t) sm.cA[t][s0] = bt[t] * dec * (sm.hraw[2 * T + t * (t - 1) / 2 + s0] * ik_s * ik_t);
         sm.cQ[t][s0] = dec * (sm.hraw[2 * T + NKK + t * (t + 1) / 2 + s0] * ik_s * iq_t);
       }
@@ -487,6 +627,95 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
   // and in DEFERRED mode already brought up to date) -------------------------
   const size_t plane = size_t(p.B) * H_v * D * D;
   const bool gated = p.gz != nullptr;
+  if constexpr (kTC) {
+    // ---- 5''. one thread issues the products; thread i < d then runs the
+    // recurrence of state row i from its 2T dot products in TMEM lane i ------
+    const uint32_t tmem = sm.tmem;
+    if (tid == 0) {
+      tc_fence_after();
+      // B_hi (rows 0..15) and B_lo (rows 16..31) form one 32-row tile
+      const uint32_t aH = smem_u32(sm.S), aL = aH + D * D * 2, bH = smem_u32(sm.bqk);
+      constexpr uint32_t idesc32 = umma_idesc_bf16(D, 2 * kTcN), idesc16 = umma_idesc_bf16(D, kTcN);
+      constexpr uint32_t sbo = (D / 8) * 128;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        umma_bf16(tmem, umma_desc(aH + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo), idesc32, kk > 0);
+        umma_bf16(tmem + 2 * kTcN, umma_desc(aL + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo), idesc16,
+                  kk > 0);
+      }
+      umma_commit(&sm.mbar);
+    }
+    const bool rower = tid < D;  // warps 0..3: TMEM lanes 32w..32w+31
+    const int i = tid;
+    float o[T], e[T];
+    uint16_t zt[T], wi = 0;
+    bool late = false;
+    if (rower) {
+      if (gated) {
+        wi = p.gw[i];
+#pragma unroll
+        for (int t = 0; t < T; ++t) zt[t] = p.gz[((size_t(b) * T + t) * H_v + h) * D + i];
+      }
+      late = __any_sync(0xffffffffu, !mbar_wait_bounded(&sm.mbar, 0));
+      tc_fence_after();
+      if (!late) {
+        float d01[2 * kTcN], d2[kTcN], red[kTcN];
+        tmem_ld32(tmem + (uint32_t(32 * warp) << 16), d01);
+        tmem_ld16(tmem + (uint32_t(32 * warp) << 16) + 2 * kTcN, d2);
+#pragma unroll
+        for (int n = 0; n < kTcN; ++n) red[n] = (d01[n] + d01[kTcN + n]) + d2[n];
+        const float *v = vrow[0];
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          float acc = fmaf(bt[t], v[t], -sm.cbk[t] * red[t]);
+#pragma unroll
+          for (int s0 = 0; s0 < t; ++s0) acc = fmaf(-sm.cA[t][s0], e[s0], acc);
+          e[t] = acc;
+          float ot = sm.cgq[t] * red[T + t];
+#pragma unroll
+          for (int s0 = 0; s0 <= t; ++s0) ot = fmaf(sm.cQ[t][s0], e[s0], ot);
+          o[t] = ot;
+        }
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          if (!gated) p.out[((size_t(b) * T + t) * H_v + h) * D + i] = f2bf(o[t]);
+          p.ws_e[(bh * T + t) * D + i] = e[t];
+        }
+        if (gated) {
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            float q2 = o[t] * o[t];
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, m);
+            if (lane == 0) sm.gsq[t][warp] = q2;
+          }
+        }
+      }
+    }
+    // every TMEM read is done before the accumulator is released
+    tc_fence_before();
+    const bool failed = __syncthreads_or(late);
+    tc_fence_after();
+    if (warp == NWARP - 1) {
+      if (failed) mbar_wait_bounded(&sm.mbar, 0);  // one more bounded wait for the products
+      tmem_dealloc(tmem, kTcCols);
+    }
+    if (failed) {
+      give_up();
+      return;
+    }
+    if (gated && rower) {
+      // out = o_t / sqrt(mean_i o_t[i]^2 + eps) * w[i] * silu(z_t[i])
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        float ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < D / 32; ++w) ss += sm.gsq[t][w];
+        const float rstd = rsqrtf(ss / float(D) + p.geps);
+        p.out[((size_t(b) * T + t) * H_v + h) * D + i] = f2bf(o[t] * rstd * bf2f(wi) * silu_fast(bf2f(zt[t])));
+      }
+    }
+  } else {
   float og[NGRP][T];           // gated: o of the rows this lane leads, until the norm is known
   uint16_t zg[NGRP][T], wg[NGRP];
   if (gated && leader) {       // the gate and weight of those rows, loaded now
@@ -640,6 +869,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
     give_up();
     return;
   }
+  }  // SIMT row loop
   // every warp applied its rows before the conv barrier
   if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) p.ws_pend[bh] = 0;  // (a repeat if applied before the wait)
 
@@ -673,7 +903,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T>::kThreads, VerifyShape<D, T>
 // the first launch of that instantiation on each device.
 template <int D, int T, int MODE>
 cudaError_t launch_verify_kernel(dim3 grid, cudaStream_t stream, const VerifyParams &p) {
-  const dim3 block(VerifyShape<D, T>::kThreads);
+  const dim3 block(VerifyShape<D, T, MODE>::kThreads);
   static bool configured[64] = {false};  // one flag set per instantiation
   constexpr int smem = int(sizeof(VerifySmem<D, T>));
   int dev = 0;

@@ -75,7 +75,7 @@ def test_cohort_b8_t2(gdn, mode):
 SWEEP = [  # (B, T, T_max, H_k, H_v, d)
     (3, 1, 1, 2, 4, 32), (2, 3, 4, 1, 3, 32), (4, 4, 4, 2, 2, 64), (3, 5, 8, 2, 6, 64),
     (2, 6, 6, 1, 2, 128), (2, 7, 8, 2, 4, 128), (3, 8, 8, 2, 4, 128), (5, 2, 3, 3, 6, 128),
-    (2, 8, 8, 4, 4, 32),
+    (2, 8, 8, 4, 4, 32), (3, 4, 4, 2, 4, 128), (2, 5, 8, 1, 4, 128),
 ]
 
 
@@ -87,6 +87,16 @@ def test_shape_sweep(gdn, shape, mode):
     active = synth.active_mask(B, (B - 1,) if B > 2 else ())
     keeps = [[(b + c) % (T + 1) for b in range(B)] for c in range(4)]
     run_cycles(geom, 10 + T, active, mode, 2, 4, keeps, flush_every=2)
+
+
+@pytest.mark.parametrize("mode", [L.GDN_COMMIT_RECOMPUTE, L.GDN_COMMIT_DEFERRED], ids=["recompute", "deferred"])
+def test_deep_draft_cohort_b8_t8(gdn, mode):
+    """The deep-draft cohort at full head count (B = 8, T = 8, H_v = 32,
+    d = 128: the tensor-core dot products), two layers over three cycles
+    with rows 6 and 7 inactive, keeps from 0 to 8."""
+    geom = synth.Geometry(B=8, T=8, H_k=16, H_v=32, d=128)
+    keeps = [[8, 0, 3, 5, 1, 8, 2, 7], [2, 8, 0, 6, 4, 1, 8, 8], [5, 5, 8, 0, 7, 3, 0, 1]]
+    run_cycles(geom, 41, synth.active_mask(8, (6, 7)), mode, 2, 3, keeps)
 
 
 def test_no_activation(gdn):
@@ -317,18 +327,22 @@ def _cycle_runs(geom, st, masks, keeps, n_layers, mode, overlap_all=False, repea
     return outs, gpu.state.clone(), host_bits(gpu.ring), gpu.offsets.clone()
 
 
+@pytest.mark.parametrize("T", [3, 8], ids=["T3", "T8"])
 @pytest.mark.parametrize("repeat_verify", [False, True], ids=["once", "repeated"])
-def test_deferred_bit_identical_to_recompute(gdn, repeat_verify):
+def test_deferred_bit_identical_to_recompute(gdn, repeat_verify, T):
     """DEFERRED applies a commit inside the next verify with the arithmetic of
     the eager commit: every output, and the flushed state, equals RECOMPUTE bit
     for bit.  Rows switch between active and inactive with commits pending, and
     every layer's verify after the first is flagged GDN_VERIFY_OVERLAP in
     DEFERRED mode, so those apply their pending commit before the PDL wait."""
-    geom = synth.Geometry(B=4, T=3, H_k=2, H_v=4, d=128, T_max=4)
+    geom = synth.Geometry(B=4, T=T, H_k=2, H_v=4, d=128, T_max=max(T, 4))
     st = synth.layer_state(geom, 30, 3)
     masks = [synth.active_mask(4), synth.active_mask(4, (1,)), synth.active_mask(4, (1,)),
              synth.active_mask(4, (1, 2)), synth.active_mask(4, (3,)), synth.active_mask(4)]
-    keeps = [[3, 2, 1, 0], [1, 3, 3, 2], [2, 0, 3, 1], [0, 1, 2, 3], [2, 2, 0, 3], [3, 0, 1, 1]]
+    keeps = [[min(k, T) for k in row] for row in
+             [[3, 2, 1, 0], [1, 3, 3, 2], [2, 0, 3, 1], [0, 1, 2, 3], [2, 2, 0, 3], [3, 0, 1, 1]]]
+    if T == 8:  # deep keeps as well
+        keeps[1], keeps[4] = [8, 5, 7, 0], [6, 8, 0, 4]
     ref = _cycle_runs(geom, st, masks, keeps, 3, L.GDN_COMMIT_RECOMPUTE, repeat_verify=repeat_verify)
     dfr = _cycle_runs(geom, st, masks, keeps, 3, L.GDN_COMMIT_DEFERRED, overlap_all=True,
                       repeat_verify=repeat_verify)
