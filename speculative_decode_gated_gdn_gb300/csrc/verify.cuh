@@ -466,8 +466,10 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
     float4 sv[kTC ? 16 : 1];
     if constexpr (kTC) {
       // the B operand: row n < T is the raw k_n, T <= n < 2T the raw q_{n-T},
-      // the rest zero; one 8-element chunk per thread
-      const int n = tid >> 4, c8 = 8 * (tid & 15);
+      // the rest zero; one 8-element chunk per thread.  A quarter-warp holds
+      // eight rows, distinct mod 8, so its stores hit eight bank groups; the
+      // chunk is rotated by the row so its loads spread over the banks too.
+      const int n = tid & 15, c8 = 8 * (((tid >> 4) + n) & 15);
       float bv[8];
       if (n < 2 * T) {
         const float *src = (n < T ? sm.k[n] : sm.q[n - T]) + c8;
