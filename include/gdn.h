@@ -75,6 +75,13 @@
  * Value head h reads key head floor(h * H_k / H_v).
  * Supported: d_k == d_v in {32, 64, 128}; width == 4; 1 <= T <= T_max <= 8;
  * H_v % H_k == 0; B <= 65535; H_v <= 65535.
+ *
+ * Numerics: the state and all arithmetic are fp32; bf16 appears only in the
+ * inputs and outputs.  At d = 128 with T >= 5 (RECOMPUTE and DEFERRED) the
+ * verify takes the dot products of the state rows with q_t and k_t on the
+ * tensor cores, from bf16 hi/lo splits of both operands (about 2^-14 of each
+ * term's magnitude); its results differ from the CUDA-core path's only by
+ * rounding.
  */
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
