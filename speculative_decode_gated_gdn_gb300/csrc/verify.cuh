@@ -463,8 +463,8 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
   const int tc_r = lane & 7, tc_q = warp * 4 + (lane >> 3);
   const int tc_i = (tc_q >> 1) * 8 + tc_r, tc_hf = tc_q & 1, tc_fsw = (tc_r >> 2) & 1;
   if constexpr (kSC) {
-    float4 sv[kTC ? 16 : 1];
     if constexpr (kTC) {
+      float4 sv[16];
       // the B operand: row n < T is the raw k_n, T <= n < 2T the raw q_{n-T},
       // the rest zero; one 8-element chunk per thread.  A quarter-warp holds
       // eight rows, distinct mod 8, so its stores hit eight bank groups; the
@@ -484,8 +484,58 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
       store8_split(bv, sm.bqk + o, sm.bqk + kTcN * D + o);
       // the accumulators; taken only now, after the PDL wait (no CTA holds
       // tensor memory while it waits for another grid), by the last warp,
-      // which has no rows, so that its release overlaps the captures
+      // which has no rows and no captures to write
       if (warp == NWARP - 1) tmem_alloc(&sm.tmem, kTcCols);
+      // this thread's 64 state values into registers (the warp's rows arrive
+      // with one bulk copy); the A tiles overwrite them after the barrier, so
+      // the write-back copy of an applied commit must have read them too
+      const bool late = !mbar_wait_bounded(&sm.bar[(16 * warp) / kTileRows], 0);
+      if (!late) {
+        const float *row = sm.S + tc_i * D + 64 * tc_hf;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = (j + tc_r) & 7;
+          sv[2 * j] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 * tc_fsw);
+          sv[2 * j + 1] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 - 4 * tc_fsw);
+        }
+      }
+      if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
+      tc_fence_before();
+      const bool failed = __syncthreads_or(late);
+      tc_fence_after();
+      if (failed) {
+        if (warp == NWARP - 1) tmem_dealloc(sm.tmem, kTcCols);
+        give_up();
+        return;
+      }
+      uint16_t *ahi = reinterpret_cast<uint16_t *>(sm.S), *alo = ahi + D * D;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = 8 * tc_hf + ((j + tc_r) & 7);
+        const float4 a = tc_fsw ? sv[2 * j + 1] : sv[2 * j], z = tc_fsw ? sv[2 * j] : sv[2 * j + 1];
+        const float v8[8] = {a.x, a.y, a.z, a.w, z.x, z.y, z.z, z.w};
+        const uint32_t o = canon_off(tc_i, 8 * c, D) / 2;
+        store8_split_trunc(v8, ahi + o, alo + o);
+      }
+      fence_async_smem();  // the tiles (and the B operand) are read by the tensor cores
+      __syncthreads();  // the A and B tiles are complete
+      // the products start now and run while the CTA computes the per-head
+      // dot products and coefficients below
+      if (tid == 0) {
+        tc_fence_after();
+        // B_hi (rows 0..15) and B_lo (rows 16..31) form one 32-row tile
+        const uint32_t tmem = sm.tmem;
+        const uint32_t aH = smem_u32(sm.S), aL = aH + D * D * 2, bH = smem_u32(sm.bqk);
+        constexpr uint32_t idesc32 = umma_idesc_bf16(D, 2 * kTcN), idesc16 = umma_idesc_bf16(D, kTcN);
+        constexpr uint32_t sbo = (D / 8) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          umma_bf16(tmem, umma_desc(aH + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo), idesc32, kk > 0);
+          umma_bf16(tmem + 2 * kTcN, umma_desc(aL + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo),
+                    idesc16, kk > 0);
+        }
+        umma_commit(&sm.mbar);
+      }
     }
     // ---- 3'. the T^2 + 2T dot products, four lanes each ----------------------
     // Lane l of quad qd sums float4 columns l, l+4, ... of its pair, starting
@@ -528,42 +578,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
         sm.cGc[tid] = a;
       }
     }
-    if constexpr (kTC) {
-      // this thread's 64 state values into registers (the warp's rows arrive
-      // with one bulk copy); the A tiles overwrite them after the barrier, so
-      // the write-back copy of an applied commit must have read them too
-      const bool late = !mbar_wait_bounded(&sm.bar[(16 * warp) / kTileRows], 0);
-      if (!late) {
-        const float *row = sm.S + tc_i * D + 64 * tc_hf;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = (j + tc_r) & 7;
-          sv[2 * j] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 * tc_fsw);
-          sv[2 * j + 1] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 - 4 * tc_fsw);
-        }
-      }
-      if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
-      tc_fence_before();
-      const bool failed = __syncthreads_or(late);
-      tc_fence_after();
-      if (failed) {
-        if (warp == NWARP - 1) tmem_dealloc(sm.tmem, kTcCols);
-        give_up();
-        return;
-      }
-      uint16_t *ahi = reinterpret_cast<uint16_t *>(sm.S), *alo = ahi + D * D;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = 8 * tc_hf + ((j + tc_r) & 7);
-        const float4 a = tc_fsw ? sv[2 * j + 1] : sv[2 * j], z = tc_fsw ? sv[2 * j] : sv[2 * j + 1];
-        const float v8[8] = {a.x, a.y, a.z, a.w, z.x, z.y, z.z, z.w};
-        const uint32_t o = canon_off(tc_i, 8 * c, D) / 2;
-        store8_split_trunc(v8, ahi + o, alo + o);
-      }
-      fence_async_smem();  // the tiles (and the B operand) are read by the tensor cores
-    } else {
-      __syncthreads();
-    }
+    __syncthreads();
     // ---- 4'. coefficients of the recurrence, one thread each -----------------
     const float qs = 1.0f / sqrtf(float(D));
     for (int i = tid; i < T + T * T; i += NTHR) {  // (T + T^2 can exceed the CTA at d = 32)
@@ -630,23 +645,9 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
   const size_t plane = size_t(p.B) * H_v * D * D;
   const bool gated = p.gz != nullptr;
   if constexpr (kTC) {
-    // ---- 5''. one thread issues the products; thread i < d then runs the
-    // recurrence of state row i from its 2T dot products in TMEM lane i ------
+    // ---- 5''. thread i < d runs the recurrence of state row i from its 2T
+    // dot products in TMEM lane i; warp 4 writes the captures meanwhile -----
     const uint32_t tmem = sm.tmem;
-    if (tid == 0) {
-      tc_fence_after();
-      // B_hi (rows 0..15) and B_lo (rows 16..31) form one 32-row tile
-      const uint32_t aH = smem_u32(sm.S), aL = aH + D * D * 2, bH = smem_u32(sm.bqk);
-      constexpr uint32_t idesc32 = umma_idesc_bf16(D, 2 * kTcN), idesc16 = umma_idesc_bf16(D, kTcN);
-      constexpr uint32_t sbo = (D / 8) * 128;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        umma_bf16(tmem, umma_desc(aH + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo), idesc32, kk > 0);
-        umma_bf16(tmem + 2 * kTcN, umma_desc(aL + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo), idesc16,
-                  kk > 0);
-      }
-      umma_commit(&sm.mbar);
-    }
     const bool rower = tid < D;  // warps 0..3: TMEM lanes 32w..32w+31
     const int i = tid;
     float o[T], e[T];
@@ -693,6 +694,19 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
           }
         }
       }
+    }
+    if (warp == 4) {
+      // the key head's normalised k (one copy per (row, value head) in
+      // DEFERRED mode, per key head otherwise) and the cumulative decay
+      const size_t bk = MODE == GDN_COMMIT_DEFERRED ? bh : size_t(b) * H_k + hk;
+      if (MODE == GDN_COMMIT_DEFERRED || qk_writer)
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const float4 kr = *reinterpret_cast<const float4 *>(&sm.k[t][4 * lane]);
+          const float ik = sm.cinvk[t];
+          st_f4(p.ws_k + (bk * T + t) * D + 4 * lane, make_float4(kr.x * ik, kr.y * ik, kr.z * ik, kr.w * ik));
+        }
+      if (lane < T) p.ws_G[bh * kMaxT + lane] = sm.cGc[lane];
     }
     // every TMEM read is done before the accumulator is released
     tc_fence_before();
@@ -876,7 +890,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
   if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) p.ws_pend[bh] = 0;  // (a repeat if applied before the wait)
 
   // ---- 6. captures of the key head and decay --------------------------------
-  if (MODE != GDN_COMMIT_SNAPSHOT) {
+  if (MODE != GDN_COMMIT_SNAPSHOT && !kTC) {  // (the tensor-core path wrote them in 5'')
     // k: one copy per key head in RECOMPUTE mode, one per (row, value head)
     // in DEFERRED mode
     const size_t bk = MODE == GDN_COMMIT_DEFERRED ? bh : size_t(b) * H_k + hk;
