@@ -50,3 +50,25 @@ def test_blocked_generation_is_block_size_independent(monkeypatch):
     c = synth.normal_bf16(9, "blk", (3000,))
     assert np.array_equal(a, b)
     assert np.array_equal(c, synth.bf16_bits(a))
+
+
+def test_splitmix64_published_vectors():
+    """The counter stream is SplitMix64: state_i = i * 0x9E3779B97F4A7C15,
+    output = its finaliser.  With a zero key the first five outputs are the
+    generator's published seed-0 test vectors."""
+    published = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F, 0xF88BB8A8724C81EC,
+                 0x1B39896A51A8749B]
+    i = np.arange(1, 6, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = synth._mix64(np.uint64(0) + i * synth._GOLDEN)
+    assert [int(v) for v in z] == published
+
+
+def test_uniform_maps_the_top_53_bits_into_the_open_interval():
+    u = synth.uniform(7, "u", 4096)
+    key = synth._key(7, "u")
+    i = np.arange(1, 4097, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = synth._mix64(key + i * synth._GOLDEN)
+    assert np.array_equal(u, ((z >> np.uint64(11)).astype(np.float64) + 0.5) / 2.0 ** 53)
+    assert (u > 0).all() and (u < 1).all()
