@@ -49,6 +49,8 @@ class gdn_dims(ctypes.Structure):
 
 
 def dims(B, T, H_k, H_v, d, T_max=None, width=4, act=GDN_ACT_SILU) -> gdn_dims:
+    """gdn_dims for one cohort: B rows, T positions per verify (T_max >= T sizes
+    the conv ring), H_k key and H_v value heads of size d, width-4 conv."""
     return gdn_dims(B, T, T if T_max is None else T_max, H_k, H_v, d, d, width, act)
 
 
@@ -98,6 +100,7 @@ def _declare(lib):
 
 
 def library_path() -> str:
+    """Where build() puts libgdn_gb300.so."""
     return _build.LIB_PATH
 
 
@@ -154,19 +157,29 @@ def _t():
 
 
 def gdn_version() -> str:
+    """Library name, version and target architecture."""
     return load().gdn_version().decode()
 
 
 def gdn_last_error() -> str:
+    """Text of the last error returned on this thread."""
     return load().gdn_last_error().decode()
 
 
 def gdn_layer_workspace_bytes(d: gdn_dims, mode: int) -> int:
+    """Bytes of per-layer workspace gdn_conv_verify fills and gdn_commit reads
+    in commit mode `mode` (0 for invalid dims or mode)."""
     return int(load().gdn_layer_workspace_bytes(ctypes.byref(d), mode))
 
 
 def gdn_conv_verify(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets, active, out,
                     layer_ws, layer_ws_bytes=None, stream=None):
+    """Verify one layer (gdn.h, gdn_conv_verify).  CUDA tensors: x [B][T][C]
+    bf16, conv_w [C][4] bf16, g and beta [B][T][H_v] fp32, state
+    [B][H_v][d][d] fp32, ring [B][R][C] bf16, offsets [B] int32 (may be
+    None), active [B] uint8, out [B][T][H_v][d] bf16, layer_ws uint8 of
+    gdn_layer_workspace_bytes.  `mode` may carry GDN_VERIFY_OVERLAP.
+    Runs on `stream` (default: torch's current stream)."""
     torch = _t()
     if layer_ws_bytes is None:
         layer_ws_bytes = layer_ws.numel() * layer_ws.element_size()
@@ -244,11 +257,16 @@ def gdn_flush(d: gdn_dims, mode, states, layer_ws, stream=None):
 
 
 def gdn_prefill_workspace_bytes(d: gdn_dims, L: int) -> int:
+    """Bytes of scratch gdn_prefill_chunked needs for an L-token prompt."""
     return int(load().gdn_prefill_workspace_bytes(ctypes.byref(d), L))
 
 
 def gdn_prefill_chunked(d: gdn_dims, L, x, conv_w, g, beta, state, ring, offsets, out, ws,
                         ws_bytes=None, stream=None):
+    """Prime state, ring and offsets over an L-token prompt (gdn.h,
+    gdn_prefill_chunked): x [B][L][C] bf16, g and beta [B][L][H_v] fp32,
+    out [B][L][H_v][d] bf16, ws of gdn_prefill_workspace_bytes; the other
+    tensors as in gdn_conv_verify."""
     torch = _t()
     if ws_bytes is None:
         ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
@@ -277,6 +295,7 @@ def gdn_move_rows(src_d: gdn_dims, dst_d: gdn_dims, mode, src_states, src_rings,
 
 
 def gdn_accept_workspace_bytes(B: int, T: int, V: int) -> int:
+    """Bytes of workspace gdn_accept_greedy needs (0 for invalid sizes)."""
     return int(load().gdn_accept_workspace_bytes(B, T, V))
 
 
@@ -294,6 +313,8 @@ def gdn_accept_greedy(logits, draft, active, keep, nxt, ws, stream=None):
 
 
 def gdn_get_status(clear: bool = False) -> int:
+    """The sticky device status word (GDN_STATUS_* bits); synchronises the
+    device.  clear=True resets it after reading."""
     v = ctypes.c_uint32(0)
     rc = load().gdn_get_status(1 if clear else 0, ctypes.byref(v))
     _check(rc, "gdn_get_status")
