@@ -178,6 +178,20 @@ def pin_dense_product(orc):
             _close(o[0, t, h], Sd[t] @ q[t, h], 1e-12, f"output t={t} h={h} vs S_t q_t")
 
 
+def pin_dense_product_deep(orc):
+    """The dense product form at the deep-draft shape the GPU path is checked
+    at (T = 8, d = 128), with two value heads sharing one key head."""
+    p = _rand_problem(19, B=1, T=8, H_k=1, H_v=2, d=128)
+    o, Sall = orc.verify(p["x"], p["w"], p["win"], p["g"], p["beta"], p["S0"], np.ones(1, np.uint8), H_k=1)
+    q, k, v = np_heads(np_conv(p["win"][0], p["x"][0], p["w"], 1), 1, 2, 128)
+    for h in range(2):
+        Sd = dense_states(p["S0"][0, h].astype(np.float64), k[:, h], v[:, h], p["g"][0, :, h],
+                          p["beta"][0, :, h])
+        for t in range(8):
+            _close(Sall[0, t, h], Sd[t], 1e-11, f"deep state t={t} h={h} vs dense product form")
+            _close(o[0, t, h], Sd[t] @ q[t, h], 1e-11, f"deep output t={t} h={h} vs S_t q_t")
+
+
 def pin_beta_zero(orc):
     p = _rand_problem(14, B=1, T=3, H_k=1, H_v=1, d=8)
     beta = np.zeros_like(p["beta"])
@@ -433,7 +447,7 @@ def pin_gated_rmsnorm(orc):
     assert np.allclose(np.sqrt((u ** 2).mean(axis=-1)), 1.0, rtol=1e-12)
 
 
-ALL_PINS = [pin_conv_numpy, pin_conv_taps, pin_dense_product, pin_beta_zero, pin_orthonormal_store,
+ALL_PINS = [pin_conv_numpy, pin_conv_taps, pin_dense_product, pin_dense_product_deep, pin_beta_zero, pin_orthonormal_store,
             pin_one_step_store, pin_key_head_sharing, pin_commit_prefix, pin_restore_and_inert,
             pin_prefill_is_verify_commit, pin_chunked_wy, pin_golden_hand, pin_row_separable,
             pin_accept_hand, pin_accept_ties_and_nan, pin_accept_random, pin_gated_rmsnorm]
