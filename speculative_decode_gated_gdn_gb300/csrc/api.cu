@@ -9,9 +9,13 @@
 // layers).
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <cmath>
 #include <mutex>
 #include <string>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "gdn_common.cuh"
 
@@ -104,6 +108,43 @@ int cuda_fail(cudaError_t e, const char *what) {
   return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "TmaDesc holds one CUtensorMap");
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (thread-safe
+// static initialisation); nullptr if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// The tensor map of one layer's state for the d = 128 tensor-core verify:
+// fp32 [rows][128] (rows = B * H_v * d_v), boxes of 128 rows x 32 columns,
+// 128-byte swizzle (the layout the kind::tf32 products read).
+int encode_state_map(TmaDesc &m, const float *state, long long rows) {
+  if (rows > (1LL << 31) - 1)
+    return fail(GDN_ERR_UNSUPPORTED, "B * H_v * d_v = %lld state rows exceed the 2^31 - 1 a tensor map addresses", rows);
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(GDN_ERR_CUDA, "the driver provides no cuTensorMapEncodeTiled");
+  CUtensorMap map;
+  const cuuint64_t dim[2] = {128, cuuint64_t(rows)};
+  const cuuint64_t stride[1] = {128 * sizeof(float)};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(state), dim, stride, box,
+                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled of the state failed (CUresult %d)", int(r));
+  std::memcpy(&m, &map, sizeof map);
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -169,6 +210,11 @@ int verify_impl(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf1
   p.geps = eps;
   p.status = status_word_address();
   if (!p.status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
+  p.wait_limit = kWaitLimit;
+  p.test_extra_tx = 0;
+  if (dims->d_k == 128 && mode != GDN_COMMIT_SNAPSHOT &&
+      (rc = encode_state_map(p.tmap_state, state, (long long)dims->B * dims->H_v * 128)))
+    return rc;
   char *ws = static_cast<char *>(layer_ws);
   if (mode == GDN_COMMIT_RECOMPUTE) {
     const RecomputeWs w = recompute_ws(dims->B, dims->T, dims->H_k, dims->H_v, dims->d_k);

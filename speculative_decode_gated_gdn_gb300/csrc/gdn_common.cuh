@@ -42,6 +42,11 @@ __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
   return v;
 }
 
+// Hint: bring the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void st_f4(float *p, float4 v) {
   *reinterpret_cast<float4 *>(p) = v;
 }
@@ -117,6 +122,42 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   return false;
 }
 
+// As mbar_wait_bounded, with the iteration limit passed in.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= 32) __nanosleep(256);
+  }
+  return false;
+}
+
+// ---- bulk tensor copies (tensor maps) -------------------------------------------
+// A tensor map (CUtensorMap) for the bulk tensor copies, encoded on the host
+// by cuTensorMapEncodeTiled and passed to kernels as a __grid_constant__
+// parameter so that its address is valid for cp.async.bulk.tensor.
+struct alignas(64) TmaDesc {
+  unsigned long long raw[16];
+};
+
+// One 2-D box of `map` at column x, row y into shared memory (complete_tx on
+// `bar`); x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void *dst, const TmaDesc *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// One 2-D box from shared memory to `map` at column x, row y (x, y >= 0),
+// tracked as a bulk group of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const TmaDesc *map, int x, int y, const void *src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+
 // ---- programmatic dependent launch --------------------------------------------
 // Every kernel of the library is launched with programmatic stream
 // serialization.  It waits for the preceding kernel on the stream
@@ -180,6 +221,37 @@ __device__ __forceinline__ void store8_split(const float *v, uint16_t *hi, uint1
   }
   *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
   if (lo) *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// fp32 -> tf32 (round to nearest, ties away from zero), as the 32-bit pattern
+// the tensor cores read.
+__device__ __forceinline__ uint32_t f2tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// Shared-memory descriptor of a K-major operand stored with the 128-byte
+// swizzle (as a bulk tensor copy with that swizzle leaves it): 8-row groups
+// of 128-byte rows, 1024 bytes apart; layout type 2 at bits 61-63.  A K step
+// inside the 128-byte row advances the start address by its bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return uint64_t((saddr >> 4) & 0x3FFF) | (uint64_t(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::tf32 (A and B tf32, fp32 accumulator, both
+// K-major), shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B^T for one K step of 8 tf32 elements; issued by one thread.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(uint32_t(acc))
+      : "memory");
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
@@ -350,6 +422,10 @@ __device__ __forceinline__ int lane_of_row(int i) {
 
 // Per-layer verify parameters.
 struct VerifyParams {
+  // d = 128 tensor-core verify: the layer's state viewed as a 2-D fp32 array
+  // [B * H_v * d_v rows][d_k columns], boxes of 128 rows x 32 columns with the
+  // 128-byte swizzle
+  TmaDesc tmap_state;
   const uint16_t *x;
   const uint16_t *w;
   const float *g;
@@ -374,6 +450,10 @@ struct VerifyParams {
   const uint16_t *gz;  // [B][T][H_v][d_v] bf16 gate, or nullptr (plain o)
   const uint16_t *gw;  // [d_v] bf16 weight
   float geps;
+  uint32_t wait_limit;  // iterations of a bounded mbarrier wait (kWaitLimit)
+  // tests only (0 in every library call): extra bytes announced on the first
+  // state-tile barrier of CTA (row 0, head 0), so that its bounded wait runs out
+  uint32_t test_extra_tx;
 };
 
 constexpr int kMaxLayers = GDN_MAX_LAYERS;

@@ -49,6 +49,8 @@
 //              S_t = a_t S_{t-1} + e_t k_t^T.
 #pragma once
 
+#include <atomic>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -920,42 +922,41 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
 template <int D, int T, int MODE>
 cudaError_t launch_verify_kernel(dim3 grid, cudaStream_t stream, const VerifyParams &p) {
   const dim3 block(VerifyShape<D, T, MODE>::kThreads);
-  static bool configured[64] = {false};  // one flag set per instantiation
+  static std::atomic<bool> configured[64];  // one flag set per instantiation
   constexpr int smem = int(sizeof(VerifySmem<D, T>));
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(verify_kernel<D, T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   return launch_pdl_smem(verify_kernel<D, T, MODE>, grid, block, smem, stream, p);
 }
 
+// One commit mode, every T.
+template <int D, int MODE>
+cudaError_t launch_verify_m(const VerifyParams &p, int T, cudaStream_t stream) {
+  const dim3 grid(p.H_v, p.B);
+  switch (T) {
+    case 1: return launch_verify_kernel<D, 1, MODE>(grid, stream, p);
+    case 2: return launch_verify_kernel<D, 2, MODE>(grid, stream, p);
+    case 3: return launch_verify_kernel<D, 3, MODE>(grid, stream, p);
+    case 4: return launch_verify_kernel<D, 4, MODE>(grid, stream, p);
+    case 5: return launch_verify_kernel<D, 5, MODE>(grid, stream, p);
+    case 6: return launch_verify_kernel<D, 6, MODE>(grid, stream, p);
+    case 7: return launch_verify_kernel<D, 7, MODE>(grid, stream, p);
+    case 8: return launch_verify_kernel<D, 8, MODE>(grid, stream, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int D>
 cudaError_t launch_verify_d(const VerifyParams &p, int T, int mode, cudaStream_t stream) {
-  const dim3 grid(p.H_v, p.B);
-#define GDN_VERIFY_CASE(TT)                                                                   \
-  case TT:                                                                                    \
-    return mode == GDN_COMMIT_RECOMPUTE                                                       \
-               ? launch_verify_kernel<D, TT, GDN_COMMIT_RECOMPUTE>(grid, stream, p)    \
-               : mode == GDN_COMMIT_SNAPSHOT                                                  \
-                     ? launch_verify_kernel<D, TT, GDN_COMMIT_SNAPSHOT>(grid, stream, p) \
-                     : launch_verify_kernel<D, TT, GDN_COMMIT_DEFERRED>(grid, stream, p);
-  switch (T) {
-    GDN_VERIFY_CASE(1)
-    GDN_VERIFY_CASE(2)
-    GDN_VERIFY_CASE(3)
-    GDN_VERIFY_CASE(4)
-    GDN_VERIFY_CASE(5)
-    GDN_VERIFY_CASE(6)
-    GDN_VERIFY_CASE(7)
-    GDN_VERIFY_CASE(8)
-    default:
-      return cudaErrorInvalidValue;
-  }
-#undef GDN_VERIFY_CASE
+  if (mode == GDN_COMMIT_RECOMPUTE) return launch_verify_m<D, GDN_COMMIT_RECOMPUTE>(p, T, stream);
+  if (mode == GDN_COMMIT_SNAPSHOT) return launch_verify_m<D, GDN_COMMIT_SNAPSHOT>(p, T, stream);
+  return launch_verify_m<D, GDN_COMMIT_DEFERRED>(p, T, stream);
 }
 
 }  // namespace gdn

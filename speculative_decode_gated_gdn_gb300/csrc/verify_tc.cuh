@@ -1,0 +1,636 @@
+// verify_tc.cuh -- the d = 128 verify (RECOMPUTE and DEFERRED commits) with
+// the state dot products on the tensor cores.
+//
+// Work decomposition.  One CTA of 128 threads owns one (row b, value head h);
+// thread j owns state row j (the d_v index).  At entry one thread stages the
+// head's 64 KiB fp32 state with four bulk tensor copies (boxes of 128 rows x
+// 32 columns, 128-byte swizzle), each completing on its own mbarrier.  The
+// staged tile is directly the A operand of a kind::tf32 tcgen05 product: the
+// 2T dot products of every state row with the raw conv outputs k_t, q_t are
+//   D[j][n] = sum_i S_0[j][i] B[n][i],   B = [k_0 .. k_{T-1}; q_0 .. q_{T-1}],
+// one M = 128, N = 16, K = 128 product (16 MMAs of K = 8) accumulated in
+// TMEM, so no thread reduces anything across lanes and no pass converts the
+// state.  The tensor cores read the fp32 state truncated to tf32 (and B
+// rounded to tf32): about 2^-11 of each term, orders of magnitude inside the
+// 1e-3 relative state tolerance, since the products only enter e_t and o_t.
+//
+// Thread i also convolves channel i of the key head's q and k and of the
+// value head's v (so the v channel it convolves is its own state row).  The
+// conv taps and the committed window are loaded before the wait on the
+// preceding kernel when the call carries GDN_VERIFY_OVERLAP; only x, g and
+// beta are read after it.
+//
+// Arithmetic: the single-chunk WY form of the gated delta rule ("MTP
+// inference: review and commit structure", Verification and limits: the
+// chunked form equals the sequential one up to rounding).  With
+// gamma_t = exp(G_t), G_t = g_0 + ... + g_t:
+//   e_t[j] = b_t v_t[j] - b_t gamma_t (S_0[j].k^_t) - sum_{s<t} b_t e^{G_t-G_s} (k^_s.k^_t) e_s[j]
+//   o_t[j] = gamma_t (S_0[j].q^_t) + sum_{s<=t} e^{G_t-G_s} (k^_s.q^_t) e_s[j]
+// with the L2 norms (and 1/sqrt(d_k)) folded into per-head coefficients.
+//
+// DEFERRED: a commit the last gdn_commit left pending for this (row, head)
+// is applied to the staged tile in shared memory (thread j, row j, the eager
+// commit's arithmetic and order) and written back with bulk tensor stores
+// before the products read the tile.
+#pragma once
+
+#include <atomic>
+#include <cstddef>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+constexpr int kVtD = 128;          // head size of this kernel
+constexpr int kVtThreads = 128;    // one thread per state row
+constexpr int kVtBoxCols = 32;     // columns per swizzled box (128 bytes of fp32)
+constexpr int kVtBoxes = kVtD / kVtBoxCols;
+constexpr uint32_t kVtBoxBytes = kVtD * kVtBoxCols * sizeof(float);  // 16 KiB
+constexpr int kVtN = 16;           // N of the product: rows 0..2T-1 of B used
+constexpr uint32_t kVtTmemCols = 32;
+
+// Per-CTA scalars of the recurrence and the barriers.
+template <int T>
+struct VtScalars {
+  static constexpr int NV = 2 * T + T * (T - 1) / 2 + T * (T + 1) / 2;
+  alignas(16) float cG[kMaxT];  // DEFERRED: G of the verify whose commit is pending (one bulk copy)
+  float hraw[NV];     // |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t) of the raw conv outputs
+  float cA[T][T];     // beta_t e^{G_t-G_s} (k^_s.k^_t), s < t
+  float cQ[T][T];     // e^{G_t-G_s} (k^_s.q^_t), s <= t
+  float cbk[T], cgq[T], cinvk[T], cGc[T];
+  float gsq[T][kVtThreads / 32];
+  uint64_t bar[kVtBoxes];  // the four state boxes
+  uint64_t cbar;           // DEFERRED captures
+  uint64_t mbar;           // products done
+  uint32_t tmem;
+  int fail;
+};
+
+// Shared memory.  B holds rows 0..7 of the product's B operand (tf32,
+// K-major, no swizzle: 8-row x 16-byte core matrices, 128 bytes apart along
+// K).  For 2T > 8 a second 8-row group follows; for 2T <= 8 the descriptor's
+// second group falls on the arrays after B, whose product columns (8..15)
+// are never read.
+template <int T>
+struct VtSmem {
+  static constexpr bool kTwoGroups = 2 * T > 8;
+  alignas(1024) float S[kVtD * kVtD];
+  alignas(1024) uint32_t B[(kTwoGroups ? 16 : 8) * kVtD];
+  float q[T][kVtD];   // raw conv outputs
+  float k[T][kVtD];
+  float ce[T][kVtD];  // DEFERRED: e_t of the verify whose commit is pending
+  float ck[T][kVtD];  // DEFERRED: its normalised k_t
+  VtScalars<T> sc;
+};
+
+// every bulk-copy destination is 16-byte aligned, the tile 1024-byte aligned
+template <int T>
+constexpr bool vt_layout_ok() {
+  return offsetof(VtSmem<T>, S) % 1024 == 0 && offsetof(VtSmem<T>, B) % 1024 == 0 &&
+         offsetof(VtSmem<T>, q) % 16 == 0 && offsetof(VtSmem<T>, k) % 16 == 0 && offsetof(VtSmem<T>, ce) % 16 == 0 &&
+         offsetof(VtSmem<T>, ck) % 16 == 0 && (offsetof(VtSmem<T>, sc) + offsetof(VtScalars<T>, cG)) % 16 == 0 &&
+         (offsetof(VtSmem<T>, sc) + offsetof(VtScalars<T>, bar)) % 8 == 0;
+}
+
+template <int T>
+constexpr size_t vt_smem_bytes() {
+  static_assert(vt_layout_ok<T>(), "shared-memory layout alignment");
+  // the B descriptor reads 16 rows (two 4 KiB groups) whatever T is
+  constexpr size_t b_off = offsetof(VtSmem<T>, B);
+  constexpr size_t need = b_off + 2 * 4096;
+  return sizeof(VtSmem<T>) > need ? sizeof(VtSmem<T>) : need;
+}
+
+// Byte offset of B element (n, i) in the canonical layout.
+__device__ __forceinline__ uint32_t vt_b_off(int n, int i) {
+  return uint32_t((n / 8) * 4096 + (i / 4) * 128 + (n % 8) * 16 + (i % 4) * 4);
+}
+
+// Float index of state element (row j, columns 4u..4u+3 of box c) in the
+// swizzled tile: the 16-byte chunk u of a 128-byte row moves to u ^ (j % 8).
+__device__ __forceinline__ int vt_s_idx(int c, int j, int u) {
+  return c * (kVtD * kVtBoxCols) + j * kVtBoxCols + ((u ^ (j & 7)) << 2);
+}
+
+// Conv taps and committed window of one channel (raw bf16 patterns).
+struct VtTaps {
+  uint2 w;
+  uint16_t win[kHist];
+};
+
+__device__ __forceinline__ void vt_load_taps(const VerifyParams &p, int b, int c, VtTaps &t) {
+  t.w = *reinterpret_cast<const uint2 *>(p.w + size_t(c) * kWidth);
+  const uint16_t *rb = p.ring + size_t(b) * p.R * p.C + c;
+#pragma unroll
+  for (int i = 0; i < kHist; ++i) t.win[i] = rb[size_t(kWinSlot + i) * p.C];
+}
+
+template <int T>
+__device__ __forceinline__ void vt_load_x(const VerifyParams &p, int b, int c, uint16_t (&x)[T]) {
+  const uint16_t *xb = p.x + size_t(b) * T * p.C + c;
+#pragma unroll
+  for (int t = 0; t < T; ++t) x[t] = xb[size_t(t) * p.C];
+}
+
+// Causal width-4 conv over the T new positions, then the activation (the
+// arithmetic of the CUDA-core verify, term for term).
+template <int T>
+__device__ __forceinline__ void vt_conv(const VtTaps &tp, const uint16_t (&x)[T], int act, float (&y)[T]) {
+  const float w0 = bf2f(uint16_t(tp.w.x & 0xffff)), w1 = bf2f(uint16_t(tp.w.x >> 16));
+  const float w2 = bf2f(uint16_t(tp.w.y & 0xffff)), w3 = bf2f(uint16_t(tp.w.y >> 16));
+  float xt[kHist + T];
+#pragma unroll
+  for (int i = 0; i < kHist; ++i) xt[i] = bf2f(tp.win[i]);
+#pragma unroll
+  for (int t = 0; t < T; ++t) xt[kHist + t] = bf2f(x[t]);
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    float acc = w0 * xt[t];
+    acc = fmaf(w1, xt[t + 1], acc);
+    acc = fmaf(w2, xt[t + 2], acc);
+    acc = fmaf(w3, xt[t + 3], acc);
+    y[t] = act ? silu_fast(acc) : acc;
+  }
+}
+
+template <int T>
+__device__ __forceinline__ void vt_store_ring(const VerifyParams &p, int b, int c, const uint16_t (&x)[T]) {
+  uint16_t *rb = p.ring + size_t(b) * p.R * p.C + c;
+#pragma unroll
+  for (int t = 0; t < T; ++t) rb[size_t(kNewSlot + t) * p.C] = x[t];
+}
+
+template <int T, int MODE>
+__global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
+    verify_tc_kernel(const __grid_constant__ VerifyParams p) {
+  constexpr int D = kVtD, NTHR = kVtThreads;
+  constexpr int NKK = T * (T - 1) / 2, NV = VtScalars<T>::NV;
+  constexpr bool kDef = MODE == GDN_COMMIT_DEFERRED;
+  static_assert(2 * T <= kVtN, "the product holds 2T <= 16 vectors");
+  extern __shared__ __align__(1024) unsigned char tsm_raw[];
+  VtSmem<T> &sm = *reinterpret_cast<VtSmem<T> *>(tsm_raw);
+  VtScalars<T> &sc = sm.sc;
+
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H_v = p.H_v, H_k = p.H_k;
+  const int hk = h / (H_v / H_k);
+  const size_t bh = size_t(b) * H_v + h;
+  const int row0 = int(bh) * D;  // first row of this tile in the state map
+  const uint32_t wl = p.wait_limit;
+
+  // With GDN_VERIFY_OVERLAP the next kernel may start at once and this one
+  // stages its state (and reads its taps, window and pending keep) before
+  // waiting for the preceding kernel; without it, it waits first.
+  if (p.overlap) {
+    pdl_trigger();
+  } else {
+    pdl_wait();
+    pdl_trigger();
+  }
+  // the swizzled copies and the products need a 1024-byte aligned tile; a
+  // misaligned window (never seen) is reported, not used
+  if (smem_u32(tsm_raw) & 1023u) {
+    if (tid == 0) atomicOr(p.status, GDN_STATUS_TIMEOUT);
+    return;
+  }
+  const bool active = p.active[b] != 0;
+  if (tid == 0) {
+#pragma unroll
+    for (int c = 0; c < kVtBoxes; ++c) mbar_init(&sc.bar[c], 1);
+    mbar_init(&sc.cbar, 1);
+    mbar_init(&sc.mbar, 1);
+    fence_mbar_init();
+    sc.fail = 0;
+  }
+  __syncthreads();  // initialised barriers are visible to every waiter
+
+  // DEFERRED: K = keep' of a commit of this (row, head) not yet applied.  It
+  // is final before the wait when the call is flagged (a commit is followed
+  // by an unflagged call), otherwise read after it.
+  int K = 0;
+  bool applied = false;
+  if (kDef && p.overlap) K = min(p.ws_pend[bh], T);
+  bool staged = false;
+  auto stage = [&]() {
+    staged = true;
+    if (tid == 0) {
+      const uint32_t extra = (b == 0 && h == 0) ? p.test_extra_tx : 0u;
+#pragma unroll
+      for (int c = 0; c < kVtBoxes; ++c) {
+        mbar_arrive_expect_tx(&sc.bar[c], kVtBoxBytes + (c == 0 ? extra : 0u));
+        tma_load_2d(&sm.S[c * D * kVtBoxCols], &p.tmap_state, c * kVtBoxCols, row0, &sc.bar[c]);
+      }
+      if (kDef && K >= 1) {
+        constexpr uint32_t kCap = T * D * sizeof(float);
+        mbar_arrive_expect_tx(&sc.cbar, 2 * kCap + kMaxT * sizeof(float));
+        bulk_g2s(&sm.ce[0][0], p.ws_e + bh * T * D, kCap, &sc.cbar);
+        bulk_g2s(&sm.ck[0][0], p.ws_k + bh * T * D, kCap, &sc.cbar);
+        bulk_g2s(sc.cG, p.ws_G + bh * kMaxT, kMaxT * sizeof(float), &sc.cbar);
+      }
+    }
+  };
+  // A bounded wait ran out: flag it, wait (bounded) for every copy this CTA
+  // issued so none lands after it has left, and write nothing more.
+  auto give_up = [&]() {
+    if (tid == 0) {
+      atomicOr(p.status, GDN_STATUS_TIMEOUT);
+      if (staged) {
+#pragma unroll
+        for (int c = 0; c < kVtBoxes; ++c) mbar_wait_limit(&sc.bar[c], 0, wl);
+        if (kDef && K >= 1) mbar_wait_limit(&sc.cbar, 0, wl);
+      }
+      if (applied) bulk_wait_read_all();
+    }
+  };
+  // DEFERRED: S <- gamma_{K-1} S + sum_{s<K} e^{G_{K-1}-G_s} e_s k^_s^T on row
+  // j = tid of the staged tile (the eager commit's arithmetic and order), then
+  // the updated tile goes back to the state buffer on the bulk-copy engine.
+  // CTA-uniform (its barrier is reached by every thread); false on a timeout.
+  auto apply_and_write = [&]() -> bool {
+    bool ok = mbar_wait_limit(&sc.cbar, 0, wl);
+    if (ok) {
+      const int j = tid;
+      const float GK = sc.cG[K - 1];
+      const float gam = expf(GK);
+      float f[T];
+#pragma unroll
+      for (int t = 0; t < T; ++t) f[t] = t < K ? expf(GK - sc.cG[t]) * sm.ce[t][j] : 0.f;
+#pragma unroll
+      for (int c = 0; c < kVtBoxes; ++c) {
+        if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int u = 0; u < kVtBoxCols / 4; ++u) {
+          float4 *sp = reinterpret_cast<float4 *>(&sm.S[vt_s_idx(c, j, u)]);
+          float4 s = *sp;
+          s = make_float4(gam * s.x, gam * s.y, gam * s.z, gam * s.w);
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            if (t < K) {
+              const float4 kv = *reinterpret_cast<const float4 *>(&sm.ck[t][c * kVtBoxCols + 4 * u]);
+              s.x = fmaf(f[t], kv.x, s.x);
+              s.y = fmaf(f[t], kv.y, s.y);
+              s.z = fmaf(f[t], kv.z, s.z);
+              s.w = fmaf(f[t], kv.w, s.w);
+            }
+          }
+          *sp = s;
+        }
+      }
+    }
+    fence_proxy_async_shared();  // the bulk stores below read these rows
+    if (__syncthreads_or(!ok)) return false;
+    if (tid == 0) {
+#pragma unroll
+      for (int c = 0; c < kVtBoxes; ++c) tma_store_2d(&p.tmap_state, c * kVtBoxCols, row0, &sm.S[c * D * kVtBoxCols]);
+      bulk_commit_group();
+      p.ws_pend[bh] = 0;
+    }
+    applied = true;
+    return true;
+  };
+
+  // ---- inactive rows: no ring access and no output of their own (the CTA of
+  // an active row zero-fills them after its wait, so these CTAs do not hold a
+  // slot while the preceding kernel runs); a pending commit is applied, before
+  // the wait when the call is flagged, like the state staging
+  if (!active) {
+    if (kDef && !p.overlap) K = min(p.ws_pend[bh], T);
+    if (kDef && K >= 1) {
+      stage();
+      if (!apply_and_write()) {
+        give_up();
+        return;
+      }
+    }
+    if (b == 0) {  // no active row at all: row 0's CTA zero-fills every row of head h
+      bool any = false;
+      for (int r = tid; r < p.B; r += NTHR) any |= p.active[r] != 0;
+      if (!__syncthreads_or(any)) {
+        if (p.overlap) pdl_wait();
+        for (int r = 0; r < p.B; ++r)
+#pragma unroll
+          for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
+      }
+    }
+    if (applied && tid == 0) bulk_wait_read_all();
+    return;
+  }
+
+  const int i = tid;  // conv channel i of q, k, v; state row i
+  const int cq = hk * D + i, ck = H_k * D + hk * D + i, cv = 2 * H_k * D + h * D + i;
+  VtTaps tq, tk, tv;
+  if (p.overlap) {
+    // flagged: tensor memory, state, captures, taps and window before the
+    // wait; a pending commit is applied and written back while the preceding
+    // kernel runs.  Allocating (and so giving up the allocation permit) at
+    // entry is what lets further CTAs start on this SM while this one waits:
+    // an SM admits one CTA still holding the permit of a kernel that
+    // allocates tensor memory.  The 32 columns cannot starve the preceding
+    // kernel: at most three verify CTAs fit on an SM (96 of 512 columns), and
+    // the library's prefill kernels, the only others that take tensor memory,
+    // need more shared memory than can sit beside a verify CTA.
+    if (warp == NTHR / 32 - 1) tmem_alloc(&sc.tmem, kVtTmemCols);
+    stage();
+    vt_load_taps(p, b, cq, tq);
+    vt_load_taps(p, b, ck, tk);
+    vt_load_taps(p, b, cv, tv);
+    // warm L2 with this call's x, g and beta lines (a prefetch only: the
+    // values are read after the wait, so a later write by the preceding
+    // kernel is still what they see)
+    if (tid < 6 * T) {
+      const int t = tid / 6, r = tid % 6;  // slabs q, k, v of 128 channels (two 128-byte lines each)
+      const int c0 = (r < 2 ? hk * D : r < 4 ? H_k * D + hk * D : 2 * H_k * D + h * D) + (r & 1) * 64;
+      prefetch_l2(p.x + (size_t(b) * T + t) * p.C + c0);
+    } else if (tid < 8 * T) {
+      const int t = (tid - 6 * T) >> 1;
+      prefetch_l2(((tid & 1) ? p.beta : p.g) + (size_t(b) * T + t) * H_v + h);
+    }
+    if (kDef && K >= 1 && !apply_and_write()) {
+      if (warp == NTHR / 32 - 1) tmem_dealloc(sc.tmem, kVtTmemCols);
+      give_up();
+      return;
+    }
+    pdl_wait();
+  } else {
+    if (kDef) K = min(p.ws_pend[bh], T);
+    stage();
+    vt_load_taps(p, b, cq, tq);
+    vt_load_taps(p, b, ck, tk);
+    vt_load_taps(p, b, cv, tv);
+  }
+  // unflagged: the accumulator columns are taken only after the wait (the
+  // preceding kernel may be any kernel, so no tensor memory is held while
+  // waiting for it)
+  if (!p.overlap && warp == NTHR / 32 - 1) tmem_alloc(&sc.tmem, kVtTmemCols);
+
+  // ---- conv inputs of this call ------------------------------------------------
+  uint16_t xq[T], xk[T], xv[T];
+  vt_load_x<T>(p, b, cq, xq);
+  vt_load_x<T>(p, b, ck, xk);
+  vt_load_x<T>(p, b, cv, xv);
+  float gt[T], bt[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
+    bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
+  }
+  // the inactive rows this CTA zero-fills: those after b up to the next
+  // active row and, when no row below b is active, every row below b
+  {
+    int r_hi = b + 1, r_lo = b - 1;
+    while (r_hi < p.B && !p.active[r_hi]) ++r_hi;
+    while (r_lo >= 0 && !p.active[r_lo]) --r_lo;
+    for (int r = b + 1; r < r_hi; ++r)
+#pragma unroll
+      for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
+    if (r_lo < 0)
+      for (int r = 0; r < b; ++r)
+#pragma unroll
+        for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
+  }
+  // DEFERRED, unflagged: the pending commit is applied while the inputs load
+  bool failed = false;
+  if (kDef && !p.overlap && K >= 1) failed = !apply_and_write();
+  if (failed) {
+    if (warp == NTHR / 32 - 1) tmem_dealloc(sc.tmem, kVtTmemCols);
+    give_up();
+    return;
+  }
+  float yq[T], yk[T], yv[T];
+  vt_conv<T>(tq, xq, p.act, yq);
+  vt_conv<T>(tk, xk, p.act, yk);
+  vt_conv<T>(tv, xv, p.act, yv);
+  unsigned char *bsm = reinterpret_cast<unsigned char *>(sm.B);
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    sm.q[t][i] = yq[t];
+    sm.k[t][i] = yk[t];
+    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(t, i)) = f2tf32(yk[t]);
+    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(T + t, i)) = f2tf32(yq[t]);
+  }
+  // new raw inputs into ring slots 3..2+T: q/k channels by one CTA of the key head
+  if (h % (H_v / H_k) == 0) {
+    vt_store_ring<T>(p, b, cq, xq);
+    vt_store_ring<T>(p, b, ck, xk);
+  }
+  vt_store_ring<T>(p, b, cv, xv);
+  fence_async_smem();  // B is read by the tensor cores
+  tc_fence_before();
+  __syncthreads();  // conv outputs, B and the TMEM address are visible
+  tc_fence_after();
+  const uint32_t tmem = sc.tmem;
+
+  // ---- the products and the per-head coefficients, side by side --------------
+  // The issuing thread stalls while the tensor cores read the 64 KiB tile
+  // (about 0.6 us), so it sits alone in the last warp; the other warps take
+  // the per-head dot products and the recurrence coefficients meanwhile and
+  // meet it at one block barrier.
+  constexpr int NCW = NTHR - 32;  // threads of the coefficient warps
+  if (warp == NTHR / 32 - 1) {
+    if (lane == 0) {
+      bool ok = true;
+      constexpr uint32_t idesc = umma_idesc_tf32(D, kVtN);
+      const uint32_t sB = smem_u32(sm.B), sS = smem_u32(sm.S);
+#pragma unroll
+      for (int c = 0; c < kVtBoxes; ++c) {
+        if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kVtBoxCols / 8; ++kk) {
+          const int ks = c * (kVtBoxCols / 8) + kk;  // K step of 8 columns
+          const uint64_t da = umma_desc_sw128(sS + c * kVtBoxBytes + kk * 32);
+          const uint64_t db = umma_desc(sB + ks * 256, 128, 4096);
+          umma_tf32(tmem, da, db, idesc, ks > 0);
+        }
+      }
+      if (!ok) sc.fail = 1;
+      umma_commit(&sc.mbar);  // also arrives when nothing was issued
+    }
+    __syncwarp();
+  } else {
+    // per-head dot products of the raw conv outputs, four lanes each
+    constexpr int NQ4 = NCW / 4, F4 = D / 4;
+    const int qd = tid >> 2, ql = tid & 3;
+    for (int r0 = 0; r0 < NV; r0 += NQ4) {  // the same trip count in every lane
+      const int n = r0 + qd;
+      float part = 0.f;
+      if (n < NV) {
+        const float *u, *w;
+        if (n < 2 * T) {
+          u = w = (n & 1) ? sm.k[n >> 1] : sm.q[n >> 1];
+        } else if (n < 2 * T + NKK) {  // k_s . k_t, s < t, t-major
+          int r = n - 2 * T, t = 1;
+          while (r >= t) r -= t, ++t;
+          u = sm.k[r], w = sm.k[t];
+        } else {  // k_s . q_t, s <= t, t-major
+          int r = n - 2 * T - NKK, t = 0;
+          while (r > t) r -= t + 1, ++t;
+          u = sm.k[r], w = sm.q[t];
+        }
+#pragma unroll
+        for (int jj = 0; jj < F4 / 4; ++jj) {
+          const int f = (ql + 4 * (jj + qd)) % F4;
+          part += dot4(*reinterpret_cast<const float4 *>(u + 4 * f), *reinterpret_cast<const float4 *>(w + 4 * f));
+        }
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (n < NV && ql == 0) sc.hraw[n] = part;
+    }
+    if (tid < T) {  // cumulative log-decay G_t = g_0 + ... + g_t, in order
+      float a = 0.f;
+#pragma unroll
+      for (int u = 0; u < T; ++u)
+        if (u <= tid) a += gt[u];
+      sc.cGc[tid] = a;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NCW) : "memory");  // the coefficient warps only
+    // coefficients of the recurrence, one thread each
+    const float qs = 1.0f / sqrtf(float(D));
+    for (int n = tid; n < T + T * T; n += NCW) {
+      if (n < T) {
+        const int t = n;
+        const float iq = rsqrtf(sc.hraw[2 * t] + kNormEps) * qs, ik = rsqrtf(sc.hraw[2 * t + 1] + kNormEps);
+        const float gm = expf(sc.cGc[t]);
+        sc.cbk[t] = (bt[t] * gm) * ik;
+        sc.cgq[t] = gm * iq;
+        sc.cinvk[t] = ik;
+        continue;
+      }
+      const int t = (n - T) / T, s0 = (n - T) % T;
+      if (s0 <= t) {
+        const float ik_s = rsqrtf(sc.hraw[2 * s0 + 1] + kNormEps), ik_t = rsqrtf(sc.hraw[2 * t + 1] + kNormEps);
+        const float iq_t = rsqrtf(sc.hraw[2 * t] + kNormEps) * qs;
+        const float dec = s0 == t ? 1.0f : expf(sc.cGc[t] - sc.cGc[s0]);
+        if (s0 < t) sc.cA[t][s0] = bt[t] * dec * (sc.hraw[2 * T + t * (t - 1) / 2 + s0] * ik_s * ik_t);
+        sc.cQ[t][s0] = dec * (sc.hraw[2 * T + NKK + t * (t + 1) / 2 + s0] * ik_s * iq_t);
+      }
+    }
+  }
+  __syncthreads();  // coefficients (and a failed issue) are visible
+
+  // ---- row j = tid: its 2T products from TMEM lane j, then the recurrence ------
+  const int j = tid;
+  const bool gated = p.gz != nullptr;
+  uint16_t zt[T], wj = 0;
+  if (gated) {
+    wj = p.gw[j];
+#pragma unroll
+    for (int t = 0; t < T; ++t) zt[t] = p.gz[((size_t(b) * T + t) * H_v + h) * D + j];
+  }
+  const bool late = !mbar_wait_limit(&sc.mbar, 0, wl) || sc.fail;
+  tc_fence_after();
+  float o[T], e[T];
+  if (!late) {
+    float red[kVtN];
+    tmem_ld16(tmem + (uint32_t(32 * warp) << 16), red);
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      float acc = fmaf(bt[t], yv[t], -sc.cbk[t] * red[t]);
+#pragma unroll
+      for (int s0 = 0; s0 < t; ++s0) acc = fmaf(-sc.cA[t][s0], e[s0], acc);
+      e[t] = acc;
+      float ot = sc.cgq[t] * red[T + t];
+#pragma unroll
+      for (int s0 = 0; s0 <= t; ++s0) ot = fmaf(sc.cQ[t][s0], e[s0], ot);
+      o[t] = ot;
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      if (!gated) p.out[((size_t(b) * T + t) * H_v + h) * D + j] = f2bf(o[t]);
+      p.ws_e[(bh * T + t) * D + j] = e[t];
+    }
+    // captures of the key head: normalised k (one copy per key head in
+    // RECOMPUTE mode, per (row, value head) in DEFERRED mode) and G
+    const size_t bk = kDef ? bh : size_t(b) * H_k + hk;
+    if (kDef || h % (H_v / H_k) == 0) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) p.ws_k[(bk * T + t) * D + i] = yk[t] * sc.cinvk[t];
+    }
+    if (tid < T) p.ws_G[bh * kMaxT + tid] = sc.cGc[tid];
+    if (gated) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        float q2 = o[t] * o[t];
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, m);
+        if (lane == 0) sc.gsq[t][warp] = q2;
+      }
+    }
+  }
+  // every TMEM read is done before the columns are released
+  tc_fence_before();
+  const bool bad = __syncthreads_or(late);
+  tc_fence_after();
+  if (warp == NTHR / 32 - 1) {
+    if (bad) mbar_wait_limit(&sc.mbar, 0, wl);  // products still running must finish first
+    tmem_dealloc(tmem, kVtTmemCols);
+  }
+  if (bad) {
+    give_up();
+    return;
+  }
+  if (gated) {
+    // out = o_t / sqrt(mean_j o_t[j]^2 + eps) * w[j] * silu(z_t[j])
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      float ss = 0.f;
+#pragma unroll
+      for (int w = 0; w < NTHR / 32; ++w) ss += sc.gsq[t][w];
+      const float rstd = rsqrtf(ss / float(D) + p.geps);
+      p.out[((size_t(b) * T + t) * H_v + h) * D + j] = f2bf(o[t] * rstd * bf2f(wj) * silu_fast(bf2f(zt[t])));
+    }
+  }
+  if (applied && tid == 0) bulk_wait_read_all();
+}
+
+// Launch one instantiation, raising its dynamic shared-memory limit once per
+// device.
+template <int T, int MODE>
+cudaError_t launch_verify_tc_kernel(const VerifyParams &p, cudaStream_t stream) {
+  constexpr int smem = int(vt_smem_bytes<T>());
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(verify_tc_kernel<T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // the whole unified L1 / shared array as shared memory: three CTAs per SM
+    // (a layer and most of the next one resident together)
+    e = cudaFuncSetAttribute(verify_tc_kernel<T, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             int(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
+  return launch_pdl_smem(verify_tc_kernel<T, MODE>, dim3(p.H_v, p.B), dim3(kVtThreads), smem, stream, p);
+}
+
+inline cudaError_t launch_verify_tc(const VerifyParams &p, int T, int mode, cudaStream_t stream) {
+#define GDN_VERIFY_TC_CASE(TT)                                                             \
+  case TT:                                                                                 \
+    return mode == GDN_COMMIT_RECOMPUTE ? launch_verify_tc_kernel<TT, GDN_COMMIT_RECOMPUTE>(p, stream) \
+                                        : launch_verify_tc_kernel<TT, GDN_COMMIT_DEFERRED>(p, stream);
+  switch (T) {
+    GDN_VERIFY_TC_CASE(1)
+    GDN_VERIFY_TC_CASE(2)
+    GDN_VERIFY_TC_CASE(3)
+    GDN_VERIFY_TC_CASE(4)
+    GDN_VERIFY_TC_CASE(5)
+    GDN_VERIFY_TC_CASE(6)
+    GDN_VERIFY_TC_CASE(7)
+    GDN_VERIFY_TC_CASE(8)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef GDN_VERIFY_TC_CASE
+}
+
+}  // namespace gdn
