@@ -71,6 +71,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// Plain arrival (count 1) of the executing thread.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Contiguous global -> shared copy on the bulk-copy engine; completion is
 // counted on `bar` in bytes.  dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -128,6 +133,16 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, 
     if (mbar_try_wait(bar, parity)) return true;
     if (i >= 32) __nanosleep(256);
   }
+  return false;
+}
+
+// As mbar_wait_limit without the sleep between polls, for waits on the
+// critical path: try_wait itself suspends the thread until the phase
+// completes or a hardware time limit passes, so each poll is cheap and the
+// wake-up immediate.  Still bounded by `limit` polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
 

@@ -42,7 +42,8 @@
 namespace gdn {
 
 constexpr int kVtD = 128;          // head size of this kernel
-constexpr int kVtThreads = 128;    // one thread per state row
+constexpr int kVtRowThreads = 128; // warps 0-3: one thread per state row
+constexpr int kVtThreads = 160;    // + warp 4: tensor memory and the products
 constexpr int kVtBoxCols = 32;     // columns per swizzled box (128 bytes of fp32)
 constexpr int kVtBoxes = kVtD / kVtBoxCols;
 constexpr uint32_t kVtBoxBytes = kVtD * kVtBoxCols * sizeof(float);  // 16 KiB
@@ -54,16 +55,19 @@ template <int T>
 struct VtScalars {
   static constexpr int NV = 2 * T + T * (T - 1) / 2 + T * (T + 1) / 2;
   alignas(16) float cG[kMaxT];  // DEFERRED: G of the verify whose commit is pending (one bulk copy)
-  float hraw[NV];     // |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t) of the raw conv outputs
+  // per-warp partial sums of the per-head dot products of the raw conv
+  // outputs: |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t)
+  float hpart[kVtRowThreads / 32][NV];
   float cA[T][T];     // beta_t e^{G_t-G_s} (k^_s.k^_t), s < t
   float cQ[T][T];     // e^{G_t-G_s} (k^_s.q^_t), s <= t
   float cbk[T], cgq[T], cinvk[T], cGc[T];
-  float gsq[T][kVtThreads / 32];
+  float gsq[T][kVtRowThreads / 32];
   uint64_t bar[kVtBoxes];  // the four state boxes
   uint64_t cbar;           // DEFERRED captures
-  uint64_t mbar;           // products done
+  uint64_t bready;         // every row thread has written its B column
+  uint64_t mbar;           // products done (never completes if they were not all issued)
+  uint64_t fbar;           // products issued before a failed wait have drained
   uint32_t tmem;
-  int fail;
 };
 
 // Shared memory.  B holds rows 0..7 of the product's B operand (tf32,
@@ -76,8 +80,6 @@ struct VtSmem {
   static constexpr bool kTwoGroups = 2 * T > 8;
   alignas(1024) float S[kVtD * kVtD];
   alignas(1024) uint32_t B[(kTwoGroups ? 16 : 8) * kVtD];
-  float q[T][kVtD];   // raw conv outputs
-  float k[T][kVtD];
   float ce[T][kVtD];  // DEFERRED: e_t of the verify whose commit is pending
   float ck[T][kVtD];  // DEFERRED: its normalised k_t
   VtScalars<T> sc;
@@ -87,7 +89,7 @@ struct VtSmem {
 template <int T>
 constexpr bool vt_layout_ok() {
   return offsetof(VtSmem<T>, S) % 1024 == 0 && offsetof(VtSmem<T>, B) % 1024 == 0 &&
-         offsetof(VtSmem<T>, q) % 16 == 0 && offsetof(VtSmem<T>, k) % 16 == 0 && offsetof(VtSmem<T>, ce) % 16 == 0 &&
+         offsetof(VtSmem<T>, ce) % 16 == 0 &&
          offsetof(VtSmem<T>, ck) % 16 == 0 && (offsetof(VtSmem<T>, sc) + offsetof(VtScalars<T>, cG)) % 16 == 0 &&
          (offsetof(VtSmem<T>, sc) + offsetof(VtScalars<T>, bar)) % 8 == 0;
 }
@@ -160,19 +162,71 @@ __device__ __forceinline__ void vt_store_ring(const VerifyParams &p, int b, int 
   for (int t = 0; t < T; ++t) rb[size_t(kNewSlot + t) * p.C] = x[t];
 }
 
+// Product n of the per-head dot products for one channel's conv outputs:
+// n < 2T: |q_{n/2}|^2 (n even), |k_{n/2}|^2 (n odd); then k_s.k_t (s < t),
+// then k_s.q_t (s <= t), both t-major.
+template <int T>
+__device__ __forceinline__ float vt_head_term(int n, const float (&yq)[T], const float (&yk)[T]) {
+  constexpr int NKK = T * (T - 1) / 2;
+  if (n < 2 * T) return (n & 1) ? yk[n >> 1] * yk[n >> 1] : yq[n >> 1] * yq[n >> 1];
+  if (n < 2 * T + NKK) {
+    int r = n - 2 * T, t = 1;
+    while (r >= t) r -= t, ++t;
+    return yk[r] * yk[t];
+  }
+  int r = n - 2 * T - NKK, t = 0;
+  while (r > t) r -= t + 1, ++t;
+  return yk[r] * yq[t];
+}
+
+// Sums of the per-head products over the warp's 32 channels: rounds of W <= 32
+// products, a reduce-scatter butterfly (masks 16, 8, .., 32/W) then plain
+// butterfly sums; afterwards lane l holds product 32 r + (l >> log2(32/W)),
+// and the first lane of each such group writes it to part[].
+template <int T>
+__device__ __forceinline__ void vt_head_partials(const float (&yq)[T], const float (&yk)[T], int lane, float *part) {
+  constexpr int NV = 2 * T + T * (T - 1) / 2 + T * (T + 1) / 2;
+  constexpr int W = NV >= 32 ? 32 : NV > 16 ? 32 : NV > 8 ? 16 : NV > 4 ? 8 : NV > 2 ? 4 : 2;
+  constexpr int SH = W == 32 ? 0 : W == 16 ? 1 : W == 8 ? 2 : W == 4 ? 3 : 4;  // log2(32 / W)
+#pragma unroll
+  for (int r0 = 0; r0 < NV; r0 += W) {
+    float v[W];
+#pragma unroll
+    for (int m = 0; m < W; ++m) v[m] = r0 + m < NV ? vt_head_term<T>(r0 + m, yq, yk) : 0.f;
+#pragma unroll
+    for (int half = W / 2, mask = 16; half >= 1; half >>= 1, mask >>= 1) {
+      const bool upper = (lane & mask) != 0;
+#pragma unroll
+      for (int m = 0; m < half; ++m) {
+        const float send = upper ? v[m] : v[m + half];
+        const float keep = upper ? v[m + half] : v[m];
+        v[m] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+      }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int mask = (1 << SH) >> 1; mask >= 1; mask >>= 1) x += __shfl_xor_sync(0xffffffffu, x, mask);
+    const int n = r0 + (lane >> SH);
+    if ((lane & ((1 << SH) - 1)) == 0 && n < NV) part[n] = x;
+  }
+}
+
 template <int T, int MODE>
 __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
     verify_tc_kernel(const __grid_constant__ VerifyParams p) {
-  constexpr int D = kVtD, NTHR = kVtThreads;
+  constexpr int D = kVtD, NROW = kVtRowThreads;
   constexpr int NKK = T * (T - 1) / 2, NV = VtScalars<T>::NV;
   constexpr bool kDef = MODE == GDN_COMMIT_DEFERRED;
   static_assert(2 * T <= kVtN, "the product holds 2T <= 16 vectors");
+  static_assert(NROW == D, "one row thread per state row");
   extern __shared__ __align__(1024) unsigned char tsm_raw[];
   VtSmem<T> &sm = *reinterpret_cast<VtSmem<T> *>(tsm_raw);
   VtScalars<T> &sc = sm.sc;
 
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool row = tid < NROW;           // warps 0-3: conv channel i = state row j = tid
+  const bool issuer = warp == NROW / 32;  // warp 4
   const int H_v = p.H_v, H_k = p.H_k;
   const int hk = h / (H_v / H_k);
   const size_t bh = size_t(b) * H_v + h;
@@ -195,15 +249,28 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
     return;
   }
   const bool active = p.active[b] != 0;
+  // Tensor memory (active rows): taken at once by warp 4, before the wait
+  // when the call is flagged.  Allocating gives up the allocation permit, and
+  // an SM admits one CTA still holding the permit of a kernel that allocates
+  // tensor memory, so this is what lets further CTAs of this and the next
+  // layer start beside a waiting one.  The 32 columns cannot starve the
+  // preceding kernel: at most three verify CTAs fit on an SM (96 of 512
+  // columns), and the library's prefill kernels, the only others that take
+  // tensor memory, need more shared memory than can sit beside a verify CTA.
+  // An unflagged call has already waited, whatever the preceding kernel is.
+  if (active && issuer) tmem_alloc(&sc.tmem, kVtTmemCols);
   if (tid == 0) {
 #pragma unroll
     for (int c = 0; c < kVtBoxes; ++c) mbar_init(&sc.bar[c], 1);
     mbar_init(&sc.cbar, 1);
+    mbar_init(&sc.bready, NROW);
     mbar_init(&sc.mbar, 1);
+    mbar_init(&sc.fbar, 1);
     fence_mbar_init();
-    sc.fail = 0;
   }
-  __syncthreads();  // initialised barriers are visible to every waiter
+  tc_fence_before();
+  __syncthreads();  // initialised barriers and the TMEM address are visible
+  tc_fence_after();
 
   // DEFERRED: K = keep' of a commit of this (row, head) not yet applied.  It
   // is final before the wait when the call is flagged (a commit is followed
@@ -246,42 +313,45 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   // DEFERRED: S <- gamma_{K-1} S + sum_{s<K} e^{G_{K-1}-G_s} e_s k^_s^T on row
   // j = tid of the staged tile (the eager commit's arithmetic and order), then
   // the updated tile goes back to the state buffer on the bulk-copy engine.
-  // CTA-uniform (its barrier is reached by every thread); false on a timeout.
+  // Reached by every thread of the CTA (its barrier); false on a timeout.
   auto apply_and_write = [&]() -> bool {
-    bool ok = mbar_wait_limit(&sc.cbar, 0, wl);
-    if (ok) {
-      const int j = tid;
-      const float GK = sc.cG[K - 1];
-      const float gam = expf(GK);
-      float f[T];
+    bool ok = true;
+    if (row) {
+      ok = mbar_wait_limit(&sc.cbar, 0, wl);
+      if (ok) {
+        const int j = tid;
+        const float GK = sc.cG[K - 1];
+        const float gam = expf(GK);
+        float f[T];
 #pragma unroll
-      for (int t = 0; t < T; ++t) f[t] = t < K ? expf(GK - sc.cG[t]) * sm.ce[t][j] : 0.f;
+        for (int t = 0; t < T; ++t) f[t] = t < K ? expf(GK - sc.cG[t]) * sm.ce[t][j] : 0.f;
 #pragma unroll
-      for (int c = 0; c < kVtBoxes; ++c) {
-        if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int u = 0; u < kVtBoxCols / 4; ++u) {
-          float4 *sp = reinterpret_cast<float4 *>(&sm.S[vt_s_idx(c, j, u)]);
-          float4 s = *sp;
-          s = make_float4(gam * s.x, gam * s.y, gam * s.z, gam * s.w);
-#pragma unroll
-          for (int t = 0; t < T; ++t) {
-            if (t < K) {
-              const float4 kv = *reinterpret_cast<const float4 *>(&sm.ck[t][c * kVtBoxCols + 4 * u]);
-              s.x = fmaf(f[t], kv.x, s.x);
-              s.y = fmaf(f[t], kv.y, s.y);
-              s.z = fmaf(f[t], kv.z, s.z);
-              s.w = fmaf(f[t], kv.w, s.w);
-            }
+        for (int c = 0; c < kVtBoxes; ++c) {
+          if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
+            ok = false;
+            break;
           }
-          *sp = s;
+#pragma unroll
+          for (int u = 0; u < kVtBoxCols / 4; ++u) {
+            float4 *sp = reinterpret_cast<float4 *>(&sm.S[vt_s_idx(c, j, u)]);
+            float4 s4 = *sp;
+            s4 = make_float4(gam * s4.x, gam * s4.y, gam * s4.z, gam * s4.w);
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+              if (t < K) {
+                const float4 kv = *reinterpret_cast<const float4 *>(&sm.ck[t][c * kVtBoxCols + 4 * u]);
+                s4.x = fmaf(f[t], kv.x, s4.x);
+                s4.y = fmaf(f[t], kv.y, s4.y);
+                s4.z = fmaf(f[t], kv.z, s4.z);
+                s4.w = fmaf(f[t], kv.w, s4.w);
+              }
+            }
+            *sp = s4;
+          }
         }
       }
+      fence_proxy_async_shared();  // the bulk stores below read these rows
     }
-    fence_proxy_async_shared();  // the bulk stores below read these rows
     if (__syncthreads_or(!ok)) return false;
     if (tid == 0) {
 #pragma unroll
@@ -308,49 +378,54 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
     }
     if (b == 0) {  // no active row at all: row 0's CTA zero-fills every row of head h
       bool any = false;
-      for (int r = tid; r < p.B; r += NTHR) any |= p.active[r] != 0;
+      for (int r = tid; r < p.B; r += kVtThreads) any |= p.active[r] != 0;
       if (!__syncthreads_or(any)) {
         if (p.overlap) pdl_wait();
-        for (int r = 0; r < p.B; ++r)
+        if (row)
+          for (int r = 0; r < p.B; ++r)
 #pragma unroll
-          for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
+            for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
       }
     }
     if (applied && tid == 0) bulk_wait_read_all();
     return;
   }
 
+  // the inactive rows this CTA zero-fills: those after b up to the next
+  // active row (rows b+1 .. r_hi-1) and, when no row below b is active
+  // (r_lo < 0), every row below b; a chain of dependent loads, so a flagged
+  // call finds them before its wait
+  int r_hi = b + 1, r_lo = b - 1;
+  auto find_inactive_neighbours = [&]() {
+    while (r_hi < p.B && !p.active[r_hi]) ++r_hi;
+    while (r_lo >= 0 && !p.active[r_lo]) --r_lo;
+  };
   const int i = tid;  // conv channel i of q, k, v; state row i
   const int cq = hk * D + i, ck = H_k * D + hk * D + i, cv = 2 * H_k * D + h * D + i;
   VtTaps tq, tk, tv;
   if (p.overlap) {
-    // flagged: tensor memory, state, captures, taps and window before the
-    // wait; a pending commit is applied and written back while the preceding
-    // kernel runs.  Allocating (and so giving up the allocation permit) at
-    // entry is what lets further CTAs start on this SM while this one waits:
-    // an SM admits one CTA still holding the permit of a kernel that
-    // allocates tensor memory.  The 32 columns cannot starve the preceding
-    // kernel: at most three verify CTAs fit on an SM (96 of 512 columns), and
-    // the library's prefill kernels, the only others that take tensor memory,
-    // need more shared memory than can sit beside a verify CTA.
-    if (warp == NTHR / 32 - 1) tmem_alloc(&sc.tmem, kVtTmemCols);
+    // flagged: state, captures, taps and window before the wait; a pending
+    // commit is applied and written back while the preceding kernel runs
     stage();
-    vt_load_taps(p, b, cq, tq);
-    vt_load_taps(p, b, ck, tk);
-    vt_load_taps(p, b, cv, tv);
-    // warm L2 with this call's x, g and beta lines (a prefetch only: the
-    // values are read after the wait, so a later write by the preceding
-    // kernel is still what they see)
-    if (tid < 6 * T) {
-      const int t = tid / 6, r = tid % 6;  // slabs q, k, v of 128 channels (two 128-byte lines each)
-      const int c0 = (r < 2 ? hk * D : r < 4 ? H_k * D + hk * D : 2 * H_k * D + h * D) + (r & 1) * 64;
-      prefetch_l2(p.x + (size_t(b) * T + t) * p.C + c0);
-    } else if (tid < 8 * T) {
-      const int t = (tid - 6 * T) >> 1;
-      prefetch_l2(((tid & 1) ? p.beta : p.g) + (size_t(b) * T + t) * H_v + h);
+    if (row) {
+      vt_load_taps(p, b, cq, tq);
+      vt_load_taps(p, b, ck, tk);
+      vt_load_taps(p, b, cv, tv);
+      // warm L2 with this call's x, g and beta lines (a prefetch only: the
+      // values are read after the wait, so a later write by the preceding
+      // kernel is still what they see)
+      if (tid < 6 * T) {
+        const int t = tid / 6, r = tid % 6;  // slabs q, k, v of 128 channels (two 128-byte lines each)
+        const int c0 = (r < 2 ? hk * D : r < 4 ? H_k * D + hk * D : 2 * H_k * D + h * D) + (r & 1) * 64;
+        prefetch_l2(p.x + (size_t(b) * T + t) * p.C + c0);
+      } else if (tid < 8 * T) {
+        const int t = (tid - 6 * T) >> 1;
+        prefetch_l2(((tid & 1) ? p.beta : p.g) + (size_t(b) * T + t) * H_v + h);
+      }
+      find_inactive_neighbours();
     }
     if (kDef && K >= 1 && !apply_and_write()) {
-      if (warp == NTHR / 32 - 1) tmem_dealloc(sc.tmem, kVtTmemCols);
+      if (issuer) tmem_dealloc(sc.tmem, kVtTmemCols);
       give_up();
       return;
     }
@@ -358,32 +433,27 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   } else {
     if (kDef) K = min(p.ws_pend[bh], T);
     stage();
-    vt_load_taps(p, b, cq, tq);
-    vt_load_taps(p, b, ck, tk);
-    vt_load_taps(p, b, cv, tv);
+    if (row) {
+      vt_load_taps(p, b, cq, tq);
+      vt_load_taps(p, b, ck, tk);
+      vt_load_taps(p, b, cv, tv);
+    }
   }
-  // unflagged: the accumulator columns are taken only after the wait (the
-  // preceding kernel may be any kernel, so no tensor memory is held while
-  // waiting for it)
-  if (!p.overlap && warp == NTHR / 32 - 1) tmem_alloc(&sc.tmem, kVtTmemCols);
 
   // ---- conv inputs of this call ------------------------------------------------
   uint16_t xq[T], xk[T], xv[T];
-  vt_load_x<T>(p, b, cq, xq);
-  vt_load_x<T>(p, b, ck, xk);
-  vt_load_x<T>(p, b, cv, xv);
   float gt[T], bt[T];
+  if (row) {
+    vt_load_x<T>(p, b, cq, xq);
+    vt_load_x<T>(p, b, ck, xk);
+    vt_load_x<T>(p, b, cv, xv);
 #pragma unroll
-  for (int t = 0; t < T; ++t) {
-    gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
-    bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
-  }
-  // the inactive rows this CTA zero-fills: those after b up to the next
-  // active row and, when no row below b is active, every row below b
-  {
-    int r_hi = b + 1, r_lo = b - 1;
-    while (r_hi < p.B && !p.active[r_hi]) ++r_hi;
-    while (r_lo >= 0 && !p.active[r_lo]) --r_lo;
+    for (int t = 0; t < T; ++t) {
+      gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
+      bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
+    }
+    // zero-fill of the inactive rows found above
+    if (!p.overlap) find_inactive_neighbours();
     for (int r = b + 1; r < r_hi; ++r)
 #pragma unroll
       for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
@@ -393,51 +463,25 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
         for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
   }
   // DEFERRED, unflagged: the pending commit is applied while the inputs load
-  bool failed = false;
-  if (kDef && !p.overlap && K >= 1) failed = !apply_and_write();
-  if (failed) {
-    if (warp == NTHR / 32 - 1) tmem_dealloc(sc.tmem, kVtTmemCols);
+  if (kDef && !p.overlap && K >= 1 && !apply_and_write()) {
+    if (issuer) tmem_dealloc(sc.tmem, kVtTmemCols);
     give_up();
     return;
   }
-  float yq[T], yk[T], yv[T];
-  vt_conv<T>(tq, xq, p.act, yq);
-  vt_conv<T>(tk, xk, p.act, yk);
-  vt_conv<T>(tv, xv, p.act, yv);
-  unsigned char *bsm = reinterpret_cast<unsigned char *>(sm.B);
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    sm.q[t][i] = yq[t];
-    sm.k[t][i] = yk[t];
-    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(t, i)) = f2tf32(yk[t]);
-    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(T + t, i)) = f2tf32(yq[t]);
-  }
-  // new raw inputs into ring slots 3..2+T: q/k channels by one CTA of the key head
-  if (h % (H_v / H_k) == 0) {
-    vt_store_ring<T>(p, b, cq, xq);
-    vt_store_ring<T>(p, b, ck, xk);
-  }
-  vt_store_ring<T>(p, b, cv, xv);
-  fence_async_smem();  // B is read by the tensor cores
-  tc_fence_before();
-  __syncthreads();  // conv outputs, B and the TMEM address are visible
-  tc_fence_after();
-  const uint32_t tmem = sc.tmem;
 
-  // ---- the products and the per-head coefficients, side by side --------------
-  // The issuing thread stalls while the tensor cores read the 64 KiB tile
-  // (about 0.6 us), so it sits alone in the last warp; the other warps take
-  // the per-head dot products and the recurrence coefficients meanwhile and
-  // meet it at one block barrier.
-  constexpr int NCW = NTHR - 32;  // threads of the coefficient warps
-  if (warp == NTHR / 32 - 1) {
+  if (issuer) {
+    // ---- warp 4: the products D[j][n] = S_0[j] . B[n], as soon as every row
+    // thread has written its B column; then, once every row thread has read
+    // its accumulators, the tensor memory goes back --------------------------
+    const uint32_t tmem = sc.tmem;
     if (lane == 0) {
-      bool ok = true;
+      bool ok = mbar_wait_spin(&sc.bready, 0, wl);
+      int issued = 0;
       constexpr uint32_t idesc = umma_idesc_tf32(D, kVtN);
       const uint32_t sB = smem_u32(sm.B), sS = smem_u32(sm.S);
 #pragma unroll
       for (int c = 0; c < kVtBoxes; ++c) {
-        if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
+        if (!ok || !mbar_wait_limit(&sc.bar[c], 0, wl)) {
           ok = false;
           break;
         }
@@ -448,73 +492,83 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
           const uint64_t da = umma_desc_sw128(sS + c * kVtBoxBytes + kk * 32);
           const uint64_t db = umma_desc(sB + ks * 256, 128, 4096);
           umma_tf32(tmem, da, db, idesc, ks > 0);
+          ++issued;
         }
       }
-      if (!ok) sc.fail = 1;
-      umma_commit(&sc.mbar);  // also arrives when nothing was issued
+      if (ok) {
+        umma_commit(&sc.mbar);
+      } else if (issued) {  // products in flight must finish before the columns go back
+        umma_commit(&sc.fbar);
+        mbar_wait_limit(&sc.fbar, 0, wl);
+      }
     }
     __syncwarp();
-  } else {
-    // per-head dot products of the raw conv outputs, four lanes each
-    constexpr int NQ4 = NCW / 4, F4 = D / 4;
-    const int qd = tid >> 2, ql = tid & 3;
-    for (int r0 = 0; r0 < NV; r0 += NQ4) {  // the same trip count in every lane
-      const int n = r0 + qd;
-      float part = 0.f;
-      if (n < NV) {
-        const float *u, *w;
-        if (n < 2 * T) {
-          u = w = (n & 1) ? sm.k[n >> 1] : sm.q[n >> 1];
-        } else if (n < 2 * T + NKK) {  // k_s . k_t, s < t, t-major
-          int r = n - 2 * T, t = 1;
-          while (r >= t) r -= t, ++t;
-          u = sm.k[r], w = sm.k[t];
-        } else {  // k_s . q_t, s <= t, t-major
-          int r = n - 2 * T - NKK, t = 0;
-          while (r > t) r -= t + 1, ++t;
-          u = sm.k[r], w = sm.q[t];
-        }
+    asm volatile("bar.sync 2, %0;" ::"n"(kVtThreads) : "memory");  // the row threads' TMEM reads are done
+    tc_fence_after();
+    tmem_dealloc(tmem, kVtTmemCols);
+    if (applied && tid == 0) bulk_wait_read_all();
+    return;
+  }
+
+  // ---- warps 0-3: conv, B column, head partial sums, ring -----------------------
+  float yq[T], yk[T], yv[T];
+  vt_conv<T>(tq, xq, p.act, yq);
+  vt_conv<T>(tk, xk, p.act, yk);
+  vt_conv<T>(tv, xv, p.act, yv);
+  unsigned char *bsm = reinterpret_cast<unsigned char *>(sm.B);
 #pragma unroll
-        for (int jj = 0; jj < F4 / 4; ++jj) {
-          const int f = (ql + 4 * (jj + qd)) % F4;
-          part += dot4(*reinterpret_cast<const float4 *>(u + 4 * f), *reinterpret_cast<const float4 *>(w + 4 * f));
-        }
-      }
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      if (n < NV && ql == 0) sc.hraw[n] = part;
-    }
-    if (tid < T) {  // cumulative log-decay G_t = g_0 + ... + g_t, in order
+  for (int t = 0; t < T; ++t) {
+    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(t, i)) = f2tf32(yk[t]);
+    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(T + t, i)) = f2tf32(yq[t]);
+  }
+  fence_async_smem();  // B is read by the tensor cores
+  mbar_arrive(&sc.bready);
+  // this warp's partial sums of the per-head dot products
+  vt_head_partials<T>(yq, yk, lane, sc.hpart[warp]);
+  // new raw inputs into ring slots 3..2+T: q/k channels by one CTA of the key head
+  if (h % (H_v / H_k) == 0) {
+    vt_store_ring<T>(p, b, cq, xq);
+    vt_store_ring<T>(p, b, ck, xk);
+  }
+  vt_store_ring<T>(p, b, cv, xv);
+  asm volatile("bar.sync 1, %0;" ::"n"(NROW) : "memory");  // the partial sums are visible
+
+  // ---- coefficients of the recurrence, one thread each --------------------------
+  {
+    // the head sums (the four warps' partials, in warp order) and the
+    // cumulative log-decays G_t = g_0 + ... + g_t (in order)
+    auto H = [&](int n) { return ((sc.hpart[0][n] + sc.hpart[1][n]) + sc.hpart[2][n]) + sc.hpart[3][n]; };
+    auto Gcum = [&](int t) {
       float a = 0.f;
 #pragma unroll
       for (int u = 0; u < T; ++u)
-        if (u <= tid) a += gt[u];
-      sc.cGc[tid] = a;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(NCW) : "memory");  // the coefficient warps only
-    // coefficients of the recurrence, one thread each
+        if (u <= t) a += gt[u];
+      return a;
+    };
     const float qs = 1.0f / sqrtf(float(D));
-    for (int n = tid; n < T + T * T; n += NCW) {
+    for (int n = tid; n < T + T * T; n += NROW) {
       if (n < T) {
         const int t = n;
-        const float iq = rsqrtf(sc.hraw[2 * t] + kNormEps) * qs, ik = rsqrtf(sc.hraw[2 * t + 1] + kNormEps);
-        const float gm = expf(sc.cGc[t]);
+        const float iq = rsqrtf(H(2 * t) + kNormEps) * qs, ik = rsqrtf(H(2 * t + 1) + kNormEps);
+        const float Gt = Gcum(t);
+        const float gm = expf(Gt);
         sc.cbk[t] = (bt[t] * gm) * ik;
         sc.cgq[t] = gm * iq;
         sc.cinvk[t] = ik;
+        sc.cGc[t] = Gt;
         continue;
       }
       const int t = (n - T) / T, s0 = (n - T) % T;
       if (s0 <= t) {
-        const float ik_s = rsqrtf(sc.hraw[2 * s0 + 1] + kNormEps), ik_t = rsqrtf(sc.hraw[2 * t + 1] + kNormEps);
-        const float iq_t = rsqrtf(sc.hraw[2 * t] + kNormEps) * qs;
-        const float dec = s0 == t ? 1.0f : expf(sc.cGc[t] - sc.cGc[s0]);
-        if (s0 < t) sc.cA[t][s0] = bt[t] * dec * (sc.hraw[2 * T + t * (t - 1) / 2 + s0] * ik_s * ik_t);
-        sc.cQ[t][s0] = dec * (sc.hraw[2 * T + NKK + t * (t + 1) / 2 + s0] * ik_s * iq_t);
+        const float ik_s = rsqrtf(H(2 * s0 + 1) + kNormEps), ik_t = rsqrtf(H(2 * t + 1) + kNormEps);
+        const float iq_t = rsqrtf(H(2 * t) + kNormEps) * qs;
+        const float dec = s0 == t ? 1.0f : expf(Gcum(t) - Gcum(s0));
+        if (s0 < t) sc.cA[t][s0] = bt[t] * dec * (H(2 * T + t * (t - 1) / 2 + s0) * ik_s * ik_t);
+        sc.cQ[t][s0] = dec * (H(2 * T + NKK + t * (t + 1) / 2 + s0) * ik_s * iq_t);
       }
     }
   }
-  __syncthreads();  // coefficients (and a failed issue) are visible
+  asm volatile("bar.sync 1, %0;" ::"n"(NROW) : "memory");  // the coefficients are visible
 
   // ---- row j = tid: its 2T products from TMEM lane j, then the recurrence ------
   const int j = tid;
@@ -525,12 +579,15 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
 #pragma unroll
     for (int t = 0; t < T; ++t) zt[t] = p.gz[((size_t(b) * T + t) * H_v + h) * D + j];
   }
-  const bool late = !mbar_wait_limit(&sc.mbar, 0, wl) || sc.fail;
+  // (the products barrier completes only when all products were issued)
+  const bool late = !mbar_wait_spin(&sc.mbar, 0, wl);
   tc_fence_after();
+  float red[kVtN];
+  if (!late) tmem_ld16(sc.tmem + (uint32_t(32 * warp) << 16), red);
+  tc_fence_before();
+  asm volatile("bar.arrive 2, %0;" ::"n"(kVtThreads) : "memory");  // this thread's TMEM reads are done
   float o[T], e[T];
   if (!late) {
-    float red[kVtN];
-    tmem_ld16(tmem + (uint32_t(32 * warp) << 16), red);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       float acc = fmaf(bt[t], yv[t], -sc.cbk[t] * red[t]);
@@ -555,40 +612,31 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
       for (int t = 0; t < T; ++t) p.ws_k[(bk * T + t) * D + i] = yk[t] * sc.cinvk[t];
     }
     if (tid < T) p.ws_G[bh * kMaxT + tid] = sc.cGc[tid];
-    if (gated) {
+  }
+  if (gated) {
+    // out = o_t / sqrt(mean_j o_t[j]^2 + eps) * w[j] * silu(z_t[j]) over the
+    // head's rows, which the four row warps share
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      float q2 = late ? 0.f : o[t] * o[t];
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, m);
+      if (lane == 0) sc.gsq[t][warp] = q2;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NROW) : "memory");
+    if (!late) {
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        float q2 = o[t] * o[t];
+        float ss = 0.f;
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, m);
-        if (lane == 0) sc.gsq[t][warp] = q2;
+        for (int w = 0; w < NROW / 32; ++w) ss += sc.gsq[t][w];
+        const float rstd = rsqrtf(ss / float(D) + p.geps);
+        p.out[((size_t(b) * T + t) * H_v + h) * D + j] = f2bf(o[t] * rstd * bf2f(wj) * silu_fast(bf2f(zt[t])));
       }
     }
   }
-  // every TMEM read is done before the columns are released
-  tc_fence_before();
-  const bool bad = __syncthreads_or(late);
-  tc_fence_after();
-  if (warp == NTHR / 32 - 1) {
-    if (bad) mbar_wait_limit(&sc.mbar, 0, wl);  // products still running must finish first
-    tmem_dealloc(tmem, kVtTmemCols);
-  }
-  if (bad) {
-    give_up();
-    return;
-  }
-  if (gated) {
-    // out = o_t / sqrt(mean_j o_t[j]^2 + eps) * w[j] * silu(z_t[j])
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      float ss = 0.f;
-#pragma unroll
-      for (int w = 0; w < NTHR / 32; ++w) ss += sc.gsq[t][w];
-      const float rstd = rsqrtf(ss / float(D) + p.geps);
-      p.out[((size_t(b) * T + t) * H_v + h) * D + j] = f2bf(o[t] * rstd * bf2f(wj) * silu_fast(bf2f(zt[t])));
-    }
-  }
-  if (applied && tid == 0) bulk_wait_read_all();
+  if (late) give_up();  // (thread 0 flags it and drains the copies)
+  else if (applied && tid == 0) bulk_wait_read_all();
 }
 
 // Launch one instantiation, raising its dynamic shared-memory limit once per
