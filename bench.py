@@ -13,7 +13,14 @@ the measured GB300 copy peak.
 Inputs are synthetic (seeded ``synth`` draws, x/g/beta from a pool of 16
 cycles, keep[] fresh every cycle) and resident in HBM before timing starts;
 the 480 MiB state stack is larger than the 129 MB L2, so no flush is needed.
-Each cycle is one captured CUDA graph of the C-ABI calls.
+The C-ABI calls of 64 consecutive cycles are captured in one CUDA graph, so
+every kernel follows its predecessor with programmatic dependent launch, across
+cycle boundaries too; the timed region is the replay of those graphs, with no
+event inside it.  The verify's share of a cycle is measured as a marginal cost:
+the same cycles are timed over half the stack, and a layer costs the
+difference per layer.  Beside the headline the default run also times the
+batch/draft sweep (B8/T8, B64/T2, B64/T8) and the chunked prefill of one row
+at L = 4096 and 32768 (--no-extras skips them).
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
         [--mode recompute|snapshot|deferred] [--B 8 --T 2 --layers 30] [--no-cpu-baseline]
@@ -46,8 +53,10 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {
     "commit": ["speculative_decode_gated_gdn_gb300/csrc/commit.cu",
                "speculative_decode_gated_gdn_gb300/csrc/gdn_common.cuh"],
-    "verify": ["speculative_decode_gated_gdn_gb300/csrc/verify.cuh",
+    "verify": ["speculative_decode_gated_gdn_gb300/csrc/verify_tc.cuh",
                "speculative_decode_gated_gdn_gb300/csrc/gdn_common.cuh"],
+    "prefill": ["speculative_decode_gated_gdn_gb300/csrc/prefill.cu",
+                "speculative_decode_gated_gdn_gb300/csrc/gdn_common.cuh"],
 }
 
 
@@ -57,7 +66,7 @@ MODES = {"recompute": 0, "snapshot": 1, "deferred": 2}  # GDN_COMMIT_* of the C 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mode", default="deferred", choices=list(MODES))
@@ -69,6 +78,8 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the batch/draft sweep and the prefill records beside the headline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="cycle", choices=["cycle", "prefill", "accept"],
                     help="cycle: the verify+commit headline; prefill: chunked state priming of one row; "
@@ -308,9 +319,10 @@ def oracle_layer_cycle(orc, geom, st, cy, layer, active, keep):
     return o
 
 
-def run_oracle_sample(geom, inactive, n_layers, seconds, max_layer_cycles=None, seed=2):
-    """Time the oracle on a bounded sample of layer-cycles using all host cores
-    (threads over independent layers; the C oracle runs without the GIL)."""
+def run_oracle_sample(geom, inactive, n_layers, seconds, max_layer_cycles=None, seed=2, cores=None):
+    """Time the oracle on a bounded sample of layer-cycles using `cores` host
+    threads (all host cores by default; threads over independent layers, the C
+    oracle runs without the GIL)."""
     import oracle
     from speculative_decode_gated_gdn_gb300 import synth
     orc = oracle.default()
@@ -319,7 +331,7 @@ def run_oracle_sample(geom, inactive, n_layers, seconds, max_layer_cycles=None, 
     cy = synth.cycle_inputs(geom, seed, 0, sample_layers)
     active = synth.active_mask(geom.B, inactive)
     keep = cy["keep"]
-    cores = os.cpu_count() or 1
+    cores = cores or os.cpu_count() or 1
     done = 0
     t0 = time.perf_counter()
     with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as ex:
@@ -342,10 +354,7 @@ def run_oracle_sample(geom, inactive, n_layers, seconds, max_layer_cycles=None, 
 
 
 # ---------------------------------------------------------------- GPU arm
-def timing_event():
-    """A timing event that records as a graph node when captured."""
-    import torch
-    return torch.cuda.Event(enable_timing=True, external=True)
+CHUNK = 64  # cycles per captured graph (a graph of a few thousand kernel nodes)
 
 
 def verify_mode(mode, layer):
@@ -357,257 +366,347 @@ def verify_mode(mode, layer):
     return mode | (L.GDN_VERIFY_OVERLAP if layer > 0 else 0)
 
 
-def run_gpu(args, rank, world, local):
+class Stack:
+    """Device tensors of one benchmark cohort (n-layer state stack, input pool)
+    and the captured verify+commit cycles."""
+
+    def __init__(self, args, geom, inactive, n_layers, seed, dev, pool=16, keep_cycles=0):
+        import torch
+        from speculative_decode_gated_gdn_gb300 import lib as L
+        from speculative_decode_gated_gdn_gb300 import synth
+        self.L, self.torch, self.args, self.geom, self.n_layers, self.dev = L, torch, args, geom, n_layers, dev
+        self.mode = MODES[args.mode]
+        self.pool = pool
+        self.d = L.dims_of(geom)
+        # the seeded draws of synth, made on the device (the host generator
+        # would take minutes for the larger cohorts)
+        st = synth.layer_state_dev(geom, seed, n_layers, dev)
+        self.st0 = {k: v.clone() for k, v in st.items()}  # the starting point, for restore()
+        self.active_np = synth.active_mask(geom.B, inactive)
+        self.keeps_np = synth.keep_draws(geom, seed, keep_cycles)
+        inp = [synth.cycle_inputs_dev(geom, seed, p, n_layers, dev) for p in range(pool)]
+        self.state, self.ring, self.conv_w, self.offsets = st["state"], st["ring"], st["conv_w"], st["offsets"]
+        self.active = torch.from_numpy(self.active_np).to(dev)
+        self.keeps = torch.from_numpy(self.keeps_np).to(dev)
+        self.ws_bytes = L.gdn_layer_workspace_bytes(self.d, self.mode)
+        self.ws = [torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev) for _ in range(n_layers)]
+        self.out = torch.empty((n_layers, geom.B, geom.T, geom.H_v, geom.d), dtype=torch.bfloat16, device=dev)
+        self.xs = [c["x"] for c in inp]
+        self.gs = [c["g"] for c in inp]
+        self.bs = [c["beta"] for c in inp]
+        self.side = torch.cuda.Stream(device=dev)
+        self.extras = {}
+
+    def bf(self, bits):
+        t = self.torch
+        return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(self.dev).view(t.bfloat16)
+
+    def restore(self):
+        """The starting point of a run: initial state, rings, offsets, zeroed workspaces."""
+        self.state.copy_(self.st0["state"])
+        self.ring.copy_(self.st0["ring"])
+        self.offsets.copy_(self.st0["offsets"])
+        for w in self.ws:
+            w.zero_()
+
+    def cycle(self, c, n_lay=None, x=None, g=None, beta=None, keep=None, out=None):
+        """One verify+commit cycle over the first n_lay layers, issued on the
+        current stream (captured into a graph by the caller)."""
+        L, a = self.L, self.args
+        n = self.n_layers if n_lay is None else n_lay
+        p = c % self.pool
+        x = self.xs[p] if x is None else x
+        g = self.gs[p] if g is None else g
+        beta = self.bs[p] if beta is None else beta
+        keep = self.keeps[c] if keep is None else keep
+        out = self.out if out is None else out
+        for l in range(n):
+            if a.gated:
+                L.gdn_conv_verify_gated(self.d, verify_mode(self.mode, l), x[l], self.conv_w[l], g[l], beta[l],
+                                        self.state[l], self.ring[l], self.offsets, self.active,
+                                        self.extras["zs"][p].view(self.geom.B, self.geom.T, self.geom.H_v,
+                                                                  self.geom.d),
+                                        self.extras["norm_w"], 1e-6, out[l], self.ws[l], self.ws_bytes)
+            else:
+                L.gdn_conv_verify(self.d, verify_mode(self.mode, l), x[l], self.conv_w[l], g[l], beta[l],
+                                  self.state[l], self.ring[l], self.offsets, self.active, out[l], self.ws[l],
+                                  self.ws_bytes)
+        if a.accept:
+            e = self.extras
+            L.gdn_accept_greedy(e["lgs"][p], e["drafts"][c], self.active, e["keep_dev"], e["next_dev"], e["ws_acc"])
+            keep = e["keep_dev"]
+        L.gdn_commit(self.d, self.mode, [self.state[l] for l in range(n)], [self.ring[l] for l in range(n)],
+                     self.ws[:n], keep, self.active, self.offsets)
+
+    def capture(self, cycles, n_lay=None):
+        """Graphs of up to CHUNK consecutive cycles each: every kernel of a chunk
+        follows the previous one with programmatic dependent launch, across the
+        cycle boundaries too."""
+        torch = self.torch
+        graphs = []
+        for c0 in range(0, len(cycles), CHUNK):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=self.side):
+                for c in cycles[c0:c0 + CHUNK]:
+                    self.cycle(c, n_lay)
+            graphs.append(gr)
+        return graphs
+
+    def time_graphs(self, warm, timed, clocks=None):
+        """Replay the warm-up graphs, then time the others with CUDA events on
+        the replay stream (synchronised on both sides); milliseconds."""
+        torch = self.torch
+        self.restore()
+        torch.cuda.synchronize()
+        for g in warm:
+            g.replay()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if clocks:
+            clocks.mark_start()
+        start.record()
+        for g in timed:
+            g.replay()
+        end.record()
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark_end()
+        return start.elapsed_time(end)
+
+
+def cycle_bytes(geom, mode, active_np, keeps_np, W, K, n_layers):
+    """Per-cycle algorithmic bytes of the timed cycles W..W+K-1 (verify, commit,
+    whole step) and the path minimum, from the cycles' actual keep[] and active[]."""
+    n_active = int(active_np.sum())
+    kp_all = np.where(active_np[None, :] == 1, keeps_np, 0)
+    n_keep_all = (kp_all >= 1).sum(axis=1)
+    n_keep = n_keep_all[W:W + K]
+    prev_keep = np.concatenate([[0], n_keep_all])  # DEFERRED: the verify of cycle c applies cycle c-1's commit
+    n_apply = prev_keep[W:W + K] if mode == "deferred" else np.zeros(K, np.int64)
+    commit_alg = np.array([commit_bytes(geom, int(nk), n_layers, mode) for nk in n_keep], dtype=np.float64)
+    verify_alg = np.array([verify_bytes(geom, n_active, mode, int(na)) for na in n_apply], dtype=np.float64)
+    step = commit_alg + n_layers * verify_alg
+    pmin = np.array([path_min_bytes(geom, n_active, int(nk), n_layers) for nk in n_keep], dtype=np.float64)
+    return verify_alg.mean(), commit_alg.mean(), step.mean(), pmin.mean()
+
+
+def measure_cycles(args, geom, inactive, n_layers, K, W, seed, dev, world=1, clocks=None, marginal=True):
+    """Build a cohort, capture W warm-up and K timed cycles in chained graphs
+    and time them; with `marginal`, also time K2 cycles of the first half of
+    the stack, so that a layer's cost is the difference per layer and the
+    commit's the rest.  Returns (Stack, dict of times and bytes)."""
     import torch
-    from speculative_decode_gated_gdn_gb300 import lib as L
+    import torch.distributed as dist
     from speculative_decode_gated_gdn_gb300 import synth
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    geom, inactive = workload(args)
-    n_layers = args.layers
-    mode = MODES[args.mode]
-    seed = rank_seed(args.seed, rank)
-    pool = 16
-    d = L.dims_of(geom)
-    K, W = args.steps, args.warmup
-
-    # persistent stack + input pool, all resident in HBM before timing
-    st = synth.layer_state(geom, seed, n_layers)
-    active_np = synth.active_mask(geom.B, inactive)
-    keeps_np = synth.keep_draws(geom, seed, K + W)
-    inp = [synth.cycle_inputs(geom, seed, p, n_layers) for p in range(pool)]
+    sk = Stack(args, geom, inactive, n_layers, seed, dev, keep_cycles=K + W)
     if args.accept:
         # synthetic logits per pool entry, and per cycle drafts that repeat the
         # targets for the drawn number of positions: greedy acceptance then
         # reproduces the draw (at least 1: position 0 is always kept)
         V = args.V
         lg_bits = [synth.normal_bf16(seed + 7, f"logits{p}", geom.B * geom.T * V).reshape(geom.B, geom.T, V)
-                   for p in range(pool)]
+                   for p in range(sk.pool)]
         tg = [np.argmax(synth.bf16_to_f32(bb), axis=2) for bb in lg_bits]
-        keeps_np = np.maximum(keeps_np, 1).astype(np.int32)
+        sk.keeps_np = np.maximum(sk.keeps_np, 1).astype(np.int32)
         drafts_np = np.zeros((K + W, geom.B, geom.T), np.int32)
         for c in range(K + W):
-            t_p = tg[c % pool]
+            t_p = tg[c % sk.pool]
             for b in range(geom.B):
-                k = int(keeps_np[c, b])
+                k = int(sk.keeps_np[c, b])
                 drafts_np[c, b, 1:k] = t_p[b, :k - 1]
                 if k < geom.T:
                     drafts_np[c, b, k] = (t_p[b, k - 1] + 1) % V
-
-    def bf(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    state = torch.from_numpy(st["state"]).to(dev)
-    ring = bf(st["ring"])
-    conv_w = bf(st["conv_w"])
-    offsets = torch.from_numpy(st["offsets"].copy()).to(dev)
-    active = torch.from_numpy(active_np).to(dev)
-    keeps = torch.from_numpy(keeps_np).to(dev)
-    ws_bytes = L.gdn_layer_workspace_bytes(d, mode)
-    ws = [torch.zeros(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(n_layers)]  # DEFERRED: zeroed
-    out = torch.empty((n_layers, geom.B, geom.T, geom.H_v, geom.d), dtype=torch.bfloat16, device=dev)
-    xs = [bf(c["x"]) for c in inp]
-    gs = [torch.from_numpy(c["g"]).to(dev) for c in inp]
-    bs = [torch.from_numpy(c["beta"]).to(dev) for c in inp]
-    states = [state[l] for l in range(n_layers)]
-    rings = [ring[l] for l in range(n_layers)]
+        sk.extras.update(lgs=[sk.bf(bb) for bb in lg_bits], drafts=torch.from_numpy(drafts_np).to(dev),
+                         keep_dev=torch.zeros(geom.B, dtype=torch.int32, device=dev),
+                         next_dev=torch.zeros(geom.B, dtype=torch.int32, device=dev),
+                         ws_acc=torch.zeros(sk.L.gdn_accept_workspace_bytes(geom.B, geom.T, V), dtype=torch.uint8,
+                                            device=dev))
     if args.gated:
-        zs = [bf(synth.normal_bf16(seed + 11, f"gate{p}", geom.B * geom.T * geom.H_v * geom.d)) for p in range(pool)]
-        norm_w = bf(synth.normal_bf16(seed, "norm_w", geom.d, std=0.5))
-    if args.accept:
-        lgs = [bf(bb) for bb in lg_bits]
-        drafts = torch.from_numpy(drafts_np).to(dev)
-        keep_dev = torch.zeros(geom.B, dtype=torch.int32, device=dev)
-        next_dev = torch.zeros(geom.B, dtype=torch.int32, device=dev)
-        ws_acc = torch.zeros(L.gdn_accept_workspace_bytes(geom.B, geom.T, args.V), dtype=torch.uint8, device=dev)
-
-    def cycle(c, x, g, beta, keep, ev=None):
-        for l in range(n_layers):
-            if args.gated:
-                L.gdn_conv_verify_gated(d, verify_mode(mode, l), x[l], conv_w[l], g[l], beta[l], state[l], ring[l],
-                                        offsets, active, zs[c % pool].view(geom.B, geom.T, geom.H_v, geom.d), norm_w,
-                                        1e-6, out[l], ws[l], ws_bytes)
-            else:
-                L.gdn_conv_verify(d, verify_mode(mode, l), x[l], conv_w[l], g[l], beta[l], state[l], ring[l],
-                                  offsets, active, out[l], ws[l], ws_bytes)
-        if args.accept:
-            L.gdn_accept_greedy(lgs[c % pool], drafts[c], active, keep_dev, next_dev, ws_acc)
-            keep = keep_dev
-        if ev is not None:
-            ev[0].record()
-        L.gdn_commit(d, mode, states, rings, ws, keep, active, offsets)
-        if ev is not None:
-            ev[1].record()
-
-    # one CUDA graph per cycle (distinct keep row and timing events per cycle)
-    side = torch.cuda.Stream(device=dev)
-    graphs, events = [], []
+        sk.extras.update(zs=[sk.bf(synth.normal_bf16(seed + 11, f"gate{p}", geom.B * geom.T * geom.H_v * geom.d))
+                             for p in range(sk.pool)],
+                         norm_w=sk.bf(synth.normal_bf16(seed, "norm_w", geom.d, std=0.5)))
+    # first calls outside capture (per-device library set-up), then the graphs
     torch.cuda.synchronize()
-    with torch.cuda.stream(side):
-        cycle(0, xs[0], gs[0], bs[0], keeps[0])  # first calls outside capture
+    with torch.cuda.stream(sk.side):
+        sk.cycle(0)
     torch.cuda.synchronize()
-    for c in range(K + W):
-        p = c % pool
-        ev = (timing_event(), timing_event())
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=side):
-            cycle(c, xs[p], gs[p], bs[p], keeps[c], ev)
-        graphs.append(gr)
-        events.append(ev)
-    # restore the starting point the capture run disturbed
-    state.copy_(torch.from_numpy(st["state"]).to(dev))
-    ring.copy_(bf(st["ring"]))
-    offsets.copy_(torch.from_numpy(st["offsets"].copy()).to(dev))
-    for w in ws:
-        w.zero_()
-    torch.cuda.synchronize()
-
-    for c in range(W):
-        graphs[c].replay()
-    torch.cuda.synchronize()
-
-    import torch.distributed as dist
+    warm = sk.capture(list(range(W)))
+    timed = sk.capture(list(range(W, W + K)))
+    half = n_layers // 2
+    K2 = min(K, 256)
+    do_half = marginal and half >= 1 and not args.accept
+    warm_h = sk.capture(list(range(W)), half) if do_half else None
+    timed_h = sk.capture(list(range(W, W + K2)), half) if do_half else None
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
+    ms = sk.time_graphs(warm, timed, clocks)
+    if world > 1:
+        dist.barrier()
+    ms = max_over_ranks(ms, dev, world)
+    step_ms = ms / K
+    if do_half:
+        half_ms = sk.time_graphs(warm_h, timed_h) / K2
+        verify_ms = max((step_ms - half_ms) / (n_layers - half), 1e-9)
+        commit_ms = max(step_ms - n_layers * verify_ms, 0.0)
+        split = f"marginal layer cost: (cycle at {n_layers} layers - cycle at {half}) / {n_layers - half}"
+    else:
+        verify_ms, commit_ms, split = step_ms / n_layers, 0.0, "cycle / layers (commit included)"
+    verify_alg, commit_alg, step_alg, min_alg = cycle_bytes(geom, args.mode, sk.active_np, sk.keeps_np, W, K,
+                                                             n_layers)
+    del warm, timed, warm_h, timed_h
+    return sk, {"step_ms": step_ms, "verify_ms": verify_ms, "commit_ms": commit_ms, "split": split,
+                "verify_alg": verify_alg, "commit_alg": commit_alg, "step_alg": step_alg, "min_alg": min_alg}
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    geom, inactive = workload(args)
+    n_layers = args.layers
+    K, W = args.steps, args.warmup
     props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
     dev_id = f"GPU-{uuid}" if uuid is not None else str(local)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev_id) as clk:
-        clk.mark_start()
-        start.record()
-        for c in range(W, W + K):
-            graphs[c].replay()
-        end.record()
-        torch.cuda.synchronize()
-        clk.mark_end()
-    if world > 1:
-        dist.barrier()
-    ms = max_over_ranks(start.elapsed_time(end), dev, world)
-    commit_ms = [events[c][0].elapsed_time(events[c][1]) for c in range(W, W + K)]
-
-    n_active = int(active_np.sum())
-    kp_all = np.where(active_np[None, :] == 1, keeps_np, 0)
-    n_keep_all = (kp_all >= 1).sum(axis=1)
-    n_keep = n_keep_all[W:W + K]
-    # DEFERRED: the verify of cycle c applies the commit of cycle c - 1
-    prev_keep = np.concatenate([[0], n_keep_all])  # [c] = kept rows of cycle c - 1 (none before cycle 0)
-    n_apply = prev_keep[W:W + K] if args.mode == "deferred" else np.zeros(K, np.int64)
-    commit_alg = np.array([commit_bytes(geom, int(nk), n_layers, args.mode) for nk in n_keep], dtype=np.float64)
-    verify_alg = np.array([verify_bytes(geom, n_active, args.mode, int(na)) for na in n_apply], dtype=np.float64)
-    step_bytes = commit_alg + n_layers * verify_alg
-    min_bytes = np.array([path_min_bytes(geom, n_active, int(nk), n_layers) for nk in n_keep], dtype=np.float64)
+        sk, m = measure_cycles(args, geom, inactive, n_layers, K, W, rank_seed(args.seed, rank), dev, world, clk)
+    step_ms, verify_ms = m["step_ms"], m["verify_ms"]
     peak, peak_kind = measured_peak()
-    step_ms = ms / K
-    commit_avg_ms = float(np.mean(commit_ms))
-    verify_avg_ms = max(step_ms - commit_avg_ms, 1e-9) / n_layers
-    commit_gbs = float(commit_alg.mean()) / (commit_avg_ms * 1e-3) / 1e9
-    verify_gbs = float(verify_alg.mean()) / (verify_avg_ms * 1e-3) / 1e9
-    step_gbs = float(step_bytes.mean()) / (step_ms * 1e-3) / 1e9
-    dominant = "commit" if commit_avg_ms >= verify_avg_ms * n_layers else "verify"
+    verify_gbs = m["verify_alg"] / (verify_ms * 1e-3) / 1e9
+    step_gbs = m["step_alg"] / (step_ms * 1e-3) / 1e9
     wl_key = f"B{geom.B}T{geom.T}L{n_layers}{args.mode}"
-    if dominant == "commit":
-        roof = {"kernel": "commit_kernel (grouped over layers)", "bound": "hbm", "achieved": round(commit_gbs, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(commit_gbs / peak, 4),
-                "traffic": profiled_traffic("commit", wl_key), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": float(commit_alg.mean()),
-                "avg_launch_ms": round(commit_avg_ms, 5)}
-    else:
-        roof = {"kernel": "verify_kernel", "bound": "hbm", "achieved": round(verify_gbs, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(verify_gbs / peak, 4),
-                "traffic": profiled_traffic("verify", wl_key), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": float(verify_alg.mean()),
-                "avg_launch_ms": round(verify_avg_ms, 5)}
     res = {
         "metric": METRIC, "value": job_rate(world, geom.B * geom.T, step_ms), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_dict(args, geom, inactive),
-        "hbm": {"step_algorithmic_bytes": float(step_bytes.mean()), "achieved_gbs": round(step_gbs, 1),
+        "hbm": {"step_algorithmic_bytes": m["step_alg"], "achieved_gbs": round(step_gbs, 1),
                 "peak_gbs": peak, "frac": round(step_gbs / peak, 4), "peak_source": peak_kind,
-                "path_min_bytes": float(min_bytes.mean()),
-                "path_min_frac": round(float(min_bytes.mean()) / (step_ms * 1e-3) / 1e9 / peak, 4),
-                "verify_gbs": round(verify_gbs, 1), "verify_avg_ms_incl_gaps": round(verify_avg_ms, 5),
-                "commit_gbs": round(commit_gbs, 1), "commit_avg_ms": round(commit_avg_ms, 5)},
-        "roofline": roof,
+                "path_min_bytes": m["min_alg"],
+                "path_min_frac": round(m["min_alg"] / (step_ms * 1e-3) / 1e9 / peak, 4),
+                "verify_gbs": round(verify_gbs, 1), "verify_ms": round(verify_ms, 5),
+                "commit_ms": round(m["commit_ms"], 5), "split": m["split"]},
+        "roofline": {"kernel": "verify_tc_kernel (d=128)" if geom.d == 128 and args.mode != "snapshot"
+                     else "verify_kernel", "bound": "hbm", "achieved": round(verify_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(verify_gbs / peak, 4),
+                     "traffic": profiled_traffic("verify", wl_key), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": m["verify_alg"], "avg_launch_ms": round(verify_ms, 5),
+                     "launch_duration": m["split"]},
         "gpu_launches": K * (n_layers + 1 + int(args.accept)),
         "clocks": clk.summary(),
     }
-
-    # end to end through the C ABI with host buffers: pinned inputs copied in,
-    # outputs and offsets copied out, every step
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, geom, d, mode, dev, inp, keeps_np, state, ring, conv_w, offsets, active,
-                             ws, ws_bytes, out, states, world)
-    del graphs
+        res["e2e"] = run_e2e(args, sk, world)
+    del sk
+    torch.cuda.empty_cache()
     return res
 
 
-def run_e2e(args, geom, d, mode, dev, inp, keeps_np, state, ring, conv_w, offsets, active, ws, ws_bytes, out,
-            states, world):
+SWEEP = [(8, 8), (64, 2), (64, 8)]  # (B, T) of the batch/draft sweep beside the headline
+
+
+def run_sweep(args, dev):
+    """The batch/draft sweep (30 layers, the last B/4 rows inactive, keep ~
+    U{0..T}) at a few cohorts, each timed like the headline but shorter."""
+    import copy
     import torch
-    from speculative_decode_gated_gdn_gb300 import lib as L
-    n_layers = args.layers
+    from speculative_decode_gated_gdn_gb300 import synth
+    out = []
+    peak, peak_kind = measured_peak()
+    for B, T in SWEEP:
+        a = copy.copy(args)
+        a.B, a.T, a.gated, a.accept, a.inactive = B, T, False, False, None
+        geom, inactive = workload(a)
+        sk, m = measure_cycles(a, geom, inactive, a.layers, 64, 4, a.seed, dev)
+        del sk
+        torch.cuda.empty_cache()
+        out.append({"B": B, "T": T, "layers": a.layers, "row_tokens_per_s": round(B * T / (m["step_ms"] * 1e-3), 1),
+                    "ms_per_cycle": round(m["step_ms"], 5), "verify_us": round(m["verify_ms"] * 1e3, 3),
+                    "verify_hbm_frac": round(m["verify_alg"] / (m["verify_ms"] * 1e-3) / 1e9 / peak, 4),
+                    "path_min_frac": round(m["min_alg"] / (m["step_ms"] * 1e-3) / 1e9 / peak, 4),
+                    "inactive_rows": list(inactive)})
+    return {"cycles": 64, "mode": args.mode, "peak_gbs": peak, "peak_source": peak_kind, "entries": out}
+
+
+def run_e2e(args, sk, world):
+    """The same cycles through the C ABI with host buffers: every step copies its
+    x/g/beta/keep in from pinned host memory and its outputs and offsets out,
+    inside the timed region.  Inputs and outputs are double-buffered on the
+    device and the copies run on a copy stream, ordered by events against the
+    compute, so step c+1's copy-in and step c-1's copy-out overlap step c."""
+    import torch
+    geom, n_layers = sk.geom, sk.n_layers
     K, W = args.steps, args.warmup
-    pool = len(inp)
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    hx = [pin(c["x"].view(np.int16)) for c in inp]
-    hg = [pin(c["g"]) for c in inp]
-    hb = [pin(c["beta"]) for c in inp]
-    hk = pin(keeps_np)
-    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-    hoff = torch.empty(offsets.shape, dtype=torch.int32).pin_memory()
-    dx = torch.empty(hx[0].shape, dtype=torch.int16, device=dev)
-    dg = torch.empty(hg[0].shape, dtype=torch.float32, device=dev)
-    db = torch.empty(hb[0].shape, dtype=torch.float32, device=dev)
-    dk = torch.empty((geom.B,), dtype=torch.int32, device=dev)
-    dxb = dx.view(torch.bfloat16)
+    dev = sk.dev
+    pin = lambda t: t.cpu().pin_memory()
+    hx = [pin(x.view(torch.int16)) for x in sk.xs]
+    hg = [pin(g) for g in sk.gs]
+    hb = [pin(b) for b in sk.bs]
+    hk = torch.from_numpy(np.ascontiguousarray(sk.keeps_np)).pin_memory()
+    hout = [torch.empty(sk.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    hoff = [torch.empty(sk.offsets.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
+    dx = [torch.empty(hx[0].shape, dtype=torch.int16, device=dev) for _ in range(2)]
+    dg = [torch.empty(hg[0].shape, dtype=torch.float32, device=dev) for _ in range(2)]
+    db = [torch.empty(hb[0].shape, dtype=torch.float32, device=dev) for _ in range(2)]
+    dk = [torch.empty((geom.B,), dtype=torch.int32, device=dev) for _ in range(2)]
+    dout = [torch.empty_like(sk.out) for _ in range(2)]
+    doff = [torch.empty_like(sk.offsets) for _ in range(2)]
+    h2d_s = torch.cuda.Stream(device=dev)  # copies in
+    d2h_s = torch.cuda.Stream(device=dev)  # copies out
 
-    def step(c):
-        p = c % pool
-        dx.copy_(hx[p], non_blocking=True)
-        dg.copy_(hg[p], non_blocking=True)
-        db.copy_(hb[p], non_blocking=True)
-        dk.copy_(hk[c], non_blocking=True)
-        for l in range(n_layers):
-            L.gdn_conv_verify(d, verify_mode(mode, l), dxb[l], conv_w[l], dg[l], db[l], state[l], ring[l],
-                              offsets, active, out[l], ws[l], ws_bytes)
-        L.gdn_commit(d, mode, states, [ring[l] for l in range(n_layers)], ws, dk, active, offsets)
-        hout.copy_(out, non_blocking=True)
-        hoff.copy_(offsets, non_blocking=True)
+    def steps(cycles):
+        """Steps of `cycles`, captured on sk.side (compute), h2d_s and d2h_s."""
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        fresh = [True, True]
+        h2d_s.wait_stream(sk.side)  # bring both copy streams into the capture
+        d2h_s.wait_stream(sk.side)
+        for c in cycles:
+            s, p = c % 2, c % sk.pool
+            # copy-in of step c into buffer s once step c-2's compute is done with it
+            if not fresh[s]:
+                h2d_s.wait_event(ev_done[s])
+            with torch.cuda.stream(h2d_s):
+                dx[s].copy_(hx[p], non_blocking=True)
+                dg[s].copy_(hg[p], non_blocking=True)
+                db[s].copy_(hb[p], non_blocking=True)
+                dk[s].copy_(hk[c], non_blocking=True)
+            ev_in[s].record(h2d_s)
+            # compute of step c: its inputs are in, and step c-2's outputs are out
+            sk.side.wait_event(ev_in[s])
+            if not fresh[s]:
+                sk.side.wait_event(ev_out[s])
+            with torch.cuda.stream(sk.side):
+                sk.cycle(c, None, dx[s].view(torch.bfloat16), dg[s], db[s], dk[s], dout[s])
+                doff[s].copy_(sk.offsets)
+            ev_done[s].record(sk.side)
+            # copy-out of step c
+            d2h_s.wait_event(ev_done[s])
+            with torch.cuda.stream(d2h_s):
+                hout[s].copy_(dout[s], non_blocking=True)
+                hoff[s].copy_(doff[s], non_blocking=True)
+            ev_out[s].record(d2h_s)
+            fresh[s] = False
+        sk.side.wait_stream(h2d_s)  # join
+        sk.side.wait_stream(d2h_s)
 
-    side = torch.cuda.Stream(device=dev)
     graphs = []
     torch.cuda.synchronize()
-    with torch.cuda.stream(side):
-        step(0)
-    torch.cuda.synchronize()
-    for c in range(K + W):
+    for cyc in ([list(range(W))] + [list(range(W + c0, min(W + K, W + c0 + CHUNK))) for c0 in range(0, K, CHUNK)]):
         gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=side):
-            step(c)
+        with torch.cuda.graph(gr, stream=sk.side):
+            steps(cyc)
         graphs.append(gr)
-    for c in range(W):
-        graphs[c].replay()
-    torch.cuda.synchronize()
-    import torch.distributed as dist
-    if world > 1:
-        dist.barrier()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for c in range(W, W + K):
-        graphs[c].replay()
-    end.record()
-    torch.cuda.synchronize()
-    ms = max_over_ranks(start.elapsed_time(end), dev, world)
+    ms = sk.time_graphs(graphs[:1], graphs[1:])
+    ms = max_over_ranks(ms, dev, world)
     h2d = hx[0].numel() * 2 + hg[0].numel() * 4 + hb[0].numel() * 4 + geom.B * 4
-    d2h = hout.numel() * 2 + hoff.numel() * 4
+    d2h = hout[0].numel() * 2 + hoff[0].numel() * 4
     return {"value": job_rate(world, geom.B * geom.T, ms / K), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / K,
             "how": "per step: pinned-host x/g/beta/keep copied in, 30 verifies + grouped commit through the C ABI, "
-                   "outputs and offsets copied out; one CUDA graph per step"}
+                   "outputs and offsets copied out; inputs/outputs double-buffered, copies on a second stream "
+                   "ordered by events so they overlap the neighbouring steps' compute; CUDA graphs of 64 steps"}
 
 
 # ---------------------------------------------------------------- prefill leg
@@ -675,18 +774,16 @@ def run_accept_bench(args, rank, world, local):
             "gpu_launches": K}
 
 
-def run_prefill_bench(args, rank, world, local):
-    """Time gdn_prefill_chunked: B rows primed over L tokens per step."""
+def measure_prefill(L_prompt, K, W, seed, dev):
+    """Time gdn_prefill_chunked priming one row (B = 1) over L_prompt tokens:
+    milliseconds per call and the algorithmic work."""
     import torch
     from speculative_decode_gated_gdn_gb300 import lib as L
     from speculative_decode_gated_gdn_gb300 import synth
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    geom = synth.Geometry(B=args.B if args.B != 8 else 1, T=2, H_k=16, H_v=32, d=128)
-    Lp, K, W = args.L, args.steps, args.warmup
+    geom = synth.Geometry(B=1, T=2, H_k=16, H_v=32, d=128)
     d = L.dims_of(geom)
-    pr = synth.prompt_inputs(geom, rank_seed(args.seed, rank), Lp)
-    st = synth.layer_state(geom, rank_seed(args.seed, rank), 1, offsets=np.zeros(geom.B, np.int32))
+    pr = synth.prompt_inputs(geom, seed, L_prompt)
+    st = synth.layer_state(geom, seed, 1, offsets=np.zeros(geom.B, np.int32))
 
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -696,11 +793,11 @@ def run_prefill_bench(args, rank, world, local):
     state = torch.zeros((geom.B, geom.H_v, geom.d, geom.d), dtype=torch.float32, device=dev)
     ring = torch.zeros((geom.B, geom.R, geom.C), dtype=torch.bfloat16, device=dev)
     offsets = torch.zeros(geom.B, dtype=torch.int32, device=dev)
-    out = torch.empty((geom.B, Lp, geom.H_v, geom.d), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(L.gdn_prefill_workspace_bytes(d, Lp), dtype=torch.uint8, device=dev)
+    out = torch.empty((geom.B, L_prompt, geom.H_v, geom.d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.gdn_prefill_workspace_bytes(d, L_prompt), dtype=torch.uint8, device=dev)
 
     def step():
-        L.gdn_prefill_chunked(d, Lp, x, w, g, beta, state, ring, offsets, out, ws)
+        L.gdn_prefill_chunked(d, L_prompt, x, w, g, beta, state, ring, offsets, out, ws)
 
     for _ in range(W):
         step()
@@ -711,17 +808,74 @@ def run_prefill_bench(args, rank, world, local):
         step()
     end.record()
     torch.cuda.synchronize()
-    ms = max_over_ranks(start.elapsed_time(end), dev, world) / K
-    flops = prefill_flops(Lp, geom.H_v, geom.d) * geom.B
-    hbm = geom.B * (Lp * geom.C * 2 + Lp * geom.H_v * geom.d * 2 + 2 * geom.H_v * geom.d * geom.d * 4
-                    + 2 * Lp * geom.H_v * 4)
-    return {"metric": "GDN chunked prefill prompt tokens/s", "value": job_rate(world, geom.B * Lp, ms),
-            "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms,
+    ms = start.elapsed_time(end) / K
+    flops = prefill_flops(L_prompt, geom.H_v, geom.d) * geom.B
+    hbm = geom.B * (L_prompt * geom.C * 2 + L_prompt * geom.H_v * geom.d * 2 + 2 * geom.H_v * geom.d * geom.d * 4
+                    + 2 * L_prompt * geom.H_v * 4)
+    del x, w, g, beta, state, ring, out, ws
+    torch.cuda.empty_cache()
+    return ms, flops, hbm, geom
+
+
+def measured_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops_sustained"]), float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return 1700.0, 1900.0, "fallback"
+
+
+def prefill_record(args, dev):
+    """Chunked prefill of one row at L = 4096 and 32768 (the state-priming
+    configuration), with the tensor-pipe utilisation of its kernels from the
+    committed ncu summary when that was taken on the current source."""
+    sust, burst, kind = measured_tflops()
+    entries = []
+    for L_prompt, K, W in ((4096, 20, 3), (32768, 4, 1)):
+        ms, flops, hbm, _ = measure_prefill(L_prompt, K, W, args.seed, dev)
+        tf = flops / (ms * 1e-3) / 1e12
+        entries.append({"L": L_prompt, "ms": round(ms, 4), "tokens_per_s": round(L_prompt / (ms * 1e-3), 1),
+                        "algorithmic_gflop": round(flops / 1e9, 2), "achieved_tflops": round(tf, 2),
+                        "frac_of_bf16_sustained": round(tf / sust, 4),
+                        "hbm_gb_per_s": round(hbm / (ms * 1e-3) / 1e9, 1)})
+    return {"B": 1, "chunk": 64, "peak_bf16_tflops_sustained": sust, "peak_source": kind,
+            "tensor_pipe": profiled_tensor_pipe(), "entries": entries}
+
+
+def profiled_tensor_pipe():
+    """sm__pipe_tensor_cycles_active per prefill kernel from profiles/traffic.json,
+    if taken on the current prefill source (null otherwise)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)["prefill"]
+    except Exception:
+        return None
+    if rec.get("source_hash") != source_hash("prefill"):
+        return None
+    return rec.get("tensor_pipe")
+
+
+def run_prefill_bench(args, rank, world, local):
+    """Time gdn_prefill_chunked: B rows primed over L tokens per step."""
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ms, flops, hbm, geom = measure_prefill(args.L, args.steps, args.warmup, rank_seed(args.seed, rank), dev)
+    ms = max_over_ranks(ms, dev, world)
+    sust, burst, kind = measured_tflops()
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"metric": "GDN chunked prefill prompt tokens/s", "value": job_rate(world, geom.B * args.L, ms),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"chunked prefill B={geom.B} L={Lp} H_k=16 H_v=32 d=128 chunk 64",
-                       "B": geom.B, "L": Lp},
-            "algorithmic_gflop_per_step": flops / 1e9, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
-            "algorithmic_hbm_mb_per_step": hbm / 1e6, "achieved_hbm_gbs": hbm / (ms * 1e-3) / 1e9}
+            "config": {"workload": f"chunked prefill B={geom.B} L={args.L} H_k=16 H_v=32 d=128 chunk 64",
+                       "B": geom.B, "L": args.L},
+            "algorithmic_gflop_per_step": flops / 1e9, "achieved_tflops": tf,
+            "frac_of_bf16_sustained": tf / sust, "peak_source": kind,
+            "algorithmic_hbm_mb_per_step": hbm / 1e6, "achieved_hbm_gbs": hbm / (ms * 1e-3) / 1e9,
+            "tensor_pipe": profiled_tensor_pipe()}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -789,10 +943,18 @@ def main():
             print(json.dumps(res), flush=True)
         return
     res = run_gpu(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_extras:
+        import torch
+        dev = torch.device("cuda", local)
+        res["sweep"] = run_sweep(args, dev)
+        res["prefill"] = prefill_record(args, dev)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             geom, inactive = workload(args)
             res["cpu_baseline"] = run_oracle_sample(geom, inactive, args.layers, args.cpu_seconds)
+            one = run_oracle_sample(geom, inactive, args.layers, args.cpu_seconds / 3, cores=1)
+            res["cpu_baseline"]["single_core"] = {k: one[k] for k in ("value", "unit", "cores", "sample",
+                                                                      "seconds_per_cycle")}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -215,3 +215,92 @@ def keep_draws(geom: Geometry, seed: int, n_cycles: int) -> np.ndarray:
     mod pool size) but re-draw keep every cycle from this stream.
     """
     return integers(seed, "keeps", (n_cycles, geom.B), 0, geom.T + 1)
+
+
+# ---------------------------------------------------------------------------
+# The same streams drawn with torch on a device, for workloads too large to
+# draw on the host in reasonable time (benchmark cohorts of many rows and
+# layers).  Integer parts are bit-identical to the numpy generator (int64
+# wrap-around arithmetic and logical shifts reproduce the uint64 steps); the
+# Box-Muller floats can differ from the host's in the last ulp of log/cos,
+# which after rounding to bf16 or fp32 changes a value only in rare ties.
+# ---------------------------------------------------------------------------
+def _i64(u: int) -> int:
+    """A 64-bit pattern as a signed int64 value."""
+    return u - (1 << 64) if u >= (1 << 63) else u
+
+
+_GOLDEN_I = _i64(int(_GOLDEN))
+_M1_I = _i64(int(_M1))
+_M2_I = _i64(int(_M2))
+_DBLOCK = 1 << 24  # values drawn per device block
+
+
+def _lsr(z, s: int):
+    return (z >> s) & ((1 << (64 - s)) - 1)
+
+
+def _mix64_t(z):
+    z = (z ^ _lsr(z, 30)) * _M1_I
+    z = (z ^ _lsr(z, 27)) * _M2_I
+    return z ^ _lsr(z, 31)
+
+
+def uniform_dev(seed: int, name: str, n: int, start: int, device):
+    """uniform() as a float64 torch tensor on `device`."""
+    import torch
+    key = _i64(int(_key(seed, name)))
+    i = torch.arange(start + 1, start + n + 1, dtype=torch.int64, device=device)
+    z = _mix64_t(i * _GOLDEN_I + key)
+    return (_lsr(z, 11).to(torch.float64) + 0.5) * (1.0 / 9007199254740992.0)
+
+
+def normal_dev(seed: int, name: str, shape, std: float = 1.0, device="cpu", dtype=None):
+    """normal() as a torch tensor on `device` (float64, or `dtype` after rounding)."""
+    import torch
+    n = int(np.prod(shape))
+    out = torch.empty(n, dtype=dtype or torch.float64, device=device)
+    for s0 in range(0, n, _DBLOCK):
+        m = min(_DBLOCK, n - s0)
+        u = uniform_dev(seed, name, 2 * m, 2 * s0, device)
+        v = std * torch.sqrt(-2.0 * torch.log(u[0::2])) * torch.cos(2.0 * np.pi * u[1::2])
+        out[s0:s0 + m] = v.to(out.dtype)
+    return out.reshape(shape)
+
+
+def integers_dev(seed: int, name: str, shape, lo: int, hi: int, device="cpu"):
+    import torch
+    n = int(np.prod(shape))
+    u = uniform_dev(seed, name, n, 0, device)
+    return (lo + torch.floor(u * (hi - lo))).to(torch.int32).reshape(shape)
+
+
+def layer_state_dev(geom: Geometry, seed: int, n_layers: int, device, offsets=None) -> dict:
+    """layer_state() drawn on `device`: torch tensors conv_w / ring as bfloat16,
+    state float32, offsets int32."""
+    import torch
+    g = geom
+    w = normal_dev(seed, "conv_w", (n_layers, g.C, g.width), 0.5, device, torch.bfloat16)
+    s0 = normal_dev(seed, "state", (n_layers, g.B, g.H_v, g.d, g.d), 0.1, device, torch.float32)
+    if offsets is None:
+        offsets = integers_dev(seed, "offsets", (g.B,), 3, 1000, device)
+    else:
+        offsets = torch.as_tensor(np.asarray(offsets, dtype=np.int32)).to(device)
+    ring = torch.full((n_layers, g.B, g.R, g.C), float("nan"), dtype=torch.bfloat16, device=device)
+    ring[:, :, : g.width - 1, :] = normal_dev(seed, "window", (n_layers, g.B, g.width - 1, g.C), 1.0, device,
+                                              torch.bfloat16)
+    return {"conv_w": w, "state": s0, "ring": ring, "offsets": offsets}
+
+
+def cycle_inputs_dev(geom: Geometry, seed: int, cycle: int, n_layers: int, device) -> dict:
+    """cycle_inputs() drawn on `device` (x bfloat16, g and beta float32, keep int32)."""
+    import torch
+    g = geom
+    tag = f"c{cycle}"
+    x = normal_dev(seed, "x" + tag, (n_layers, g.B, g.T, g.C), 1.0, device, torch.bfloat16)
+    gz = normal_dev(seed, "g" + tag, (n_layers, g.B, g.T, g.H_v), 1.0, device)
+    gl = (-torch.nn.functional.softplus(gz) * 0.5).to(torch.float32)
+    bz = normal_dev(seed, "beta" + tag, (n_layers, g.B, g.T, g.H_v), 1.0, device)
+    beta = (1.0 / (1.0 + torch.exp(-bz))).to(torch.float32)
+    keep = integers_dev(seed, "keep" + tag, (g.B,), 0, g.T + 1, device)
+    return {"x": x, "g": gl, "beta": beta, "keep": keep}

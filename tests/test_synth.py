@@ -72,3 +72,25 @@ def test_uniform_maps_the_top_53_bits_into_the_open_interval():
         z = synth._mix64(key + i * synth._GOLDEN)
     assert np.array_equal(u, ((z >> np.uint64(11)).astype(np.float64) + 0.5) / 2.0 ** 53)
     assert (u > 0).all() and (u < 1).all()
+
+
+def test_device_draws_match_host_generator():
+    """The torch (device) form of the generator reproduces the host streams:
+    integers and bf16 patterns bit for bit, fp32 values exactly here (same
+    libm on one host), fp64 normals to the last ulp."""
+    import torch
+    u = synth.uniform(3, "abc", 1000, 17)
+    assert np.array_equal(u, synth.uniform_dev(3, "abc", 1000, 17, "cpu").numpy())
+    n = synth.normal(5, "state", (3, 700), 0.1)
+    assert np.abs(n - synth.normal_dev(5, "state", (3, 700), 0.1, "cpu").numpy()).max() <= 1e-15
+    g = synth.Geometry(B=2, T=3, H_k=2, H_v=4, d=32, T_max=4)
+    a, b = synth.layer_state(g, 2, 2), synth.layer_state_dev(g, 2, 2, "cpu")
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(a["conv_w"], bits(b["conv_w"]))
+    assert np.array_equal(a["ring"], bits(b["ring"]))
+    assert np.array_equal(a["state"], b["state"].numpy())
+    assert np.array_equal(a["offsets"], b["offsets"].numpy())
+    c, d = synth.cycle_inputs(g, 2, 3, 2), synth.cycle_inputs_dev(g, 2, 3, 2, "cpu")
+    assert np.array_equal(c["x"], bits(d["x"]))
+    assert np.array_equal(c["g"], d["g"].numpy()) and np.array_equal(c["beta"], d["beta"].numpy())
+    assert np.array_equal(c["keep"], d["keep"].numpy())
