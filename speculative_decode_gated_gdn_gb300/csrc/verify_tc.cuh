@@ -162,37 +162,52 @@ __device__ __forceinline__ void vt_store_ring(const VerifyParams &p, int b, int 
   for (int t = 0; t < T; ++t) rb[size_t(kNewSlot + t) * p.C] = x[t];
 }
 
-// Product n of the per-head dot products for one channel's conv outputs:
-// n < 2T: |q_{n/2}|^2 (n even), |k_{n/2}|^2 (n odd); then k_s.k_t (s < t),
-// then k_s.q_t (s <= t), both t-major.
-template <int T>
-__device__ __forceinline__ float vt_head_term(int n, const float (&yq)[T], const float (&yk)[T]) {
-  constexpr int NKK = T * (T - 1) / 2;
-  if (n < 2 * T) return (n & 1) ? yk[n >> 1] * yk[n >> 1] : yq[n >> 1] * yq[n >> 1];
-  if (n < 2 * T + NKK) {
-    int r = n - 2 * T, t = 1;
-    while (r >= t) r -= t, ++t;
-    return yk[r] * yk[t];
+// The products of one round (r0 .. r0+W-1) of the per-head dot products for
+// one channel's conv outputs, in the order n: |q_t|^2, |k_t|^2 (t = 0..T-1,
+// interleaved); k_s.k_t (s < t, t-major); k_s.q_t (s <= t, t-major).  Every
+// loop is unrolled, so n is a compile-time constant and yq, yk stay in
+// registers.
+template <int T, int W>
+__device__ __forceinline__ void vt_head_round(int r0, const float (&yq)[T], const float (&yk)[T], float (&v)[W]) {
+  int n = 0;
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    if (n >= r0 && n < r0 + W) v[n - r0] = yq[t] * yq[t];
+    ++n;
+    if (n >= r0 && n < r0 + W) v[n - r0] = yk[t] * yk[t];
+    ++n;
   }
-  int r = n - 2 * T - NKK, t = 0;
-  while (r > t) r -= t + 1, ++t;
-  return yk[r] * yq[t];
+#pragma unroll
+  for (int t = 1; t < T; ++t)
+#pragma unroll
+    for (int s0 = 0; s0 < t; ++s0) {
+      if (n >= r0 && n < r0 + W) v[n - r0] = yk[s0] * yk[t];
+      ++n;
+    }
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+#pragma unroll
+    for (int s0 = 0; s0 <= t; ++s0) {
+      if (n >= r0 && n < r0 + W) v[n - r0] = yk[s0] * yq[t];
+      ++n;
+    }
 }
 
 // Sums of the per-head products over the warp's 32 channels: rounds of W <= 32
 // products, a reduce-scatter butterfly (masks 16, 8, .., 32/W) then plain
-// butterfly sums; afterwards lane l holds product 32 r + (l >> log2(32/W)),
+// butterfly sums; afterwards lane l holds product r0 + (l >> log2(32/W)),
 // and the first lane of each such group writes it to part[].
 template <int T>
 __device__ __forceinline__ void vt_head_partials(const float (&yq)[T], const float (&yk)[T], int lane, float *part) {
   constexpr int NV = 2 * T + T * (T - 1) / 2 + T * (T + 1) / 2;
-  constexpr int W = NV >= 32 ? 32 : NV > 16 ? 32 : NV > 8 ? 16 : NV > 4 ? 8 : NV > 2 ? 4 : 2;
+  constexpr int W = NV > 16 ? 32 : NV > 8 ? 16 : NV > 4 ? 8 : NV > 2 ? 4 : 2;
   constexpr int SH = W == 32 ? 0 : W == 16 ? 1 : W == 8 ? 2 : W == 4 ? 3 : 4;  // log2(32 / W)
 #pragma unroll
   for (int r0 = 0; r0 < NV; r0 += W) {
     float v[W];
 #pragma unroll
-    for (int m = 0; m < W; ++m) v[m] = r0 + m < NV ? vt_head_term<T>(r0 + m, yq, yk) : 0.f;
+    for (int m = 0; m < W; ++m) v[m] = 0.f;
+    vt_head_round<T, W>(r0, yq, yk, v);
 #pragma unroll
     for (int half = W / 2, mask = 16; half >= 1; half >>= 1, mask >>= 1) {
       const bool upper = (lane & mask) != 0;
@@ -545,6 +560,13 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
         if (u <= t) a += gt[u];
       return a;
     };
+    auto beta_of = [&](int t) {  // bt[t] for a run-time t, kept in registers
+      float r = 0.f;
+#pragma unroll
+      for (int u = 0; u < T; ++u)
+        if (u == t) r = bt[u];
+      return r;
+    };
     const float qs = 1.0f / sqrtf(float(D));
     for (int n = tid; n < T + T * T; n += NROW) {
       if (n < T) {
@@ -552,7 +574,7 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
         const float iq = rsqrtf(H(2 * t) + kNormEps) * qs, ik = rsqrtf(H(2 * t + 1) + kNormEps);
         const float Gt = Gcum(t);
         const float gm = expf(Gt);
-        sc.cbk[t] = (bt[t] * gm) * ik;
+        sc.cbk[t] = (beta_of(t) * gm) * ik;
         sc.cgq[t] = gm * iq;
         sc.cinvk[t] = ik;
         sc.cGc[t] = Gt;
@@ -563,7 +585,7 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
         const float ik_s = rsqrtf(H(2 * s0 + 1) + kNormEps), ik_t = rsqrtf(H(2 * t + 1) + kNormEps);
         const float iq_t = rsqrtf(H(2 * t) + kNormEps) * qs;
         const float dec = s0 == t ? 1.0f : expf(Gcum(t) - Gcum(s0));
-        if (s0 < t) sc.cA[t][s0] = bt[t] * dec * (H(2 * T + t * (t - 1) / 2 + s0) * ik_s * ik_t);
+        if (s0 < t) sc.cA[t][s0] = beta_of(t) * dec * (H(2 * T + t * (t - 1) / 2 + s0) * ik_s * ik_t);
         sc.cQ[t][s0] = dec * (H(2 * T + NKK + t * (t + 1) / 2 + s0) * ik_s * iq_t);
       }
     }
