@@ -77,11 +77,14 @@
  * H_v % H_k == 0; B <= 65535; H_v <= 65535.
  *
  * Numerics: the state and all arithmetic are fp32; bf16 appears only in the
- * inputs and outputs.  At d = 128 with T >= 5 (RECOMPUTE and DEFERRED) the
- * verify takes the dot products of the state rows with q_t and k_t on the
- * tensor cores, from bf16 hi/lo splits of both operands (about 2^-14 of each
- * term's magnitude); its results differ from the CUDA-core path's only by
- * rounding.
+ * inputs and outputs.  At d = 128 in RECOMPUTE and DEFERRED mode the verify
+ * takes the dot products of the state rows with q_t and k_t on the tensor
+ * cores in tf32 (the state read truncated to tf32, q and k rounded to it:
+ * about 2^-11 of each term's magnitude); these products only enter e_t and
+ * o_t, and every state update, conv, norm, gate and recurrence step stays in
+ * fp32.  Its results differ from the CUDA-core path's (d = 32, 64, SNAPSHOT)
+ * only by rounding.  The d = 128 tensor-core verify addresses the state as
+ * B * H_v * d_v rows of a tensor map, so it needs B * H_v * 128 < 2^31.
  */
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
@@ -127,26 +130,34 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
  * the library is launched with programmatic dependent launch and waits for
  * the preceding kernel on the stream before reading anything it may write.
  * With GDN_VERIFY_OVERLAP the call's kernel also lets the next kernel on the
- * stream start as soon as it has started, and stages its own state tiles
- * before waiting for its predecessor, so consecutive flagged verifies stream
- * their state ahead of one another; in DEFERRED mode it also fetches the
- * captures of the layer's previous verify and applies a pending commit (and
- * writes it back) before that wait.  The caller guarantees that no work
- * issued since the last library call made WITHOUT the flag writes this
- * call's `state`, `active` or `layer_ws`, and that the previous verify of
- * this layer was issued before that call.  In a verify cycle over a layer
- * stack that means: flag every layer but the first one after a gdn_commit
- * (any mode), gdn_prefill_chunked, gdn_flush or any other write of these
- * buffers.  Never flag a repeated verify of the same layer.  It is always
- * safe to omit. */
+ * stream start as soon as it has started, and before waiting for its
+ * predecessor it stages its own state tiles, reads its conv taps, committed
+ * conv window (ring slots 0..2) and active mask, and warms L2 with its x, g
+ * and beta (a prefetch only; those values are read after the wait), so
+ * consecutive flagged verifies stream their state ahead of one another; in
+ * DEFERRED mode it also fetches the captures of the layer's previous verify
+ * and applies a pending commit (and writes it back) before that wait.  The
+ * caller guarantees that no work issued since the last library call made
+ * WITHOUT the flag writes this call's `state`, `conv_w`, ring slots 0..2,
+ * `active` or `layer_ws`, and that the previous verify of this layer was
+ * issued before that call.  In a verify cycle over a layer stack that means:
+ * flag every layer but the first one after a gdn_commit (any mode),
+ * gdn_prefill_chunked, gdn_flush, gdn_move_rows or any other write of these
+ * buffers.  Never flag a repeated verify of the same layer.  At d = 128 a
+ * flagged verify also takes 32 tensor-memory columns per CTA before that
+ * wait; so the kernel that precedes it on the stream must not be one that,
+ * after letting its dependents start, allocates tensor memory and needs more
+ * than 416 of an SM's 512 columns (no kernel of this library does).  It is
+ * always safe to omit. */
 #define GDN_VERIFY_OVERLAP 0x100
 
 /* sticky device status bits (gdn_get_status) */
 #define GDN_STATUS_BAD_KEEP 1u /* an active row passed keep outside [0, T];
                                   that row was committed with keep = 0 */
 #define GDN_STATUS_TIMEOUT 2u  /* a kernel gave up waiting for one of its own
-                                  bulk copies (bounded wait); its outputs for
-                                  that tile were not written */
+                                  bulk copies or products (bounded wait); it
+                                  wrote no output, capture or state for that
+                                  (row, head) after the wait */
 #define GDN_STATUS_BAD_ROW 4u  /* gdn_move_rows got a row index outside its
                                   cohort; that pair was not copied */
 
@@ -164,24 +175,40 @@ typedef struct gdn_dims {
   int32_t act;    /* GDN_ACT_SILU or GDN_ACT_NONE */
 } gdn_dims;
 
-/* Library version string (static storage). */
+/* Library version string (static storage).  (The pages describe no such
+ * call; it identifies the library build.) */
 const char *gdn_version(void);
 
 /* Message for the last error returned on the calling host thread ("" if none;
- * thread-local storage, valid until the next call on that thread). */
+ * thread-local storage, valid until the next call on that thread).  Every
+ * call validates its arguments and fails with a message before it launches
+ * anything ("Add request-owned eight-way MTP serving for Qwen 35B",
+ * Clean-install public launch verification: an incomplete launch contract
+ * fails closed before any work). */
 const char *gdn_last_error(void);
 
 /*
  * Bytes of per-layer workspace that gdn_conv_verify fills and gdn_commit reads
- * for `mode`; 0 if dims or mode are invalid.  RECOMPUTE needs
- * 4*B*T*(H_v*d_v + H_k*d_k + H_v) bytes (+ alignment padding); SNAPSHOT needs
- * 4*T*B*H_v*d_v*d_k bytes; DEFERRED twice RECOMPUTE's captures plus a header.
+ * for `mode`: the captured verification inputs that let the commit rerun the
+ * recurrence over the accepted prefix ("perf(qwen): full-context MTP draft
+ * prefill and replay-free rewind", Summary item 4); 0 if dims or mode are
+ * invalid.  Regions are 256-byte aligned:
+ *   RECOMPUTE  e [B][H_v][T][d_v], normalised k [B][H_k][T][d_k] and the
+ *              cumulative log-decay [B][H_v][8], fp32:
+ *              about 4*B*T*(H_v*d_v + H_k*d_k) + 32*B*H_v bytes;
+ *   SNAPSHOT   S_1..S_T: 4*T*B*H_v*d_v*d_k bytes;
+ *   DEFERRED   the pending keep [B][H_v] int32, then e and k (one copy per
+ *              (row, value head): [B][H_v][T][d]) and the decay:
+ *              about 4*B*H_v + 4*B*T*(2*H_v*d) + 32*B*H_v bytes.
  */
 size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int mode);
 
 /*
  * Verify one layer: for every active row b run the T positions from the
- * committed window and the pre-verification state, writing o_t to `out`.
+ * committed window and the pre-verification state, writing o_t to `out`
+ * ("MTP inference: review and commit structure", Functional commits item 2:
+ * a speculative transaction that verifies from verifier buffers and leaves
+ * the committed state to the accepted-prefix commit).
  *  - reads  x, conv_w, g, beta, state, ring slots 0..2, active;
  *  - writes out; ring slots 3..2+T of active rows (never the committed
  *    window); layer_ws (the captured verification quantities the matching
@@ -221,7 +248,10 @@ int gdn_conv_verify_gated(const gdn_dims *dims, int mode, const gdn_bf16 *x, con
 
 /*
  * Commit the accepted prefix of every row for n_layers layers in one launch
- * (grouped across layers).  keep'[b] = keep[b] if active[b] and
+ * (grouped across layers: "MTP inference: review and commit structure",
+ * Functional commits item 2, accepted-prefix state replay with grouped copies;
+ * "Add request-owned eight-way MTP serving for Qwen 35B", section 4, keep =
+ * 0, 1, 2 per row with keep = 0 restoring the pre-verification state).  keep'[b] = keep[b] if active[b] and
  * 0 <= keep[b] <= T, else 0 (an active row with keep outside [0, T] also sets
  * GDN_STATUS_BAD_KEEP).  For keep' >= 1 the layer's state rows of b become the
  * state after the first keep' positions (RECOMPUTE, SNAPSHOT: now; DEFERRED:
@@ -245,7 +275,8 @@ int gdn_commit(const gdn_dims *dims, int mode, int n_layers, float *const *state
 /*
  * Apply every commit a DEFERRED cycle left pending in the n_layers layer
  * workspaces to the state buffers, so that they hold the committed state (as
- * an eager commit would have left them).  Call it before reading a state
+ * an eager commit would have left them: the accepted-prefix state of "MTP
+ * inference: review and commit structure", Functional commits item 2).  Call it before reading a state
  * buffer directly, before gdn_prefill_chunked, and before switching a layer
  * to another mode.  Idempotent; a no-op for RECOMPUTE and SNAPSHOT.
  * Errors: as gdn_commit.
@@ -254,13 +285,17 @@ int gdn_flush(const gdn_dims *dims, int mode, int n_layers, float *const *state,
               void *const *layer_ws, void *stream);
 
 /*
- * Bytes of workspace gdn_prefill_chunked needs for a prompt of L tokens;
- * 0 if the arguments are invalid.
+ * Bytes of workspace gdn_prefill_chunked needs for a prompt of L tokens (the
+ * per-chunk operands of the chunked form, "MTP inference: review and commit
+ * structure", Verification and limits); 0 if the arguments are invalid.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L);
 
 /*
- * Prime every row over a prompt of L tokens in chunked form (chunk = 64):
+ * Prime every row over a prompt of L tokens in chunked form (chunk = 64; "MTP
+ * inference: review and commit structure", Verification and limits: the
+ * chunked recurrence used for a prompt differs from the sequential one only
+ * in its rounding boundaries):
  * conv from the committed window (ring slots 0..2), L2 norm, then per chunk
  * the UT transform of the decay-weighted strictly-lower K K^T block on tensor
  * cores and a sequential pass of the state across chunks.  Equivalent, up to
@@ -319,7 +354,13 @@ int gdn_conv_verify_noalloc(const gdn_dims *dims, int mode, const gdn_bf16 *x, c
 /*
  * Read the sticky device status word of the current device (GDN_STATUS_*
  * bits) into *status; clear it if `clear` is nonzero.  Synchronises the
- * device.  Returns GDN_OK or GDN_ERR_CUDA / GDN_ERR_INVALID_ARG.
+ * device.  Returns GDN_OK or GDN_ERR_CUDA / GDN_ERR_INVALID_ARG.  Conditions
+ * found on the device (a keep outside [0, T], a row index outside its cohort,
+ * a bounded wait that ran out) cannot fail the launch that met them; the
+ * kernel takes the safe action (commit nothing, copy nothing, write nothing
+ * more) and records the condition here ("Add request-owned eight-way MTP
+ * serving for Qwen 35B", section 4: keep = 0 restores the pre-verification
+ * state; Clean-install public launch verification: fail closed).
  */
 int gdn_get_status(int clear, uint32_t *status);
 
@@ -372,6 +413,29 @@ int gdn_move_rows(const gdn_dims *src_dims, const gdn_dims *dst_dims, int mode, 
 size_t gdn_accept_workspace_bytes(int B, int T, int V);
 int gdn_accept_greedy(int B, int T, int V, const gdn_bf16 *logits, const int32_t *draft, const uint8_t *active,
                       int32_t *keep, int32_t *next, void *ws, size_t ws_bytes, void *stream);
+
+/* ---- test hook ---------------------------------------------------------------
+ * gdn_conv_verify at d = 128 (RECOMPUTE or DEFERRED) with its failure path
+ * forced, for tests of that path.  (The pages describe no such call; it
+ * exercises the bounded waits that every kernel of the library puts on its
+ * own copies.)  The CTA of (row 0, head 0) announces 16 bytes more on one of
+ * its state-tile barriers than its copy delivers, so that barrier's phase
+ * never completes; every bounded wait of the call gives up after wait_limit
+ * polls instead of the library's default (a poll lasts at most about a
+ * microsecond).  That CTA then sets GDN_STATUS_TIMEOUT, waits (bounded) for
+ * its own copies, writes no output, no capture and no state (it may already
+ * have written its new ring inputs, slots 3..2+T) and leaves; every other
+ * CTA completes as in gdn_conv_verify.  Row 0 must be active.  Contract after
+ * a timeout: the layer's state is unchanged in RECOMPUTE mode (in DEFERRED
+ * mode a commit that was pending for (row 0, head 0) stays pending), and the
+ * next ordinary gdn_conv_verify of the layer recomputes everything it
+ * writes.  Errors: as gdn_conv_verify, plus GDN_ERR_UNSUPPORTED for another
+ * head size or SNAPSHOT mode.
+ */
+int gdn_test_verify_timeout(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w,
+                            const float *g, const float *beta, const float *state, gdn_bf16 *ring,
+                            const int32_t *offsets, const uint8_t *active, gdn_bf16 *out, void *layer_ws,
+                            size_t layer_ws_bytes, uint32_t wait_limit, void *stream);
 
 #ifdef __cplusplus
 }

@@ -16,6 +16,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "gdn_common.cuh"
 
@@ -24,6 +25,15 @@ using namespace gdn;
 namespace {
 
 thread_local std::string t_err;
+
+// An NVTX range around each entry point (what a profiler timeline shows as
+// the call's host-side extent; a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 int fail(int code, const char *fmt, ...) {
   char buf[512];
@@ -165,7 +175,9 @@ namespace {
 int verify_impl(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
                 const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
                 const uint8_t *active, const gdn_bf16 *gate_z, const gdn_bf16 *norm_w, float eps, gdn_bf16 *out,
-                void *layer_ws, size_t layer_ws_bytes_given, void *stream) {
+                void *layer_ws, size_t layer_ws_bytes_given, void *stream, uint32_t test_extra_tx = 0,
+                uint32_t wait_limit = kWaitLimit) {
+  NvtxRange range(gate_z ? "gdn_conv_verify_gated" : "gdn_conv_verify");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (mode & ~(GDN_VERIFY_OVERLAP | 0xff))
@@ -210,8 +222,8 @@ int verify_impl(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf1
   p.geps = eps;
   p.status = status_word_address();
   if (!p.status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
-  p.wait_limit = kWaitLimit;
-  p.test_extra_tx = 0;
+  p.wait_limit = wait_limit;
+  p.test_extra_tx = test_extra_tx;
   if (dims->d_k == 128 && mode != GDN_COMMIT_SNAPSHOT &&
       (rc = encode_state_map(p.tmap_state, state, (long long)dims->B * dims->H_v * 128)))
     return rc;
@@ -253,6 +265,18 @@ __attribute__((visibility("default"))) int gdn_conv_verify(
                      layer_ws, layer_ws_bytes_given, stream);
 }
 
+__attribute__((visibility("default"))) int gdn_test_verify_timeout(
+    const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
+    const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
+    const uint8_t *active, gdn_bf16 *out, void *layer_ws, size_t layer_ws_bytes_given, uint32_t wait_limit,
+    void *stream) {
+  if (check_dims(dims) == GDN_OK && (dims->d_k != 128 || (mode & 0xff) == GDN_COMMIT_SNAPSHOT))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_test_verify_timeout: d = 128, RECOMPUTE or DEFERRED only");
+  if (wait_limit < 1) return fail(GDN_ERR_INVALID_ARG, "gdn_test_verify_timeout: wait_limit must be >= 1");
+  return verify_impl(dims, mode, x, conv_w, g, beta, state, ring, offsets, active, nullptr, nullptr, 0.f, out,
+                     layer_ws, layer_ws_bytes_given, stream, 16u, wait_limit);
+}
+
 __attribute__((visibility("default"))) int gdn_conv_verify_gated(
     const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
     const float *beta, const float *state, gdn_bf16 *ring, const int32_t *offsets,
@@ -271,6 +295,7 @@ __attribute__((visibility("default"))) int gdn_commit(const gdn_dims *dims, int 
                                                       float *const *state, gdn_bf16 *const *ring,
                                                       void *const *layer_ws, const int32_t *keep,
                                                       const uint8_t *active, int32_t *offsets, void *stream) {
+  NvtxRange range("gdn_commit");
   int rc = check_dims(dims);
   if (rc) return rc;
   if ((rc = check_mode(mode))) return rc;
@@ -299,6 +324,7 @@ __attribute__((visibility("default"))) int gdn_commit(const gdn_dims *dims, int 
 
 __attribute__((visibility("default"))) int gdn_flush(const gdn_dims *dims, int mode, int n_layers,
                                                      float *const *state, void *const *layer_ws, void *stream) {
+  NvtxRange range("gdn_flush");
   int rc = check_dims(dims);
   if (rc) return rc;
   if ((rc = check_mode(mode))) return rc;
@@ -323,6 +349,7 @@ __attribute__((visibility("default"))) int gdn_prefill_chunked(
     const gdn_dims *dims, int L, const gdn_bf16 *x, const gdn_bf16 *conv_w, const float *g,
     const float *beta, float *state, gdn_bf16 *ring, int32_t *offsets, gdn_bf16 *out, void *ws,
     size_t ws_bytes, void *stream) {
+  NvtxRange range("gdn_prefill_chunked");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (L < 0 || L > kMaxPrefillLen)
@@ -371,6 +398,7 @@ __attribute__((visibility("default"))) int gdn_accept_greedy(int B, int T, int V
                                                              const int32_t *draft, const uint8_t *active,
                                                              int32_t *keep, int32_t *next, void *ws,
                                                              size_t ws_bytes, void *stream) {
+  NvtxRange range("gdn_accept_greedy");
   if (B < 0 || T < 1 || V < 1) return fail(GDN_ERR_INVALID_ARG, "accept: B=%d T=%d V=%d", B, T, V);
   if (T > kMaxAcceptT) return fail(GDN_ERR_UNSUPPORTED, "accept: T=%d above %d", T, kMaxAcceptT);
   if ((long long)B * T > 65535) return fail(GDN_ERR_UNSUPPORTED, "accept: B*T=%lld above 65535", (long long)B * T);
@@ -393,6 +421,7 @@ __attribute__((visibility("default"))) int gdn_move_rows(
     const gdn_bf16 *const *src_ring, const int32_t *src_offsets, float *const *dst_state, gdn_bf16 *const *dst_ring,
     int32_t *dst_offsets, void *const *dst_layer_ws, const int32_t *src_rows, const int32_t *dst_rows, int n_rows,
     void *stream) {
+  NvtxRange range("gdn_move_rows");
   int rc = check_dims(src_dims);
   if (rc) return rc;
   if ((rc = check_dims(dst_dims))) return rc;

@@ -14,6 +14,8 @@
 // DEFERRED mode the commit only records keep' per layer, and the next verify
 // of each (row, head) applies it.  Every mode also shifts the conv window of
 // committed rows (the conv-cache mutation).
+#include <atomic>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -23,13 +25,15 @@ __device__ uint32_t g_status;  // sticky GDN_STATUS_* bits of this device
 // Device address of g_status on the current device, looked up once per device
 // (the launchers pass it to kernels in other translation units).
 uint32_t *status_word_address() {
-  static void *cached[64] = {nullptr};
+  static std::atomic<void *> cached[64];  // per device; host threads may race to fill it (same value)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  if (dev >= 0 && dev < 64 && cached[dev]) return static_cast<uint32_t *>(cached[dev]);
+  if (dev >= 0 && dev < 64) {
+    if (void *c = cached[dev].load(std::memory_order_acquire)) return static_cast<uint32_t *>(c);
+  }
   void *ptr = nullptr;
   if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
-  if (dev >= 0 && dev < 64) cached[dev] = ptr;
+  if (dev >= 0 && dev < 64) cached[dev].store(ptr, std::memory_order_release);
   return static_cast<uint32_t *>(ptr);
 }
 
@@ -237,16 +241,16 @@ __global__ void __launch_bounds__(128) flush_kernel(const CommitParams p) {
 }
 
 static int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // per device, 0 until looked up
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 152;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 template <int D>

@@ -137,12 +137,19 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, 
 }
 
 // As mbar_wait_limit without the sleep between polls, for waits on the
-// critical path: try_wait itself suspends the thread until the phase
-// completes or a hardware time limit passes, so each poll is cheap and the
-// wake-up immediate.  Still bounded by `limit` polls.
+// critical path: each try_wait suspends the thread until the phase completes
+// or at most ~1 us passes (its suspend-time hint), so a poll is cheap, the
+// wake-up immediate and the whole wait bounded by `limit` polls.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+        : "memory");
+    if (ok) return true;
+  }
   return false;
 }
 

@@ -11,13 +11,8 @@
 // GDN_VERIFY_OVERLAP part of the next layer's CTAs fit beside it and stream
 // their state while this one computes.
 //
-// Deep drafts at d = 128 (T >= kTcMinT, RECOMPUTE and DEFERRED) take the
-// state dot products on the tensor cores instead: after the conv barrier the
-// staged fp32 state is split in place into bf16 hi/lo operand tiles, one
-// thread issues the products into TMEM, and thread i < d reads the 2T dot
-// products of state row i from TMEM lane i and runs the row's recurrence.
-// The fixed cost of the split and the products (about 2 us per CTA) beats
-// the SIMT row loop, whose shuffles and registers grow with T, from T = 5 on.
+// (d = 128 in RECOMPUTE and DEFERRED mode runs the tensor-core verify of
+// verify_tc.cuh; this CUDA-core kernel serves d = 32, 64 and SNAPSHOT mode.)
 //
 // The pre-verification state S_0 is only read ("MTP inference: review and
 // commit structure", Functional commits item 2: speculative transactions with
@@ -107,45 +102,12 @@ __device__ __forceinline__ void conv_store_ring(const VerifyParams &p, int b, in
   for (int t = 0; t < T; ++t) ringb[size_t(kNewSlot + t) * p.C] = in.x[t];
 }
 
-// Tensor-core dot products (d = 128, T >= kTcMinT, not SNAPSHOT): the 2T
-// dot products of every state row with the raw k_t and q_t are one
-// 128 x 16 x 128 product, D[i][n] = sum_j S_0[i][j] B[n][j] with B's rows
-// k_0..k_{T-1}, q_0..q_{T-1} and zero rows up to kTcN, taken in bf16 pieces
-// as S_hi [B_hi; B_lo]^T (N = 32, TMEM columns 0..31) and S_lo B_hi^T
-// (N = 16, columns 32..47), summed per row afterwards; the SIMT row loop and
-// its butterflies are gone.
-constexpr int kTcMinT = 5;
-constexpr int kTcN = 2 * kMaxT;   // the 2T vectors, zero-padded
-constexpr int kTcCols = 64;       // TMEM columns allocated (48 used)
-
-// Split 8 fp32 values by truncation: x_hi = the upper 16 bits of x (a bf16),
-// x_lo = the upper 16 bits of x - x_hi (exact in fp32), so that
-// |x - x_hi - x_lo| < 2^-14 |x|; byte permutes and one subtraction per
-// value, no conversion instructions.  Stored as two 16-byte runs.
-__device__ __forceinline__ void store8_split_trunc(const float *v, uint16_t *hi, uint16_t *lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t a = __float_as_uint(v[2 * q]), c = __float_as_uint(v[2 * q + 1]);
-    h[q] = __byte_perm(a, c, 0x7632);
-    const float ra = v[2 * q] - __uint_as_float(a & 0xffff0000u);
-    const float rc = v[2 * q + 1] - __uint_as_float(c & 0xffff0000u);
-    l[q] = __byte_perm(__float_as_uint(ra), __float_as_uint(rc), 0x7632);
-  }
-  *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
 // Shared memory of one verify CTA: the (row, head) state tile, the conv
 // outputs of its key head and, in DEFERRED mode, the captures of the previous
 // verify (e_t, normalised k_t, G_t) for the commit that may still be pending.
 template <int D, int T>
 struct VerifySmem {
-  static constexpr bool kTc = D == 128 && T >= kTcMinT;
-  // fp32 state; on the tensor-core path, once every thread holds its part in
-  // registers, the same bytes take the bf16 hi and lo A tiles (K-major,
-  // no-swizzle canonical layout, 32 KiB each)
-  alignas(128) float S[D * D];
+  alignas(128) float S[D * D];  // fp32 state tile
   float q[T][D];
   float k[T][D];
   float ce[T][D];
@@ -157,24 +119,20 @@ struct VerifySmem {
   float cQ[T][T];             // e^{G_t-G_s} (k^_s.q^_t), s <= t: weight of e_s in o_t
   float cbk[T], cgq[T], cinvk[T], cGc[T];
   float gsq[T][8];  // gated RMSNorm: per-warp sums of o_t^2 (at most 8 warps)
-  alignas(128) uint16_t bqk[kTc ? 2 * kTcN * D : 8];  // tensor-core B operand: hi tile, then lo tile
   uint64_t bar[D / kTileRows];
   uint64_t cbar;
-  uint64_t mbar;  // tensor-core products done
-  uint32_t tmem;  // TMEM accumulator address
 };
 
 // Threads per verify CTA: 2d (8 warps at d = 128, 16 state rows per warp).
 // Measured at B = 8, T = 2: d threads (3 CTAs per SM, 32 rows per warp) make
 // a layer about 1 us slower, the longer per-warp row loop costing more than
 // the deeper residency gains.
-// Two CTAs per SM for T <= 4 and on the tensor-core path; the SIMT path at
-// T > 4 needs more registers than that leaves (spills measured).
+// Two CTAs per SM for T <= 4; at T > 4 the row loop needs more registers
+// than that leaves (spills measured).
 template <int D, int T, int MODE>
 struct VerifyShape {
-  static constexpr bool kTc = VerifySmem<D, T>::kTc && MODE != GDN_COMMIT_SNAPSHOT;
   static constexpr int kThreads = 2 * D;
-  static constexpr int kMinBlocks = (T <= 4 || kTc) ? 2 : 1;
+  static constexpr int kMinBlocks = T <= 4 ? 2 : 1;
 };
 
 template <int D, int T, int MODE>
@@ -190,9 +148,6 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
   constexpr int NT = D / kTileRows;   // 32-row tiles, one bulk copy and barrier each
   // per-head reductions: |q_t|^2, |k_t|^2, k_s.k_t (s<t), k_s.q_t (s<=t)
   constexpr int NKK = T * (T - 1) / 2, NKQ = T * (T + 1) / 2, NV = 2 * T + NKK + NKQ;
-  constexpr bool kTC = VerifyShape<D, T, MODE>::kTc;
-  static_assert(!kTC || (T >= 4 && 2 * T <= kTcN && NTHR == kTcN * D / 8 && NWARP == 8),
-                "tensor-core path: one B-tile chunk per thread, 16 rows per warp");
 
   extern __shared__ __align__(128) unsigned char vsm_raw[];
   VerifySmem<D, T> &sm = *reinterpret_cast<VerifySmem<D, T> *>(vsm_raw);
@@ -247,7 +202,6 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
 #pragma unroll
     for (int i = 0; i < NT; ++i) mbar_init(&sm.bar[i], 1);
     mbar_init(&sm.cbar, 1);
-    if (kTC) mbar_init(&sm.mbar, 1);
     fence_mbar_init();
   }
   if (active) stage_state();
@@ -378,20 +332,15 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
     // the CTA) and the v channels of the rows this lane will hold; every load
     // is issued before the first use
     constexpr int NQK = (2 * D + NTHR - 1) / NTHR;
-    // (tensor-core path: thread i < d takes the v channel of state row i)
-    ConvIn<T> inqk[NQK], inv[kTC ? 1 : NGRP];
+    ConvIn<T> inqk[NQK], inv[NGRP];
 #pragma unroll
     for (int r = 0; r < NQK; ++r) {
       const int c2 = tid + r * NTHR;
       if (c2 < 2 * D) conv_load<T>(p, b, (c2 >= D ? H_k * D + c2 - D : c2) + hk * D, inqk[r]);
     }
-    if constexpr (kTC) {
-      if (tid < D) conv_load<T>(p, b, 2 * H_k * D + h * D + tid, inv[0]);
-    } else {
 #pragma unroll
-      for (int grp8 = 0; grp8 < NGRP; ++grp8)
-        conv_load<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
-    }
+    for (int grp8 = 0; grp8 < NGRP; ++grp8)
+      conv_load<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       gt[t] = p.g[(size_t(b) * T + t) * H_v + h];
@@ -411,12 +360,8 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
         for (int t = 0; t < T; ++t) (c2 >= D ? sm.k : sm.q)[t][c2 >= D ? c2 - D : c2] = y[t];
       }
     }
-    if constexpr (kTC) {
-      if (tid < D) conv_eval<T>(inv[0], p.act, vrow[0]);
-    } else {
 #pragma unroll
-      for (int grp8 = 0; grp8 < NGRP; ++grp8) conv_eval<T>(inv[grp8], p.act, vrow[grp8]);
-    }
+    for (int grp8 = 0; grp8 < NGRP; ++grp8) conv_eval<T>(inv[grp8], p.act, vrow[grp8]);
     // new raw inputs into the ring: q/k channels by one CTA of the key head,
     // v channels by one lane of the four sharing a row
 #pragma unroll
@@ -424,9 +369,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
       const int c2 = tid + r * NTHR;
       if (qk_writer && c2 < 2 * D) conv_store_ring<T>(p, b, (c2 >= D ? H_k * D + c2 - D : c2) + hk * D, inqk[r]);
     }
-    if constexpr (kTC) {
-      if (tid < D) conv_store_ring<T>(p, b, 2 * H_k * D + h * D + tid, inv[0]);
-    } else if (leader) {
+    if (leader) {
 #pragma unroll
       for (int grp8 = 0; grp8 < NGRP; ++grp8)
         conv_store_ring<T>(p, b, 2 * H_k * D + h * D + jw0 + 8 * grp8 + grp + GPW * istar, inv[grp8]);
@@ -456,89 +399,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
   float red_h[NV];
   float inv_q[T], inv_k[T], Gc[T], gam[T];
   float decay[T][T];  // exp(G_t - G_s), s < t
-  // tensor-core path: thread (warp w, lane l) converts 64 state values of row
-  // i = 16w + 8(l/16) + l % 8, columns [64 hf, +64) with hf = (l/8) % 2,
-  // one 8-column chunk per step, starting at chunk (l % 8) so that the eight
-  // lanes of a quarter-warp read distinct banks and, holding distinct i % 8,
-  // write distinct banks of the canonical tile; fsw swaps the two 16-byte
-  // halves of a chunk for the upper four lanes of each eight
-  const int tc_r = lane & 7, tc_q = warp * 4 + (lane >> 3);
-  const int tc_i = (tc_q >> 1) * 8 + tc_r, tc_hf = tc_q & 1, tc_fsw = (tc_r >> 2) & 1;
   if constexpr (kSC) {
-    if constexpr (kTC) {
-      float4 sv[16];
-      // the B operand: row n < T is the raw k_n, T <= n < 2T the raw q_{n-T},
-      // the rest zero; one 8-element chunk per thread.  A quarter-warp holds
-      // eight rows, distinct mod 8, so its stores hit eight bank groups; the
-      // chunk is rotated by the row so its loads spread over the banks too.
-      const int n = tid & 15, c8 = 8 * (((tid >> 4) + n) & 15);
-      float bv[8];
-      if (n < 2 * T) {
-        const float *src = (n < T ? sm.k[n] : sm.q[n - T]) + c8;
-        const float4 lo4 = *reinterpret_cast<const float4 *>(src), hi4 = *reinterpret_cast<const float4 *>(src + 4);
-        bv[0] = lo4.x, bv[1] = lo4.y, bv[2] = lo4.z, bv[3] = lo4.w;
-        bv[4] = hi4.x, bv[5] = hi4.y, bv[6] = hi4.z, bv[7] = hi4.w;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) bv[u] = 0.f;
-      }
-      const uint32_t o = canon_off(n, c8, D) / 2;
-      store8_split(bv, sm.bqk + o, sm.bqk + kTcN * D + o);
-      // the accumulators; taken only now, after the PDL wait (no CTA holds
-      // tensor memory while it waits for another grid), by the last warp,
-      // which has no rows and no captures to write
-      if (warp == NWARP - 1) tmem_alloc(&sm.tmem, kTcCols);
-      // this thread's 64 state values into registers (the warp's rows arrive
-      // with one bulk copy); the A tiles overwrite them after the barrier, so
-      // the write-back copy of an applied commit must have read them too
-      const bool late = !mbar_wait_bounded(&sm.bar[(16 * warp) / kTileRows], 0);
-      if (!late) {
-        const float *row = sm.S + tc_i * D + 64 * tc_hf;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = (j + tc_r) & 7;
-          sv[2 * j] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 * tc_fsw);
-          sv[2 * j + 1] = *reinterpret_cast<const float4 *>(row + 8 * c + 4 - 4 * tc_fsw);
-        }
-      }
-      if (MODE == GDN_COMMIT_DEFERRED && applied && tid == 0) bulk_wait_read_all();
-      tc_fence_before();
-      const bool failed = __syncthreads_or(late);
-      tc_fence_after();
-      if (failed) {
-        if (warp == NWARP - 1) tmem_dealloc(sm.tmem, kTcCols);
-        give_up();
-        return;
-      }
-      uint16_t *ahi = reinterpret_cast<uint16_t *>(sm.S), *alo = ahi + D * D;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = 8 * tc_hf + ((j + tc_r) & 7);
-        const float4 a = tc_fsw ? sv[2 * j + 1] : sv[2 * j], z = tc_fsw ? sv[2 * j] : sv[2 * j + 1];
-        const float v8[8] = {a.x, a.y, a.z, a.w, z.x, z.y, z.z, z.w};
-        const uint32_t o = canon_off(tc_i, 8 * c, D) / 2;
-        store8_split_trunc(v8, ahi + o, alo + o);
-      }
-      fence_async_smem();  // the tiles (and the B operand) are read by the tensor cores
-      __syncthreads();  // the A and B tiles are complete
-      // the products start now and run while the CTA computes the per-head
-      // dot products and coefficients below
-      if (tid == 0) {
-        tc_fence_after();
-        // B_hi (rows 0..15) and B_lo (rows 16..31) form one 32-row tile
-        const uint32_t tmem = sm.tmem;
-        const uint32_t aH = smem_u32(sm.S), aL = aH + D * D * 2, bH = smem_u32(sm.bqk);
-        constexpr uint32_t idesc32 = umma_idesc_bf16(D, 2 * kTcN), idesc16 = umma_idesc_bf16(D, kTcN);
-        constexpr uint32_t sbo = (D / 8) * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          umma_bf16(tmem, umma_desc(aH + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo), idesc32, kk > 0);
-          umma_bf16(tmem + 2 * kTcN, umma_desc(aL + kk * 256, 128, sbo), umma_desc(bH + kk * 256, 128, sbo),
-                    idesc16, kk > 0);
-        }
-        umma_commit(&sm.mbar);
-      }
-    }
     // ---- 3'. the T^2 + 2T dot products, four lanes each ----------------------
     // Lane l of quad qd sums float4 columns l, l+4, ... of its pair, starting
     // 4*qd columns in, so the two quads of a quarter-warp read different banks.
@@ -646,94 +507,7 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
   // and in DEFERRED mode already brought up to date) -------------------------
   const size_t plane = size_t(p.B) * H_v * D * D;
   const bool gated = p.gz != nullptr;
-  if constexpr (kTC) {
-    // ---- 5''. thread i < d runs the recurrence of state row i from its 2T
-    // dot products in TMEM lane i; warp 4 writes the captures meanwhile -----
-    const uint32_t tmem = sm.tmem;
-    const bool rower = tid < D;  // warps 0..3: TMEM lanes 32w..32w+31
-    const int i = tid;
-    float o[T], e[T];
-    uint16_t zt[T], wi = 0;
-    bool late = false;
-    if (rower) {
-      if (gated) {
-        wi = p.gw[i];
-#pragma unroll
-        for (int t = 0; t < T; ++t) zt[t] = p.gz[((size_t(b) * T + t) * H_v + h) * D + i];
-      }
-      late = __any_sync(0xffffffffu, !mbar_wait_bounded(&sm.mbar, 0));
-      tc_fence_after();
-      if (!late) {
-        float d01[2 * kTcN], d2[kTcN], red[kTcN];
-        tmem_ld32(tmem + (uint32_t(32 * warp) << 16), d01);
-        tmem_ld16(tmem + (uint32_t(32 * warp) << 16) + 2 * kTcN, d2);
-#pragma unroll
-        for (int n = 0; n < kTcN; ++n) red[n] = (d01[n] + d01[kTcN + n]) + d2[n];
-        const float *v = vrow[0];
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          float acc = fmaf(bt[t], v[t], -sm.cbk[t] * red[t]);
-#pragma unroll
-          for (int s0 = 0; s0 < t; ++s0) acc = fmaf(-sm.cA[t][s0], e[s0], acc);
-          e[t] = acc;
-          float ot = sm.cgq[t] * red[T + t];
-#pragma unroll
-          for (int s0 = 0; s0 <= t; ++s0) ot = fmaf(sm.cQ[t][s0], e[s0], ot);
-          o[t] = ot;
-        }
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          if (!gated) p.out[((size_t(b) * T + t) * H_v + h) * D + i] = f2bf(o[t]);
-          p.ws_e[(bh * T + t) * D + i] = e[t];
-        }
-        if (gated) {
-#pragma unroll
-          for (int t = 0; t < T; ++t) {
-            float q2 = o[t] * o[t];
-#pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, m);
-            if (lane == 0) sm.gsq[t][warp] = q2;
-          }
-        }
-      }
-    }
-    if (warp == 4) {
-      // the key head's normalised k (one copy per (row, value head) in
-      // DEFERRED mode, per key head otherwise) and the cumulative decay
-      const size_t bk = MODE == GDN_COMMIT_DEFERRED ? bh : size_t(b) * H_k + hk;
-      if (MODE == GDN_COMMIT_DEFERRED || qk_writer)
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          const float4 kr = *reinterpret_cast<const float4 *>(&sm.k[t][4 * lane]);
-          const float ik = sm.cinvk[t];
-          st_f4(p.ws_k + (bk * T + t) * D + 4 * lane, make_float4(kr.x * ik, kr.y * ik, kr.z * ik, kr.w * ik));
-        }
-      if (lane < T) p.ws_G[bh * kMaxT + lane] = sm.cGc[lane];
-    }
-    // every TMEM read is done before the accumulator is released
-    tc_fence_before();
-    const bool failed = __syncthreads_or(late);
-    tc_fence_after();
-    if (warp == NWARP - 1) {
-      if (failed) mbar_wait_bounded(&sm.mbar, 0);  // one more bounded wait for the products
-      tmem_dealloc(tmem, kTcCols);
-    }
-    if (failed) {
-      give_up();
-      return;
-    }
-    if (gated && rower) {
-      // out = o_t / sqrt(mean_i o_t[i]^2 + eps) * w[i] * silu(z_t[i])
-#pragma unroll
-      for (int t = 0; t < T; ++t) {
-        float ss = 0.f;
-#pragma unroll
-        for (int w = 0; w < D / 32; ++w) ss += sm.gsq[t][w];
-        const float rstd = rsqrtf(ss / float(D) + p.geps);
-        p.out[((size_t(b) * T + t) * H_v + h) * D + i] = f2bf(o[t] * rstd * bf2f(wi) * silu_fast(bf2f(zt[t])));
-      }
-    }
-  } else {
+  {
   float og[NGRP][T];           // gated: o of the rows this lane leads, until the norm is known
   uint16_t zg[NGRP][T], wg[NGRP];
   if (gated && leader) {       // the gate and weight of those rows, loaded now
@@ -887,12 +661,12 @@ __global__ void __launch_bounds__(VerifyShape<D, T, MODE>::kThreads, VerifyShape
     give_up();
     return;
   }
-  }  // SIMT row loop
+  }  // row loop
   // every warp applied its rows before the conv barrier
   if (MODE == GDN_COMMIT_DEFERRED && pending && tid == 0) p.ws_pend[bh] = 0;  // (a repeat if applied before the wait)
 
   // ---- 6. captures of the key head and decay --------------------------------
-  if (MODE != GDN_COMMIT_SNAPSHOT && !kTC) {  // (the tensor-core path wrote them in 5'')
+  if (MODE != GDN_COMMIT_SNAPSHOT) {
     // k: one copy per key head in RECOMPUTE mode, one per (row, value head)
     // in DEFERRED mode
     const size_t bk = MODE == GDN_COMMIT_DEFERRED ? bh : size_t(b) * H_k + hk;

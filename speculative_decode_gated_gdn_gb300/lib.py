@@ -35,7 +35,7 @@ GDN_NOALLOC_WS_BYTES = 4 << 20
 EXPORTS = ("gdn_version", "gdn_last_error", "gdn_layer_workspace_bytes", "gdn_conv_verify",
            "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_get_status",
            "gdn_conv_verify_noalloc", "gdn_flush", "gdn_accept_workspace_bytes", "gdn_accept_greedy",
-           "gdn_conv_verify_gated", "gdn_move_rows")
+           "gdn_conv_verify_gated", "gdn_move_rows", "gdn_test_verify_timeout")
 
 
 class GdnError(RuntimeError):
@@ -85,6 +85,8 @@ def _declare(lib):
     lib.gdn_prefill_chunked.argtypes = [D, ctypes.c_int] + [_P] * 9 + [ctypes.c_size_t, _P]
     lib.gdn_conv_verify_noalloc.restype = ctypes.c_int
     lib.gdn_conv_verify_noalloc.argtypes = [D, ctypes.c_int] + [_P] * 9 + [ctypes.POINTER(_P), _P]
+    lib.gdn_test_verify_timeout.restype = ctypes.c_int
+    lib.gdn_test_verify_timeout.argtypes = [D, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, ctypes.c_uint32, _P]
     lib.gdn_get_status.restype = ctypes.c_int
     lib.gdn_get_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)]
     lib.gdn_conv_verify_gated.restype = ctypes.c_int
@@ -227,6 +229,22 @@ def gdn_conv_verify_noalloc(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, 
         _stream(stream))
     _check(rc, "gdn_conv_verify_noalloc")
     return int(used.value)
+
+
+def gdn_test_verify_timeout(d: gdn_dims, mode, x, conv_w, g, beta, state, ring, offsets, active, out, layer_ws,
+                            wait_limit, layer_ws_bytes=None, stream=None):
+    """gdn_conv_verify with its bounded-wait failure path forced for the CTA of
+    (row 0, head 0), giving up after `wait_limit` polls (gdn.h, test hook)."""
+    torch = _t()
+    if layer_ws_bytes is None:
+        layer_ws_bytes = layer_ws.numel() * layer_ws.element_size()
+    rc = load().gdn_test_verify_timeout(
+        ctypes.byref(d), mode, _ptr(x, "x", torch.bfloat16), _ptr(conv_w, "conv_w", torch.bfloat16),
+        _ptr(g, "g", torch.float32), _ptr(beta, "beta", torch.float32), _ptr(state, "state", torch.float32),
+        _ptr(ring, "ring", torch.bfloat16), _ptr(offsets, "offsets", torch.int32),
+        _ptr(active, "active", torch.uint8), _ptr(out, "out", torch.bfloat16), _ptr(layer_ws, "layer_ws"),
+        int(layer_ws_bytes), int(wait_limit), _stream(stream))
+    _check(rc, "gdn_test_verify_timeout")
 
 
 def _layer_ptrs(seq, what, dtype=None):

@@ -176,3 +176,23 @@ def test_binding_argument_counts_match_header(lib):
     for name, n in arity.items():
         argtypes = getattr(lib, name).argtypes
         assert argtypes is not None and len(argtypes) == n, f"{name}: header has {n} parameters, binding {argtypes}"
+
+
+PAGES = ('"perf(qwen): full-context MTP draft prefill and replay-free rewind"',
+         '"MTP inference: review and commit structure"',
+         '"Add request-owned eight-way MTP serving for Qwen 35B"')
+
+
+def test_every_declaration_cites_its_passage():
+    """Each call of the boundary names the page passage that defines it in the
+    comment before it, or says that the pages have no such call."""
+    text = open(os.path.join(HEADER_DIR, "gdn.h")).read()
+    body = text[text.index('extern "C" {'):]
+    flat = lambda c: " ".join(c.split()).replace(" * ", " ")
+    missing = []
+    for m in re.finditer(r"^[a-z][\w\s\*]*?\b(gdn_\w+)\s*\(", body, flags=re.M):
+        comments = re.findall(r"/\*.*?\*/", body[:m.start()], flags=re.S)
+        last = flat(comments[-1]) if comments else ""
+        if not (any(" ".join(pg.split()) in last for pg in PAGES) or "describe no such call" in last):
+            missing.append(m.group(1))
+    assert not missing, f"declarations without a page citation: {missing}"
