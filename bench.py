@@ -360,10 +360,14 @@ CHUNK = 64  # cycles per captured graph (a graph of a few thousand kernel nodes)
 def verify_mode(mode, layer):
     """Layers after the first follow another layer's verify, which writes none of
     their buffers, so they may stage state (and in DEFERRED mode apply their
-    pending commit) before that verify finishes.  Layer 0 follows the commit,
-    which writes every layer's state or workspace."""
+    pending commit) before that verify finishes.  Layer 0 follows the commit:
+    a DEFERRED commit writes no state, taps or captures, so layer 0 may still
+    stage those early (GDN_VERIFY_OVERLAP_STATE); an eager commit writes the
+    state, so layer 0 waits."""
     from speculative_decode_gated_gdn_gb300 import lib as L
-    return mode | (L.GDN_VERIFY_OVERLAP if layer > 0 else 0)
+    if layer > 0:
+        return mode | L.GDN_VERIFY_OVERLAP
+    return mode | (L.GDN_VERIFY_OVERLAP_STATE if mode == L.GDN_COMMIT_DEFERRED else 0)
 
 
 class Stack:

@@ -81,8 +81,8 @@
  * takes the dot products of the state rows with q_t and k_t on the tensor
  * cores in tf32 (the state read truncated to tf32, q and k rounded to it:
  * about 2^-11 of each term's magnitude); these products only enter e_t and
- * o_t, and every state update, conv, norm, gate and recurrence step stays in
- * fp32.  Its results differ from the CUDA-core path's (d = 32, 64, SNAPSHOT)
+ * o_t through per-head coefficients, and the state itself, every state
+ * update, conv, norm, gate and recurrence step stays in fp32.  Its results differ from the CUDA-core path's (d = 32, 64, SNAPSHOT)
  * only by rounding.  The d = 128 tensor-core verify addresses the state as
  * B * H_v * d_v rows of a tensor map, so it needs B * H_v * 128 < 2^31.
  */
@@ -136,11 +136,14 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
  * and beta (a prefetch only; those values are read after the wait), so
  * consecutive flagged verifies stream their state ahead of one another; in
  * DEFERRED mode it also fetches the captures of the layer's previous verify
- * and applies a pending commit (and writes it back) before that wait.  The
- * caller guarantees that no work issued since the last library call made
- * WITHOUT the flag writes this call's `state`, `conv_w`, ring slots 0..2,
- * `active` or `layer_ws`, and that the previous verify of this layer was
- * issued before that call.  In a verify cycle over a layer stack that means:
+ * and applies a pending commit (and writes it back) before that wait.  A
+ * kernel of any other library call (including a verify flagged
+ * GDN_VERIFY_OVERLAP_STATE) lets the next kernel start only after its own
+ * wait, so a chain of flagged verifies never runs ahead of the last call
+ * made without this flag.  The caller guarantees that no work issued since
+ * that call writes this call's `state`, `conv_w`, ring slots 0..2, `active`
+ * or `layer_ws`, and that the previous verify of this layer was issued
+ * before that call.  In a verify cycle over a layer stack that means:
  * flag every layer but the first one after a gdn_commit (any mode),
  * gdn_prefill_chunked, gdn_flush, gdn_move_rows or any other write of these
  * buffers.  Never flag a repeated verify of the same layer.  At d = 128 a
@@ -150,6 +153,23 @@ typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
  * than 416 of an SM's 512 columns (no kernel of this library does).  It is
  * always safe to omit. */
 #define GDN_VERIFY_OVERLAP 0x100
+
+/* A weaker flag for the first layer of a cycle after a DEFERRED gdn_commit
+ * (OR-ed into the mode argument instead of GDN_VERIFY_OVERLAP, never with
+ * it).  Before waiting for its predecessor the call stages its state tiles,
+ * reads its conv taps and active mask and (DEFERRED) fetches the captures of
+ * the layer's previous verify whether or not a commit is pending; the
+ * pending keep and the conv window are read after the wait, and the next
+ * kernel may start only after that wait, as for an unflagged call.  The caller guarantees that the work issued
+ * since this layer's previous gdn_conv_verify does not write this call's
+ * `state`, `conv_w`, `active` or the capture region of `layer_ws`: a
+ * DEFERRED gdn_commit writes none of them (it writes the pending keep, the
+ * conv windows and the offsets), while RECOMPUTE and SNAPSHOT commits write
+ * the state and gdn_flush, gdn_prefill_chunked and gdn_move_rows write the
+ * state and conv cache.  The tensor-memory condition of GDN_VERIFY_OVERLAP
+ * applies too.  It acts at d = 128 in RECOMPUTE and DEFERRED mode and is the
+ * same as no flag elsewhere.  It is always safe to omit. */
+#define GDN_VERIFY_OVERLAP_STATE 0x200
 
 /* sticky device status bits (gdn_get_status) */
 #define GDN_STATUS_BAD_KEEP 1u /* an active row passed keep outside [0, T];

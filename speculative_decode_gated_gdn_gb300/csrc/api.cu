@@ -180,10 +180,15 @@ int verify_impl(const gdn_dims *dims, int mode, const gdn_bf16 *x, const gdn_bf1
   NvtxRange range(gate_z ? "gdn_conv_verify_gated" : "gdn_conv_verify");
   int rc = check_dims(dims);
   if (rc) return rc;
-  if (mode & ~(GDN_VERIFY_OVERLAP | 0xff))
+  if (mode & ~(GDN_VERIFY_OVERLAP | GDN_VERIFY_OVERLAP_STATE | 0xff))
     return fail(GDN_ERR_INVALID_ARG, "unknown flag bits in mode 0x%x", mode);
-  const int overlap = (mode & GDN_VERIFY_OVERLAP) != 0;
+  if ((mode & GDN_VERIFY_OVERLAP) && (mode & GDN_VERIFY_OVERLAP_STATE))
+    return fail(GDN_ERR_INVALID_ARG, "GDN_VERIFY_OVERLAP and GDN_VERIFY_OVERLAP_STATE exclude each other");
+  int overlap = (mode & GDN_VERIFY_OVERLAP) ? 1 : (mode & GDN_VERIFY_OVERLAP_STATE) ? 2 : 0;
   mode &= 0xff;
+  // the state-only level exists in the d = 128 tensor-core verify; elsewhere
+  // it is the same as no flag
+  if (overlap == 2 && (dims->d_k != 128 || mode == GDN_COMMIT_SNAPSHOT)) overlap = 0;
   if ((rc = check_mode(mode))) return rc;
   if (dims->B == 0) return ok();
   GDN_NEED_PTR(x, 16);

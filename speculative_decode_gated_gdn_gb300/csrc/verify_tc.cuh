@@ -1,18 +1,22 @@
 // verify_tc.cuh -- the d = 128 verify (RECOMPUTE and DEFERRED commits) with
 // the state dot products on the tensor cores.
 //
-// Work decomposition.  One CTA of 128 threads owns one (row b, value head h);
-// thread j owns state row j (the d_v index).  At entry one thread stages the
-// head's 64 KiB fp32 state with four bulk tensor copies (boxes of 128 rows x
-// 32 columns, 128-byte swizzle), each completing on its own mbarrier.  The
-// staged tile is directly the A operand of a kind::tf32 tcgen05 product: the
-// 2T dot products of every state row with the raw conv outputs k_t, q_t are
+// Work decomposition.  One CTA owns one (row b, value head h): warps 0-3
+// (128 threads, thread j = state row j, the d_v index) convolve and run the
+// recurrence; warp 4 owns the tensor memory and issues the products.  At
+// entry one thread stages the head's 64 KiB fp32 state with four bulk tensor
+// copies (boxes of 128 rows x 32 columns, 128-byte swizzle), each completing
+// on its own mbarrier.  The staged tile is directly the A operand of a
+// kind::tf32 tcgen05 product: the 2T dot products of every state row with the
+// raw conv outputs k_t, q_t are
 //   D[j][n] = sum_i S_0[j][i] B[n][i],   B = [k_0 .. k_{T-1}; q_0 .. q_{T-1}],
 // one M = 128, N = 16, K = 128 product (16 MMAs of K = 8) accumulated in
 // TMEM, so no thread reduces anything across lanes and no pass converts the
 // state.  The tensor cores read the fp32 state truncated to tf32 (and B
-// rounded to tf32): about 2^-11 of each term, orders of magnitude inside the
-// 1e-3 relative state tolerance, since the products only enter e_t and o_t.
+// rounded to tf32): about 2^-11 of each term; the products only enter e_t and
+// o_t through per-head coefficients, and every state update, conv, norm, gate
+// and recurrence step stays in fp32.  (Measured: bf16 products need half the
+// instructions, but converting the tile costs the SM more than they save.)
 //
 // Thread i also convolves channel i of the key head's q and k and of the
 // value head's v (so the v channel it convolves is its own state row).  The
@@ -70,11 +74,12 @@ struct VtScalars {
   uint32_t tmem;
 };
 
-// Shared memory.  B holds rows 0..7 of the product's B operand (tf32,
-// K-major, no swizzle: 8-row x 16-byte core matrices, 128 bytes apart along
-// K).  For 2T > 8 a second 8-row group follows; for 2T <= 8 the descriptor's
-// second group falls on the arrays after B, whose product columns (8..15)
-// are never read.
+// Shared memory.  S is the fp32 state tile as the swizzled copies leave it.
+// B holds the product's B operand (tf32, K-major, no swizzle: 8-row x
+// 16-byte core matrices of 4 elements, 128 bytes apart along K, 8-row groups
+// 4 KiB apart).  Rows 2T..15 are never read back, so for 2T <= 8 B holds
+// only the first 8-row group and the descriptor's second group falls on the
+// arrays after it.
 template <int T>
 struct VtSmem {
   static constexpr bool kTwoGroups = 2 * T > 8;
@@ -97,14 +102,15 @@ constexpr bool vt_layout_ok() {
 template <int T>
 constexpr size_t vt_smem_bytes() {
   static_assert(vt_layout_ok<T>(), "shared-memory layout alignment");
-  // the B descriptor reads 16 rows (two 4 KiB groups) whatever T is
-  constexpr size_t b_off = offsetof(VtSmem<T>, B);
-  constexpr size_t need = b_off + 2 * 4096;
+  // the descriptors read two 8-row groups of B whatever T is
+  constexpr size_t need = offsetof(VtSmem<T>, B) + 2 * 4096;
   return sizeof(VtSmem<T>) > need ? sizeof(VtSmem<T>) : need;
 }
 
-// Byte offset of B element (n, i) in the canonical layout.
-__device__ __forceinline__ uint32_t vt_b_off(int n, int i) {
+// Byte offset of tf32 element (row n, column i) of the B operand (K = 128:
+// 8-row groups 4 KiB apart, core matrices of 4 elements 128 bytes apart
+// along K, 16 bytes per row of a core matrix).
+__device__ __forceinline__ uint32_t vt_canon32(int n, int i) {
   return uint32_t((n / 8) * 4096 + (i / 4) * 128 + (n % 8) * 16 + (i % 4) * 4);
 }
 
@@ -120,8 +126,11 @@ struct VtTaps {
   uint16_t win[kHist];
 };
 
-__device__ __forceinline__ void vt_load_taps(const VerifyParams &p, int b, int c, VtTaps &t) {
+__device__ __forceinline__ void vt_load_w(const VerifyParams &p, int c, VtTaps &t) {
   t.w = *reinterpret_cast<const uint2 *>(p.w + size_t(c) * kWidth);
+}
+
+__device__ __forceinline__ void vt_load_win(const VerifyParams &p, int b, int c, VtTaps &t) {
   const uint16_t *rb = p.ring + size_t(b) * p.R * p.C + c;
 #pragma unroll
   for (int i = 0; i < kHist; ++i) t.win[i] = rb[size_t(kWinSlot + i) * p.C];
@@ -247,13 +256,19 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   const size_t bh = size_t(b) * H_v + h;
   const int row0 = int(bh) * D;  // first row of this tile in the state map
   const uint32_t wl = p.wait_limit;
+  const bool gated = p.gz != nullptr;
 
-  // With GDN_VERIFY_OVERLAP the next kernel may start at once and this one
-  // stages its state (and reads its taps, window and pending keep) before
-  // waiting for the preceding kernel; without it, it waits first.
-  if (p.overlap) {
+  // With GDN_VERIFY_OVERLAP (level 1) the next kernel may start at once and
+  // this one stages its state (and reads its taps, window and pending keep)
+  // before waiting for the preceding kernel.  Without it the next kernel
+  // starts only after this one's wait, so a chain of level-1 calls can never
+  // run ahead of the last call below level 1 (whose own reads of the pending
+  // keep and the window may not run ahead of the preceding commit); at level
+  // 2 (GDN_VERIFY_OVERLAP_STATE) this one still stages its state before its
+  // wait, and lets the next kernel start right after it.
+  if (p.overlap == 1) {
     pdl_trigger();
-  } else {
+  } else if (p.overlap == 0) {
     pdl_wait();
     pdl_trigger();
   }
@@ -287,15 +302,21 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   __syncthreads();  // initialised barriers and the TMEM address are visible
   tc_fence_after();
 
+  // Overlap level: 0 none; 1 (GDN_VERIFY_OVERLAP) state, captures, taps,
+  // window, active and pending keep before the wait; 2
+  // (GDN_VERIFY_OVERLAP_STATE) state, captures, taps and active before it,
+  // the pending keep and the window after it.
+  const int ov = p.overlap;
   // DEFERRED: K = keep' of a commit of this (row, head) not yet applied.  It
-  // is final before the wait when the call is flagged (a commit is followed
-  // by an unflagged call), otherwise read after it.
+  // is final before the wait at level 1 (a commit is followed by a call
+  // without that flag), otherwise read after it.
   int K = 0;
   bool applied = false;
-  if (kDef && p.overlap) K = min(p.ws_pend[bh], T);
-  bool staged = false;
-  auto stage = [&]() {
+  if (kDef && ov == 1) K = min(p.ws_pend[bh], T);
+  bool staged = false, cap_staged = false;
+  auto stage = [&](bool captures) {
     staged = true;
+    cap_staged = captures;
     if (tid == 0) {
       const uint32_t extra = (b == 0 && h == 0) ? p.test_extra_tx : 0u;
 #pragma unroll
@@ -303,7 +324,7 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
         mbar_arrive_expect_tx(&sc.bar[c], kVtBoxBytes + (c == 0 ? extra : 0u));
         tma_load_2d(&sm.S[c * D * kVtBoxCols], &p.tmap_state, c * kVtBoxCols, row0, &sc.bar[c]);
       }
-      if (kDef && K >= 1) {
+      if (captures) {
         constexpr uint32_t kCap = T * D * sizeof(float);
         mbar_arrive_expect_tx(&sc.cbar, 2 * kCap + kMaxT * sizeof(float));
         bulk_g2s(&sm.ce[0][0], p.ws_e + bh * T * D, kCap, &sc.cbar);
@@ -320,7 +341,7 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
       if (staged) {
 #pragma unroll
         for (int c = 0; c < kVtBoxes; ++c) mbar_wait_limit(&sc.bar[c], 0, wl);
-        if (kDef && K >= 1) mbar_wait_limit(&sc.cbar, 0, wl);
+        if (cap_staged) mbar_wait_limit(&sc.cbar, 0, wl);
       }
       if (applied) bulk_wait_read_all();
     }
@@ -383,9 +404,15 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   // slot while the preceding kernel runs); a pending commit is applied, before
   // the wait when the call is flagged, like the state staging
   if (!active) {
-    if (kDef && !p.overlap) K = min(p.ws_pend[bh], T);
+    if (kDef && ov != 1) {
+      if (ov == 2) {  // the pending keep may be written by the preceding kernel
+        pdl_wait();
+        pdl_trigger();
+      }
+      K = min(p.ws_pend[bh], T);
+    }
     if (kDef && K >= 1) {
-      stage();
+      stage(true);
       if (!apply_and_write()) {
         give_up();
         return;
@@ -395,7 +422,7 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
       bool any = false;
       for (int r = tid; r < p.B; r += kVtThreads) any |= p.active[r] != 0;
       if (!__syncthreads_or(any)) {
-        if (p.overlap) pdl_wait();
+        if (ov) pdl_wait();
         if (row)
           for (int r = 0; r < p.B; ++r)
 #pragma unroll
@@ -418,14 +445,21 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   const int i = tid;  // conv channel i of q, k, v; state row i
   const int cq = hk * D + i, ck = H_k * D + hk * D + i, cv = 2 * H_k * D + h * D + i;
   VtTaps tq, tk, tv;
-  if (p.overlap) {
-    // flagged: state, captures, taps and window before the wait; a pending
-    // commit is applied and written back while the preceding kernel runs
-    stage();
+  if (ov) {
+    // flagged: state, captures, taps (and at level 1 the window) before the
+    // wait; at level 1 a pending commit is applied and written back while the
+    // preceding kernel runs.  At level 2 the pending keep is not known yet, so
+    // the captures are fetched whether or not a commit is pending.
+    stage(kDef && (ov == 2 || K >= 1));
     if (row) {
-      vt_load_taps(p, b, cq, tq);
-      vt_load_taps(p, b, ck, tk);
-      vt_load_taps(p, b, cv, tv);
+      vt_load_w(p, cq, tq);
+      vt_load_w(p, ck, tk);
+      vt_load_w(p, cv, tv);
+      if (ov == 1) {
+        vt_load_win(p, b, cq, tq);
+        vt_load_win(p, b, ck, tk);
+        vt_load_win(p, b, cv, tv);
+      }
       // warm L2 with this call's x, g and beta lines (a prefetch only: the
       // values are read after the wait, so a later write by the preceding
       // kernel is still what they see)
@@ -439,19 +473,31 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
       }
       find_inactive_neighbours();
     }
-    if (kDef && K >= 1 && !apply_and_write()) {
+    if (ov == 1 && kDef && K >= 1 && !apply_and_write()) {
       if (issuer) tmem_dealloc(sc.tmem, kVtTmemCols);
       give_up();
       return;
     }
     pdl_wait();
+    if (ov == 2) {
+      pdl_trigger();
+      if (kDef) K = min(p.ws_pend[bh], T);
+      if (row) {
+        vt_load_win(p, b, cq, tq);
+        vt_load_win(p, b, ck, tk);
+        vt_load_win(p, b, cv, tv);
+      }
+    }
   } else {
     if (kDef) K = min(p.ws_pend[bh], T);
-    stage();
+    stage(kDef && K >= 1);
     if (row) {
-      vt_load_taps(p, b, cq, tq);
-      vt_load_taps(p, b, ck, tk);
-      vt_load_taps(p, b, cv, tv);
+      vt_load_w(p, cq, tq);
+      vt_load_w(p, ck, tk);
+      vt_load_w(p, cv, tv);
+      vt_load_win(p, b, cq, tq);
+      vt_load_win(p, b, ck, tk);
+      vt_load_win(p, b, cv, tv);
     }
   }
 
@@ -468,7 +514,7 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
       bt[t] = p.beta[(size_t(b) * T + t) * H_v + h];
     }
     // zero-fill of the inactive rows found above
-    if (!p.overlap) find_inactive_neighbours();
+    if (!ov) find_inactive_neighbours();
     for (int r = b + 1; r < r_hi; ++r)
 #pragma unroll
       for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
@@ -477,8 +523,8 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
 #pragma unroll
         for (int t = 0; t < T; ++t) p.out[((size_t(r) * T + t) * H_v + h) * D + tid] = 0;
   }
-  // DEFERRED, unflagged: the pending commit is applied while the inputs load
-  if (kDef && !p.overlap && K >= 1 && !apply_and_write()) {
+  // DEFERRED below level 1: the pending commit is applied while the inputs load
+  if (ov != 1 && kDef && K >= 1 && !apply_and_write()) {
     if (issuer) tmem_dealloc(sc.tmem, kVtTmemCols);
     give_up();
     return;
@@ -490,10 +536,12 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
     // its accumulators, the tensor memory goes back --------------------------
     const uint32_t tmem = sc.tmem;
     if (lane == 0) {
+      const uint32_t sB = smem_u32(sm.B);
+      // tf32 straight from the swizzled fp32 tile, box by box as it lands
       bool ok = mbar_wait_spin(&sc.bready, 0, wl);
-      int issued = 0;
       constexpr uint32_t idesc = umma_idesc_tf32(D, kVtN);
-      const uint32_t sB = smem_u32(sm.B), sS = smem_u32(sm.S);
+      const uint32_t sS = smem_u32(sm.S);
+      int issued = 0;
 #pragma unroll
       for (int c = 0; c < kVtBoxes; ++c) {
         if (!ok || !mbar_wait_limit(&sc.bar[c], 0, wl)) {
@@ -504,15 +552,14 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
 #pragma unroll
         for (int kk = 0; kk < kVtBoxCols / 8; ++kk) {
           const int ks = c * (kVtBoxCols / 8) + kk;  // K step of 8 columns
-          const uint64_t da = umma_desc_sw128(sS + c * kVtBoxBytes + kk * 32);
-          const uint64_t db = umma_desc(sB + ks * 256, 128, 4096);
-          umma_tf32(tmem, da, db, idesc, ks > 0);
+          umma_tf32(tmem, umma_desc_sw128(sS + c * kVtBoxBytes + kk * 32), umma_desc(sB + ks * 256, 128, 4096),
+                    idesc, ks > 0);
           ++issued;
         }
       }
       if (ok) {
         umma_commit(&sc.mbar);
-      } else if (issued) {  // products in flight must finish before the columns go back
+      } else if (issued) {  // products in flight finish before the columns go back
         umma_commit(&sc.fbar);
         mbar_wait_limit(&sc.fbar, 0, wl);
       }
@@ -533,8 +580,8 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   unsigned char *bsm = reinterpret_cast<unsigned char *>(sm.B);
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(t, i)) = f2tf32(yk[t]);
-    *reinterpret_cast<uint32_t *>(bsm + vt_b_off(T + t, i)) = f2tf32(yq[t]);
+    *reinterpret_cast<uint32_t *>(bsm + vt_canon32(t, i)) = f2tf32(yk[t]);
+    *reinterpret_cast<uint32_t *>(bsm + vt_canon32(T + t, i)) = f2tf32(yq[t]);
   }
   fence_async_smem();  // B is read by the tensor cores
   mbar_arrive(&sc.bready);
@@ -594,7 +641,6 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
 
   // ---- row j = tid: its 2T products from TMEM lane j, then the recurrence ------
   const int j = tid;
-  const bool gated = p.gz != nullptr;
   uint16_t zt[T], wj = 0;
   if (gated) {
     wj = p.gw[j];

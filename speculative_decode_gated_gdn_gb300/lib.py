@@ -26,6 +26,7 @@ GDN_COMMIT_RECOMPUTE = 0
 GDN_COMMIT_SNAPSHOT = 1
 GDN_COMMIT_DEFERRED = 2
 GDN_VERIFY_OVERLAP = 0x100
+GDN_VERIFY_OVERLAP_STATE = 0x200
 GDN_STATUS_TIMEOUT = 2
 GDN_STATUS_BAD_KEEP = 1
 GDN_STATUS_BAD_ROW = 4

@@ -1,6 +1,7 @@
 """GPU parity at the batch/draft sweep's large cohorts (B = 64 at T = 2 and 8,
 B = 32 at T = 5; 32 value heads of 128), in the launch configuration the
-benchmark times (layers after the first flagged GDN_VERIFY_OVERLAP).
+benchmark times (layers after the first flagged GDN_VERIFY_OVERLAP, the first
+GDN_VERIFY_OVERLAP_STATE in DEFERRED mode).
 
 Three layers over three cycles, the last B/4 rows inactive, keep ~ U{0..T}.
 Every cycle: sampled (layer, row, head) units against the oracle (each unit
@@ -17,6 +18,7 @@ import torch
 from speculative_decode_gated_gdn_gb300 import lib as L
 from speculative_decode_gated_gdn_gb300 import synth
 from tests.gdn_harness import GpuStack, OracleUnit, check_out, check_state, dev_bf16, host_bits
+from tests.test_verify_commit_gpu import bench_verify_mode
 
 pytestmark = pytest.mark.gpu
 N_LAYERS, N_CYCLES = 3, 3
@@ -50,7 +52,7 @@ def test_large_cohort_sampled_parity(gdn, B, T, mode):
     for c in range(N_CYCLES):
         cy = synth.cycle_inputs(geom, seed, c, N_LAYERS)
         for l in range(N_LAYERS):
-            vmode = mode | (L.GDN_VERIFY_OVERLAP if l > 0 else 0)
+            vmode = bench_verify_mode(mode, l)
             L.gdn_conv_verify(gpu.dims, vmode, dev_bf16(cy["x"][l]), gpu.w[l], torch.from_numpy(cy["g"][l]).cuda(),
                               torch.from_numpy(cy["beta"][l]).cuda(), gpu.state[l], gpu.ring[l], gpu.offsets,
                               gpu.active, gpu.out[l], gpu.ws[l])

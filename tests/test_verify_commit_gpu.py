@@ -251,8 +251,9 @@ def test_stack_30_layers_256_cycles_sampled(gdn, mode):
         xd, gd, bd = dev_pool[c % pool]
         for l in range(n_layers):
             # the launch configuration the benchmark times: layers after the
-            # first stage their state while the previous layer's verify ends
-            vmode = gpu.mode | (L.GDN_VERIFY_OVERLAP if l > 0 else 0)
+            # first stage their state while the previous layer's verify ends;
+            # in DEFERRED mode the first stages its state beside the commit
+            vmode = bench_verify_mode(gpu.mode, l)
             L.gdn_conv_verify(gpu.dims, vmode, xd[l], gpu.w[l], gd[l], bd[l], gpu.state[l], gpu.ring[l],
                               gpu.offsets, gpu.active, gpu.out[l], gpu.ws[l])
         o_units = [u.verify(cy["x"][u.layer], cy["g"][u.layer], cy["beta"][u.layer], active[u.b]) for u in units]
@@ -294,13 +295,51 @@ def test_overlap_flag_is_bit_identical(gdn):
     assert torch.equal(a[1], b[1]) and np.array_equal(a[2], b[2]) and torch.equal(a[3], b[3])
 
 
+def bench_verify_mode(mode, layer):
+    """The flags the benchmark puts on layer `layer` of a cycle."""
+    if layer > 0:
+        return mode | L.GDN_VERIFY_OVERLAP
+    return mode | (L.GDN_VERIFY_OVERLAP_STATE if mode == L.GDN_COMMIT_DEFERRED else 0)
+
+
+@pytest.mark.parametrize("T", [2, 8], ids=["T2", "T8"])
+def test_overlap_state_flag_is_bit_identical(gdn, T):
+    """DEFERRED cycles with the first layer flagged GDN_VERIFY_OVERLAP_STATE
+    (and the others GDN_VERIFY_OVERLAP) give the same bytes as unflagged
+    calls: outputs every cycle, then the flushed state, rings and offsets."""
+    geom = synth.Geometry(B=4, T=T, H_k=2, H_v=4, d=128)
+    st = synth.layer_state(geom, 15, 3)
+    active = synth.active_mask(4, (3,))
+    runs = []
+    for flagged in (False, True):
+        gpu = GpuStack(geom, st, active, L.GDN_COMMIT_DEFERRED, 3)
+        outs = []
+        for c in range(4):
+            cy = synth.cycle_inputs(geom, 15, c, 3)
+            for l in range(3):
+                mode = bench_verify_mode(gpu.mode, l) if flagged else gpu.mode
+                L.gdn_conv_verify(gpu.dims, mode, dev_bf16(cy["x"][l]), gpu.w[l],
+                                  torch.from_numpy(cy["g"][l]).cuda(), torch.from_numpy(cy["beta"][l]).cuda(),
+                                  gpu.state[l], gpu.ring[l], gpu.offsets, gpu.active, gpu.out[l], gpu.ws[l])
+            outs.append(gpu.out.clone())
+            gpu.commit(cy["keep"])
+        gpu.flush()
+        torch.cuda.synchronize()
+        runs.append((outs, gpu.state.clone(), host_bits(gpu.ring), gpu.offsets.clone()))
+    (oa, sa, ra, fa), (ob, sb, rb, fb) = runs
+    for c, (a, b) in enumerate(zip(oa, ob)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"cycle {c} outputs"
+    assert torch.equal(sa, sb) and np.array_equal(ra, rb) and torch.equal(fa, fb)
+    assert L.gdn_get_status(clear=True) == 0
+
+
 def test_unknown_mode_flag_rejected(gdn):
     geom = synth.TINY
     st = synth.layer_state(geom, 0, 1)
     gpu = GpuStack(geom, st, synth.active_mask(1), L.GDN_COMMIT_RECOMPUTE, 1)
     cy = synth.cycle_inputs(geom, 0, 0, 1)
     with pytest.raises(L.GdnError) as ei:
-        L.gdn_conv_verify(gpu.dims, 0x200, dev_bf16(cy["x"][0]), gpu.w[0],
+        L.gdn_conv_verify(gpu.dims, 0x400, dev_bf16(cy["x"][0]), gpu.w[0],
                           torch.from_numpy(cy["g"][0]).cuda(), torch.from_numpy(cy["beta"][0]).cuda(),
                           gpu.state[0], gpu.ring[0], gpu.offsets, gpu.active, gpu.out[0], gpu.ws[0])
     assert ei.value.code == L.GDN_ERR_INVALID_ARG
