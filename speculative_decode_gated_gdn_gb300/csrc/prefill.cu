@@ -18,7 +18,9 @@
 // in parallel over chunks; the last three run sequentially over chunks.
 //
 // Kernels (one stream, in order):
-//   prefill_conv_kernel   conv + SiLU + L2 norm of every token  -> Q, K, V (fp32)
+//   prefill_conv_kernel   conv + SiLU + L2 norm of every token  -> Q, K, V (fp32;
+//                         at d = 128 prefill_conv128_kernel, straight into the
+//                         operand tiles)
 //   prefill_chunk_tc_kernel  per (chunk pair, value head): G, A, Tm, W, U, Pm
 //                         (the products on tcgen05)
 //   prefill_state_kernel  per (value head, 32-row d_v slice): the chunk loop
@@ -49,7 +51,8 @@ struct PrefillParams {
   // bf16 hi/lo operand tiles for the tensor-core chunk kernel, one 64-token
   // chunk per tile, in the tcgen05 K-major no-swizzle canonical layout
   // (8-row x 16-byte core matrices; K-direction stride 128 B).
-  uint16_t *qn_hi, *qn_lo;  // [B][H_k][NCp] tiles of q  as [t][i] (K dim = d)
+  uint16_t *qn_hi;          // [B][H_k][NCp] tiles of q  as [t][i] (K dim = d), bf16
+                            // only: q enters the outputs alone
   uint16_t *kn_hi, *kn_lo;  // [B][H_k][NCp] tiles of k  as [t][i]
   uint16_t *kt_hi, *kt_lo;  // [B][H_k][NCp] tiles of k^T as [i][t] (K dim = 64 tokens)
   uint16_t *vt_hi, *vt_lo;  // [B][H_v][NCp] tiles of v^T as [j][t]
@@ -62,7 +65,7 @@ struct PrefillParams {
 };
 
 struct PrefillWs {
-  size_t q, k, W, U, Gc, Pm, qn_hi, qn_lo, kn_hi, kn_lo, kt_hi, kt_lo, vt_hi, vt_lo, w_hi, w_lo, pm_hi, total;
+  size_t q, k, W, U, Gc, Pm, qn_hi, kn_hi, kn_lo, kt_hi, kt_lo, vt_hi, vt_lo, w_hi, w_lo, pm_hi, total;
 };
 
 // The sequential pass runs on the tensor cores at d = 128 (one TMEM lane per
@@ -83,7 +86,7 @@ inline PrefillWs prefill_ws(int B, int L, int H_k, int H_v, int D) {
   w.Gc = o, o += align256(sizeof(float) * size_t(B) * H_v * Lp);
   w.Pm = o, o += tc ? 0 : align256(sizeof(float) * size_t(B) * H_v * NC * kChunk * kChunk);
   const size_t tile = size_t(kChunk) * D * sizeof(uint16_t);
-  size_t *hk_tiles[6] = {&w.qn_hi, &w.qn_lo, &w.kn_hi, &w.kn_lo, &w.kt_hi, &w.kt_lo};
+  size_t *hk_tiles[5] = {&w.qn_hi, &w.kn_hi, &w.kn_lo, &w.kt_hi, &w.kt_lo};
   for (size_t *f : hk_tiles) *f = o, o += align256(tile * B * H_k * NCp);
   w.vt_hi = o, o += align256(tile * B * H_v * NCp);
   w.vt_lo = o, o += align256(tile * B * H_v * NCp);
@@ -213,17 +216,167 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
   if (kind == 1) store_tiles<D>(y, tid, nullptr, nullptr, p.kt_hi + tbase, p.kt_lo + tbase);
   __syncthreads();
   {
-    uint16_t *nh = (kind == 0 ? p.qn_hi : p.kn_hi) + tbase, *nl = (kind == 0 ? p.qn_lo : p.kn_lo) + tbase;
+    uint16_t *nh = (kind == 0 ? p.qn_hi : p.kn_hi) + tbase, *nl = kind == 0 ? nullptr : p.kn_lo + tbase;
     for (int u = tid; u < kChunk * (D / 8); u += D) {
       const int t = u / (D / 8), i8 = (u % (D / 8)) * 8;
       const uint32_t o = canon_off(t, i8, D) / 2;
-      store8_split(&s_y[t][i8], nh + o, nl + o);
+      store8_split(&s_y[t][i8], nh + o, nl ? nl + o : nullptr);
     }
   }
   if (state_pass_tc(D) || chunk >= p.NC) return;
   float *dst = (kind == 0 ? p.q : p.k) + ((size_t(b) * H_k + hk) * Lp + t0) * D + tid;
 #pragma unroll
   for (int i = 0; i < kChunk; ++i) dst[size_t(i) * D] = y[i];
+}
+
+// ---------------------------------------------------------------------------
+// 1b. conv + activation + L2 norm at d = 128, for the tensor-core passes.
+//    Block = one chunk of 64 tokens of one head (q, k or v) of one row, 128
+//    threads; thread (o, g) = (tid % 16, tid / 16) owns channels 8o..8o+7 of
+//    tokens 8g..8g+7.  That 8 x 8 block is exactly one 128-byte core matrix
+//    of every operand tile the chunk feeds (the [t][i] tiles of q and k, the
+//    [i][t] tiles of k and v), so each thread reads its inputs as 16-byte
+//    runs of one token row, and a token's squared norm is the sum over the
+//    16 lanes of its half warp.  Each 16 KiB tile is staged in shared memory
+//    (the 16-byte rows of a 128-byte line rotated by an XOR key, so that the
+//    lanes of a warp hit distinct banks) and copied out by the block as
+//    whole contiguous lines.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(w[q] << 16);
+    f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+  }
+}
+
+// Shared staging of one bf16 hi/lo tile pair (64 x 128 elements = 1024
+// lines' worth of 16-byte rows each): row r of 128-byte line l sits at
+// position r ^ key(l) of the line.
+struct ConvStage {
+  uint4 hi[kChunk * 128 / 8], lo[kChunk * 128 / 8];
+};
+
+// One core matrix (8 rows of 8 values) split into bf16 hi/lo into line
+// `line` of the staging tiles.
+__device__ __forceinline__ void stage_core_split(const float (&v)[8][8], ConvStage &st, int line, int key) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // the rounding of store8_split
+      const __nv_bfloat162 hv = __floats2bfloat162_rn(v[r][2 * q], v[r][2 * q + 1]);
+      const __nv_bfloat162 lv =
+          __floats2bfloat162_rn(v[r][2 * q] - __low2float(hv), v[r][2 * q + 1] - __high2float(hv));
+      h[q] = *reinterpret_cast<const uint32_t *>(&hv);
+      l[q] = *reinterpret_cast<const uint32_t *>(&lv);
+    }
+    st.hi[line * 8 + (r ^ key)] = make_uint4(h[0], h[1], h[2], h[3]);
+    st.lo[line * 8 + (r ^ key)] = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// The staged tile pair out to global memory, 16 contiguous bytes per thread
+// per step.  `tkey` selects the key of a line: its index mod 8 ([t][i]
+// tiles, 16 lines per token group) or its index / 8 mod 8 ([i][t] tiles, 8
+// lines per channel group).
+// `lo` may be null (the hi tile alone).
+__device__ __forceinline__ void flush_stage(const ConvStage &st, uint16_t *hi, uint16_t *lo, bool tkey) {
+  __syncthreads();
+  uint4 *gh = reinterpret_cast<uint4 *>(hi), *gl = reinterpret_cast<uint4 *>(lo);
+  for (int i = threadIdx.x; i < kChunk * 128 / 8; i += blockDim.x) {
+    const int line = i >> 3, key = (tkey ? line >> 3 : line) & 7;
+    const int src = line * 8 + ((i & 7) ^ key);
+    gh[i] = st.hi[src];
+    if (lo) gl[i] = st.lo[src];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(128, 4) prefill_conv128_kernel(const PrefillParams p) {
+  constexpr int D = 128;
+  const int chunk = blockIdx.x, head = blockIdx.y, b = blockIdx.z;  // head in [0, 2 H_k + H_v)
+  const int tid = threadIdx.x, o = tid & 15, g = tid >> 4;
+  pdl_wait();
+  pdl_trigger();
+  const int H_k = p.H_k, C = p.C, R = p.R, L = p.L;
+  const int kind = head < H_k ? 0 : head < 2 * H_k ? 1 : 2;
+  const int c0 = head * D + 8 * o;  // first of this thread's channels
+  // raw inputs of tokens t1-3 .. t1+7: from the prompt, the committed window
+  // (ring slots 0..2) before it, zeros past it
+  const int t1 = chunk * kChunk + 8 * g;
+  uint4 xr[8 + kHist];
+#pragma unroll
+  for (int k = 0; k < 8 + kHist; ++k) {
+    const int t = t1 - kHist + k;
+    xr[k] = t >= L   ? make_uint4(0, 0, 0, 0)
+            : t >= 0 ? *reinterpret_cast<const uint4 *>(p.x + (size_t(b) * L + t) * C + c0)
+                     : *reinterpret_cast<const uint4 *>(p.ring + (size_t(b) * R + kWinSlot + kHist + t) * C + c0);
+  }
+  float y[8][8];  // [token][channel]
+  const uint4 *wp = reinterpret_cast<const uint4 *>(p.w + size_t(c0) * kWidth);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // channels 2q, 2q+1: their taps are 16 bytes
+    float w[8];
+    unpack8(wp[q], w);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < kWidth; ++i) {
+        const uint32_t word = q == 0 ? xr[r + i].x : q == 1 ? xr[r + i].y : q == 2 ? xr[r + i].z : xr[r + i].w;
+        acc0 = fmaf(w[i], __uint_as_float(word << 16), acc0);
+        acc1 = fmaf(w[kWidth + i], __uint_as_float(word & 0xffff0000u), acc1);
+      }
+      const bool live = t1 + r < L;
+      y[r][2 * q] = live ? (p.act ? silu_fast(acc0) : acc0) : 0.f;
+      y[r][2 * q + 1] = live ? (p.act ? silu_fast(acc1) : acc1) : 0.f;
+    }
+  }
+  __shared__ ConvStage st;
+  const size_t tile = size_t(kChunk) * D;  // elements per bf16 tile
+  // this thread's core matrix: line g * 16 + o of a [t][i] tile (K = D),
+  // line o * 8 + g of an [i][t] tile (K = 64); both keyed by o % 8
+  const int nat = g * (D / 8) + o, tra = o * (kChunk / 8) + g, key = o & 7;
+  if (kind == 2) {
+    float yt[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) yt[c][r] = y[r][c];
+    const size_t tb = ((size_t(b) * p.H_v + (head - 2 * H_k)) * p.NCp + chunk) * tile;
+    stage_core_split(yt, st, tra, key);
+    flush_stage(st, p.vt_hi + tb, p.vt_lo + tb, true);
+    return;
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) ss = fmaf(y[r][c], y[r][c], ss);
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);  // the 16 lanes of this token
+    float inv = rsqrtf(ss + kNormEps);
+    if (kind == 0) inv *= rsqrtf(float(D));
+#pragma unroll
+    for (int c = 0; c < 8; ++c) y[r][c] *= inv;
+  }
+  const int hk = kind == 0 ? head : head - H_k;
+  const size_t tb = ((size_t(b) * H_k + hk) * p.NCp + chunk) * tile;
+  stage_core_split(y, st, nat, key);
+  if (kind == 0) {
+    flush_stage(st, p.qn_hi + tb, nullptr, false);
+    return;
+  }
+  flush_stage(st, p.kn_hi + tb, p.kn_lo + tb, false);
+  float yt[8][8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) yt[c][r] = y[r][c];
+  stage_core_split(yt, st, tra, key);
+  flush_stage(st, p.kt_hi + tb, p.kt_lo + tb, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -235,10 +388,12 @@ __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) 
 //                                   chunk are the diagonal 64 x 64 blocks
 //      W  = (Tm diag(beta gamma)) K,  U = (Tm diag(beta)) V  (128 x d, K dim
 //           128 tokens; Tm is block diagonal, so the chunks stay separate)
-//    Each product is taken in three bf16 passes, x = x_hi + x_lo with
-//    x_hi = bf16(x), x_lo = bf16(x - x_hi):  a b ~ a_hi b_hi + a_hi b_lo +
-//    a_lo b_hi, which keeps about 16 bits of the fp32 operands (the state
-//    tolerance is 1e-3 relative; a single bf16 pass would sit at that level).
+//    The products that reach the state (KK, W, U) are taken in three bf16
+//    passes, x = x_hi + x_lo with x_hi = bf16(x), x_lo = bf16(x - x_hi):
+//    a b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi, which keeps about 16 bits of
+//    the fp32 operands (a single pass sits near the 1e-3 relative state
+//    tolerance once the decay is weak enough for the state to carry over many
+//    chunks).  QK only forms Pm, which only enters the bf16 outputs: one pass.
 //    The UT transform itself is a forward substitution on the CUDA cores:
 //    each thread solves one column of one chunk's Tm, without block barriers.
 // ---------------------------------------------------------------------------
@@ -252,11 +407,17 @@ struct TcLayout {
   static constexpr uint32_t tr_tile = uint32_t(D) * kChunk * 2;    // one [i][t] tile
   static constexpr uint32_t sq_op = kPairRows * kPairRows * 2;     // a 128 x 128 bf16 operand
   static constexpr uint32_t R0 = 0, R1 = 65536, R2 = 131072, R3 = 196608;
-  static constexpr int kAStride = kChunk + 1;  // odd stride: the epilogue's row writes hit distinct banks
-  static constexpr uint32_t solve_bytes = 2 * kChunk * kAStride * 4;
-  static constexpr uint32_t misc = R3 + solve_bytes;              // G[128], beta[128]
-  static constexpr uint32_t total = misc + 2 * kPairRows * 4;
+  // the UT solve's columns, in the second half of R1 (q takes the first;
+  // the U operand's lo tile reuses this half after the solve)
+  static constexpr uint32_t xs_off = 32768;
+  // A of each chunk stored transposed, At[u][r] = A[r][u]: the epilogue's
+  // writes (thread r, one column u at a time) are consecutive, and the
+  // solve reads 16 rows of a column as four broadcast 16-byte loads
+  static constexpr uint32_t solve_bytes = 2 * kChunk * kChunk * 4;
+  static constexpr uint32_t misc = R3 + solve_bytes;              // G[128], beta[128], beta gamma[128]
+  static constexpr uint32_t total = misc + 3 * kPairRows * 4;
   static_assert(2 * nat_pair <= 65536 && 4 * tr_tile <= 65536 && 2 * sq_op <= 65536, "regions");
+  static_assert(nat_pair <= xs_off && xs_off + 2 * kChunk * kChunk * 4 <= 65536, "solve columns");
 };
 
 template <int D>
@@ -266,9 +427,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   __shared__ __align__(8) uint64_t bars[6];
   __shared__ uint32_t s_tmem;
   __shared__ float s_wsum[4];
-  float(*As)[kChunk][Lay::kAStride] = reinterpret_cast<float(*)[kChunk][Lay::kAStride]>(smem + Lay::R3);
+  float(*At)[kChunk][kChunk] = reinterpret_cast<float(*)[kChunk][kChunk]>(smem + Lay::R3);
   float *sG = reinterpret_cast<float *>(smem + Lay::misc);
   float *sBeta = sG + kPairRows;
+  float *sColW = sBeta + kPairRows;  // beta_s gamma_s of column s of the pair
 
   const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -294,11 +456,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   const size_t tile_el = size_t(kChunk) * D;
   if (tid == 0) {
     const size_t kq = ((size_t(b) * H_k + hk) * p.NCp + c0) * tile_el;
-    mbar_arrive_expect_tx(&bars[0], 4 * Lay::nat_pair);
+    mbar_arrive_expect_tx(&bars[0], 3 * Lay::nat_pair);
     bulk_g2s(smem + Lay::R0, p.kn_hi + kq, Lay::nat_pair, &bars[0]);
     bulk_g2s(smem + Lay::R0 + Lay::nat_pair, p.kn_lo + kq, Lay::nat_pair, &bars[0]);
     bulk_g2s(smem + Lay::R1, p.qn_hi + kq, Lay::nat_pair, &bars[0]);
-    bulk_g2s(smem + Lay::R1 + Lay::nat_pair, p.qn_lo + kq, Lay::nat_pair, &bars[0]);
     mbar_arrive_expect_tx(&bars[1], 4 * Lay::tr_tile);
     bulk_g2s(smem + Lay::R2, p.kt_hi + kq, 2 * Lay::tr_tile, &bars[1]);
     bulk_g2s(smem + Lay::R2 + 2 * Lay::tr_tile, p.kt_lo + kq, 2 * Lay::tr_tile, &bars[1]);
@@ -337,19 +498,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
       constexpr uint32_t idesc = umma_idesc_bf16(kPairRows, kPairRows);
       constexpr uint32_t sbo = (D / 8) * 128;
       const uint32_t aK[2] = {sbase + Lay::R0, sbase + Lay::R0 + Lay::nat_pair};
-      const uint32_t aQ[2] = {sbase + Lay::R1, sbase + Lay::R1 + Lay::nat_pair};
+      const uint32_t aQ = sbase + Lay::R1;
 #pragma unroll
       for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           umma_bf16(tmem, umma_desc(aK[pa[ps]] + k * 256, 128, sbo), umma_desc(aK[pb[ps]] + k * 256, 128, sbo),
                     idesc, ps | k);
+      // QK only feeds Pm, which only enters the bf16 outputs: one pass
 #pragma unroll
-      for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16(tmem + 128, umma_desc(aQ[pa[ps]] + k * 256, 128, sbo),
-                    umma_desc(aK[pb[ps]] + k * 256, 128, sbo), idesc, ps | k);
+      for (int k = 0; k < D / 16; ++k)
+        umma_bf16(tmem + 128, umma_desc(aQ + k * 256, 128, sbo), umma_desc(aK[0] + k * 256, 128, sbo), idesc,
+                  k > 0);
     }
     umma_commit(&bars[2]);  // also arrives when nothing was issued
   }
@@ -374,7 +534,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
       for (int j = 0; j < 32; ++j) {
         const int sl = cc + j;
         const float decay = sl <= tl ? expf(Gt - sG[cb + sl]) : 0.f;
-        As[q][tl][sl] = sl < tl ? bq * decay * kk[j] : 0.f;
+        At[q][sl][tl] = sl < tl ? bq * decay * kk[j] : 0.f;
         pm[j] = decay * qk[j];
       }
       if (chunk < p.NC) {
@@ -394,42 +554,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   tc_fence_after();
 
   // ---- UT transform: column s of chunk q of Tm, by forward substitution ----
+  // Thread s keeps its column x in shared memory (the free half of the q
+  // region, Tm[u][s] of chunk q at xs[q][u][s ^ 8 (u % 8)]: conflict-free
+  // across the warp, and row runs of 8 columns stay contiguous) and solves
+  // it in blocks of 16 rows: first the block's right-hand side loses the
+  // contribution of every row already solved (16 independent accumulators),
+  // then a 16-step substitution inside the block.
+  constexpr int kBlk = 16;
+  const int s = tl;
+  float *xq = reinterpret_cast<float *>(smem + Lay::R1 + Lay::xs_off) + q * kChunk * kChunk;
+  auto xsw = [](int u, int col) { return u * kChunk + (col ^ ((u & 7) << 3)); };
   if (ok) {
-    const int s = tl;
-    float x[kChunk];
+    for (int ib = 0; ib < kChunk / kBlk; ++ib) {
+      const int r0 = ib * kBlk;
+      float y[kBlk];
 #pragma unroll
-    for (int r = 0; r < kChunk; ++r) {
-      float a0 = r == s ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      for (int rr = 0; rr < kBlk; ++rr) y[rr] = r0 + rr == s ? 1.f : 0.f;
+      for (int u = 0; u < r0; ++u) {
+        const float xu = xq[xsw(u, s)];
+        const float4 *ac = reinterpret_cast<const float4 *>(&At[q][u][r0]);
 #pragma unroll
-      for (int u = 0; u + 3 < r; u += 4) {
-        a0 = fmaf(-As[q][r][u], x[u], a0);
-        a1 = fmaf(-As[q][r][u + 1], x[u + 1], a1);
-        a2 = fmaf(-As[q][r][u + 2], x[u + 2], a2);
-        a3 = fmaf(-As[q][r][u + 3], x[u + 3], a3);
+        for (int v = 0; v < kBlk / 4; ++v) {
+          const float4 a = ac[v];
+          y[4 * v] = fmaf(-a.x, xu, y[4 * v]);
+          y[4 * v + 1] = fmaf(-a.y, xu, y[4 * v + 1]);
+          y[4 * v + 2] = fmaf(-a.z, xu, y[4 * v + 2]);
+          y[4 * v + 3] = fmaf(-a.w, xu, y[4 * v + 3]);
+        }
       }
 #pragma unroll
-      for (int u = r & ~3; u < r; ++u) a0 = fmaf(-As[q][r][u], x[u], a0);
-      x[r] = (a0 + a1) + (a2 + a3);
+      for (int rr = 0; rr < kBlk; ++rr) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: a short dependency chain
+#pragma unroll
+        for (int c = 0; c < rr; ++c) d[c & 3] = fmaf(At[q][r0 + c][r0 + rr], y[c], d[c & 3]);
+        y[rr] -= (d[0] + d[1]) + (d[2] + d[3]);
+        xq[xsw(r0 + rr, s)] = y[rr];
+      }
     }
-    // operands of W and U: Tm scaled by beta_s gamma_s (resp. beta_s) per
-    // column, block diagonal over the pair, split into bf16 hi/lo
-    const int ks = q * kChunk + s, kz = (1 - q) * kChunk + s;
-    const float bs = sBeta[ks], bgs = bs * expf(sG[ks]);
+  }
+  // operands of W and U: Tm scaled by beta_s gamma_s (resp. beta_s) per
+  // column s, block diagonal over the pair, split into bf16 hi/lo.  Written
+  // by rows: item (chunk, row t, columns 8 c8 .. 8 c8 + 7) is one 16-byte row
+  // of a core matrix, and eight consecutive threads (rows t .. t+7) fill a
+  // whole 128-byte core matrix.
+  if (ok) sColW[tid] = sBeta[tid] * expf(sG[tid]);  // column tid of the pair
+  __syncthreads();  // every column is solved (and the U lo tile may reuse its space below)
+  constexpr int kItems = kPairRows * kChunk / 8 / kTcThreads;  // 8 per thread
+  float rv[kItems][8];
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int idx = it * kTcThreads + tid, qq = idx / (kChunk * 8), t = idx % kChunk, c8 = (idx / kChunk) % 8;
+    const float4 *src = reinterpret_cast<const float4 *>(
+        reinterpret_cast<const float *>(smem + Lay::R1 + Lay::xs_off) + qq * kChunk * kChunk + xsw(t, 8 * c8));
+    const float4 lo4 = src[0], hi4 = src[1];
+    rv[it][0] = lo4.x, rv[it][1] = lo4.y, rv[it][2] = lo4.z, rv[it][3] = lo4.w;
+    rv[it][4] = hi4.x, rv[it][5] = hi4.y, rv[it][6] = hi4.z, rv[it][7] = hi4.w;
+  }
+  __syncthreads();
+  if (ok) {
     uint16_t *awh = reinterpret_cast<uint16_t *>(smem + Lay::R0), *awl = awh + kPairRows * kPairRows;
     uint16_t *auh = reinterpret_cast<uint16_t *>(smem + Lay::R1), *aul = auh + kPairRows * kPairRows;
 #pragma unroll
-    for (int r = 0; r < kChunk; ++r) {
-      const int tr = q * kChunk + r;
-      uint16_t hi, lo;
-      const uint32_t o = canon_off(tr, ks, kPairRows) / 2;
-      split_bf16(x[r] * bgs, hi, lo);
-      awh[o] = hi, awl[o] = lo;
-      split_bf16(x[r] * bs, hi, lo);
-      auh[o] = hi, aul[o] = lo;
+    for (int it = 0; it < kItems; ++it) {
+      const int idx = it * kTcThreads + tid, qq = idx / (kChunk * 8), t = idx % kChunk, c8 = (idx / kChunk) % 8;
+      const int tr = qq * kChunk + t, ks0 = qq * kChunk + 8 * c8;
+      float w[8], u[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        w[e] = rv[it][e] * sColW[ks0 + e];
+        u[e] = rv[it][e] * sBeta[ks0 + e];
+      }
+      const uint32_t o = canon_off(tr, ks0, kPairRows) / 2;
+      store8_split(w, awh + o, awl + o);
+      store8_split(u, auh + o, aul + o);
     }
     // the off-diagonal 64 x 64 quadrants are zero: in the canonical layout
     // each 8-row group of a quadrant is one contiguous kilobyte
-    (void)kz;
     const uint4 z = make_uint4(0, 0, 0, 0);
     constexpr int kQuadU4 = kChunk / 8 * 1024 / 16;  // uint4 per quadrant
 #pragma unroll
@@ -654,36 +854,45 @@ __global__ void __launch_bounds__(kStateThreads) prefill_state_kernel(const Pref
 //     per (row, value head); state row j <-> TMEM lane j.  The fp32 state
 //     stays in TMEM for the whole prompt; per chunk of n tokens (t, s index
 //     tokens, i, j state columns and rows):
-//       E'^T = S W^T,   QS^T = S Q^T       M = 128 rows j, N = 64 tokens, K = d
+//       E'^T = S W^T,   QS^T = S Q^T       M = 128 rows j, N = 64 tokens each, K = d
 //       E = U - E',  E~_t = exp(G_n - G_t) E_t,  S <- gamma_n S   (epilogue)
 //       O^T = E^T Pm^T                     N = 64 tokens, K = 64 tokens
 //       S += E~^T K                        N = d columns, K = 64 tokens
 //       o_t = gamma_t QS^T + O^T,  then the bf16 hi/lo tiles of the new S
 //     The products that feed the state (E', S += ...) take three bf16 passes
-//     (hi hi, hi lo, lo hi); those that only feed the bf16 output take two
-//     (A split, B rounded once).  Operand tiles of the next chunk are fetched
-//     as soon as the products of this chunk that read them are done.  The
-//     epilogues are spread over 16 warps: warp w reads TMEM lane quarter
-//     w % 4 and takes column group w / 4 (16 tokens or 32 state columns);
-//     the per-token decay factors are computed once per chunk.
+//     (hi hi, hi lo, lo hi); those that only feed the bf16 outputs (QS^T,
+//     O^T) take one (both operands rounded to bf16 once: about 2^-9 of each
+//     term, far inside the output tolerance, and nothing of it flows back
+//     into the state).  The first products stack [W_hi; Q_hi; W_lo] into one
+//     N = 192 operand against S_hi, so E'^T arrives as two column ranges the
+//     epilogue adds.  The chunk's [E' | QS | E'] columns alternate between two
+//     TMEM ranges by chunk parity: the next chunk's first products run while
+//     this chunk's outputs are read out, after the bf16 hi/lo tiles of the
+//     new state (all the next products wait for) are written.  Operand tiles
+//     of the next chunk are fetched as soon as the products of this chunk
+//     that read them are done.  The epilogues are spread over 16 warps: warp
+//     w reads TMEM lane quarter w % 4 and takes column group w / 4 (16 tokens
+//     or 32 state columns); the per-token decay factors are computed once per
+//     chunk.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kStCols = 512;
-constexpr uint32_t kColE = 0, kColQS = 64, kColEP = 128, kColS = 256;
+// [E'a | QS | E'c] of a chunk at kColE (even chunks) or kColE1 (odd chunks);
+// O^T later takes the E'c columns; the state at kColS
+constexpr uint32_t kColE = 0, kColE1 = 192, kColS = 384;
 constexpr int kStThreads = 512;
 
 struct StLayout {  // d = 128, byte offsets in dynamic shared memory
   static constexpr uint32_t S_hi = 0, S_lo = 32768;          // S [j][i], K = 128: A operand
-  static constexpr uint32_t W_lo = 65536, W_hi = 81920;      // W [t][i], K = 128: B operand
-  static constexpr uint32_t Q_hi = 98304;                    // Q [t][i] right after W_hi: [W; Q] is
-                                                             // one 128-row B operand
+  static constexpr uint32_t W_hi = 65536, Q_hi = 81920;      // W, Q [t][i], K = 128: B operands;
+  static constexpr uint32_t W_lo = 98304;                    // [W_hi; Q_hi; W_lo] is one 192-row one
   static constexpr uint32_t Kt_hi = 114688, Kt_lo = 131072;  // K^T [i][t], K = 64: B operand
   static constexpr uint32_t Pm_hi = 147456;                  // Pm [t][s], K = 64: B operand
-  static constexpr uint32_t E_hi = 155648, E_lo = 172032;    // E^T [j][s], K = 64: A operand
+  static constexpr uint32_t E_hi = 155648;                   // E^T [j][s], K = 64: A operand (bf16)
   static constexpr uint32_t Et_hi = 188416, Et_lo = 204800;  // decayed E^T [j][t], K = 64: A operand
   static constexpr uint32_t G = 221184;                      // [2][64] within-chunk G, by chunk parity
-  static constexpr uint32_t Dec = G + 2 * kChunk * 4;        // [64] exp(G_n - G_t), 0 past n
-  static constexpr uint32_t Gam = Dec + kChunk * 4;          // [64] exp(G_t)
-  static constexpr uint32_t total = Gam + kChunk * 4;
+  static constexpr uint32_t Dec = G + 2 * kChunk * 4;        // [2][64] exp(G_n - G_t), 0 past n
+  static constexpr uint32_t Gam = Dec + 2 * kChunk * 4;      // [2][64] exp(G_t)
+  static constexpr uint32_t total = Gam + 2 * kChunk * 4;
 };
 
 __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const PrefillParams p) {
@@ -770,8 +979,15 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       const float4 f = *reinterpret_cast<const float4 *>(Sg + i);
       v[i] = f.x, v[i + 1] = f.y, v[i + 2] = f.z, v[i + 3] = f.w;
     }
-    tmem_st32(trow + kColS + ic0, v);
     put_row(v);
+    // the TMEM state is kept pre-multiplied by the decay of the chunk about
+    // to be accumulated onto it (S <- gamma_n S + E~^T K)
+    if (NC > 0) {
+      const float g0 = expf(sG[min(kChunk, L) - 1]);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= g0;
+    }
+    tmem_st32(trow + kColS + ic0, v);
   }
   fence_async_smem();
   tc_fence_before();
@@ -781,16 +997,61 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
   constexpr int pa[3] = {0, 0, 1}, pb[3] = {0, 1, 0};  // (hi,hi), (hi,lo), (lo,hi)
   constexpr uint32_t sbo128 = (D / 8) * 128, sbo64 = (kChunk / 8) * 128;
   constexpr uint32_t idesc64 = umma_idesc_bf16(128, kChunk), idesc128 = umma_idesc_bf16(128, D);
+  constexpr uint32_t idesc192 = umma_idesc_bf16(128, 192);
+  // [E'a | QS | E'c] of chunk c lives in the columns of its parity, so that
+  // chunk c+1's products 1 can run while chunk c's outputs are read out
+  auto col_e = [](int c) -> uint32_t { return (c & 1) ? kColE1 : kColE; };
+  // ---- products 1 of chunk c (thread 0):
+  //   [E'a | QS | E'c]^T = S_hi [W_hi; Q_hi; W_lo]^T     (N = 192)
+  //   E'a^T += S_lo W_hi^T                                (N = 64)
+  // so E'^T = E'a^T + E'c^T takes the three passes and QS^T (outputs only)
+  // the one ----
+  auto issue_p1 = [&](int c) -> bool {
+    const bool ok = mbar_wait_bounded(&bars[0], uint32_t(c) & 1u);
+    if (ok) {
+      pend_wq = -1;
+      tc_fence_after();
+      static_assert(Lay::Q_hi == Lay::W_hi + kT128 && Lay::W_lo == Lay::Q_hi + kT128, "[W_hi; Q_hi; W_lo]");
+      const uint32_t ce = col_e(c);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k)
+        umma_bf16(tm + ce, umma_desc(sbase + Lay::S_hi + k * 256, 128, sbo128),
+                  umma_desc(sbase + Lay::W_hi + k * 256, 128, sbo128), idesc192, k > 0);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k)
+        umma_bf16(tm + ce, umma_desc(sbase + Lay::S_lo + k * 256, 128, sbo128),
+                  umma_desc(sbase + Lay::W_hi + k * 256, 128, sbo128), idesc64, true);
+    }
+    umma_commit(&bars[2]);  // also arrives when nothing was issued
+    return ok;
+  };
+  // per-token factors of chunk c (threads < 64), in the buffers of its parity
+  auto factors = [&](int c) {
+    if (tid < kChunk) {
+      const int n = min(kChunk, L - c * kChunk);
+      const float *Gs = sG + (c & 1) * kChunk;
+      sDec[(c & 1) * kChunk + tid] = tid < n ? expf(Gs[n - 1] - Gs[tid]) : 0.f;
+      sGam[(c & 1) * kChunk + tid] = expf(Gs[tid]);
+    }
+  };
+  if (NC > 0) {
+    if (tid == 0 && !issue_p1(0)) s_fail = 1;
+    factors(0);
+  }
+  __syncthreads();  // factors of chunk 0
+
   for (int c = 0; c < NC; ++c) {
     const int t0 = c * kChunk, n = min(kChunk, L - t0);
     const uint32_t ph = uint32_t(c) & 1u;
-    const float *Gs = sG + (c & 1) * kChunk;
-    // the next chunk's gate (threads < 64) and this thread's U of the chunk,
-    // issued before the products
-    float g_next = 0.f;
+    const int par = c & 1;
+    const uint32_t ce = col_e(c);
+    if (s_fail) break;
+    // the next chunk's gates (threads < 64, into the buffer of its parity)
+    // and this thread's U of the chunk, in flight while products 1 finish
+    // (that buffer was last read by the factors of chunk c-1)
     if (tid < kChunk && c + 1 < NC) {
       const int t = (c + 1) * kChunk + tid;
-      g_next = t < L ? p.Gc[bh * Lp + t] : 0.f;
+      sG[((c + 1) & 1) * kChunk + tid] = t < L ? p.Gc[bh * Lp + t] : 0.f;
     }
     float u[16];
     {
@@ -798,68 +1059,32 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
 #pragma unroll
       for (int t = 0; t < 16; ++t) u[t] = Ug[size_t(t) * D];
     }
-    // ---- products 1: E'^T = S W^T, QS^T = S Q^T ----
-    bool ok1 = true;
-    if (tid == 0) {
-      ok1 = mbar_wait_bounded(&bars[0], ph);
-      if (ok1) {
-        pend_wq = -1;
-        tc_fence_after();
-        // [E'^T | QS^T] = S [W; Q]^T over the hi parts (N = 128, columns
-        // kColE..kColE+127 = E' then QS), then E'^T += S_hi W_lo^T
-        static_assert(Lay::Q_hi == Lay::W_hi + kT128 && kColQS == kColE + kChunk, "[W; Q] operand");
-        const uint32_t aS[2] = {sbase + Lay::S_hi, sbase + Lay::S_lo};
-#pragma unroll
-        for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            umma_bf16(tm + kColE, umma_desc(aS[ps] + k * 256, 128, sbo128),
-                      umma_desc(sbase + Lay::W_hi + k * 256, 128, sbo128), idesc128, ps | k);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16(tm + kColE, umma_desc(aS[0] + k * 256, 128, sbo128),
-                    umma_desc(sbase + Lay::W_lo + k * 256, 128, sbo128), idesc64, true);
-      }
-      umma_commit(&bars[2]);  // also arrives when nothing was issued
-    }
-    // per-token factors of this chunk, once
-    if (tid < kChunk) {
-      const float Gn = Gs[n - 1];
-      sDec[tid] = tid < n ? expf(Gn - Gs[tid]) : 0.f;
-      sGam[tid] = expf(Gs[tid]);
-    }
-    __syncthreads();
-    ok1 = mbar_wait_bounded(&bars[2], ph) && ok1;
+    const bool ok1 = mbar_wait_bounded(&bars[2], ph);
     tc_fence_after();
     if (!ok1) s_fail = 1;
     if (tid == 0 && ok1 && c + 1 < NC) {  // W and Q tiles are free
       load_wq(c + 1);
       pend_wq = c + 1;
     }
-    // ---- epilogue 1: E^T and decayed E^T tiles; S <- gamma_n S ----
+    // ---- epilogue 1: E^T and decayed E^T tiles ----
     {
-      float ep[16], ev[16], et[16];
-      tmem_ld16(trow + kColE + tc0, ep);
+      const float *dec = sDec + par * kChunk;
+      float ea[16], ec[16], ev[16], et[16];
+      tmem_ld16x2(trow + ce + tc0, trow + ce + 2 * kChunk + tc0, ea, ec);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int t = tc0 + k;
-        ev[k] = t < n ? u[k] - ep[k] : 0.f;
-        et[k] = ev[k] * sDec[t];
+        ev[k] = t < n ? u[k] - (ea[k] + ec[k]) : 0.f;
+        et[k] = ev[k] * dec[t];
       }
 #pragma unroll
       for (int t8 = 0; t8 < 16; t8 += 8) {
         const uint32_t o = canon_off(j, tc0 + t8, kChunk);
-        store8_split(ev + t8, reinterpret_cast<uint16_t *>(smem + Lay::E_hi + o),
-                     reinterpret_cast<uint16_t *>(smem + Lay::E_lo + o));
+        store8_split(ev + t8, reinterpret_cast<uint16_t *>(smem + Lay::E_hi + o), nullptr);
         store8_split(et + t8, reinterpret_cast<uint16_t *>(smem + Lay::Et_hi + o),
                      reinterpret_cast<uint16_t *>(smem + Lay::Et_lo + o));
       }
-      const float gn = sGam[n - 1];
-      float v[32];
-      tmem_ld32(trow + kColS + ic0, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= gn;
-      tmem_st32(trow + kColS + ic0, v);
+      tmem_wait_st();  // the previous epilogue's decayed state is in place
     }
     fence_async_smem();
     tc_fence_before();
@@ -873,15 +1098,14 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       if (ok2) {
         pend_kp = -1;
         tc_fence_after();
-        const uint32_t aE[2] = {sbase + Lay::E_hi, sbase + Lay::E_lo};
+        const uint32_t aE = sbase + Lay::E_hi;
         const uint32_t aEt[2] = {sbase + Lay::Et_hi, sbase + Lay::Et_lo};
         const uint32_t bK[2] = {sbase + Lay::Kt_hi, sbase + Lay::Kt_lo};
+        // O^T only enters the bf16 outputs: one pass
 #pragma unroll
-        for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-          for (int k = 0; k < kChunk / 16; ++k)
-            umma_bf16(tm + kColEP, umma_desc(aE[ps] + k * 256, 128, sbo64),
-                      umma_desc(sbase + Lay::Pm_hi + k * 256, 128, sbo64), idesc64, ps | k);
+        for (int k = 0; k < kChunk / 16; ++k)
+          umma_bf16(tm + ce + 2 * kChunk, umma_desc(aE + k * 256, 128, sbo64),
+                    umma_desc(sbase + Lay::Pm_hi + k * 256, 128, sbo64), idesc64, k > 0);
 #pragma unroll
         for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
@@ -898,25 +1122,39 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       load_kp(c + 1);
       pend_kp = c + 1;
     }
-    // ---- epilogue 2: outputs, then the A tiles of the updated state ----
+    // ---- epilogue 2: the A tiles of the updated state (the next chunk's
+    // products 1 wait for them); this chunk's QS^T and O^T into registers ----
+    float qs[16], eo[16];
+    tmem_ld16x2(trow + ce + kChunk + tc0, trow + ce + 2 * kChunk + tc0, qs, eo);
     {
-      float qs[16], ep[16];
-      tmem_ld16(trow + kColQS + tc0, qs);
-      tmem_ld16(trow + kColEP + tc0, ep);
-      uint16_t *o = p.out + ((size_t(b) * L + t0 + tc0) * H_v + h) * D + j;
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (tc0 + k < n) o[size_t(k) * H_v * D] = f2bf(fmaf(sGam[tc0 + k], qs[k], ep[k]));
       float v[32];
       tmem_ld32(trow + kColS + ic0, v);
       put_row(v);
+      if (c + 1 < NC) {  // the TMEM state, decayed for the next chunk
+        const float gn = expf(sG[((c + 1) & 1) * kChunk + min(kChunk, L - (c + 1) * kChunk) - 1]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= gn;
+        tmem_st32_async(trow + kColS + ic0, v);
+      }
     }
-    if (tid < kChunk && c + 1 < NC) sG[((c + 1) & 1) * kChunk + tid] = g_next;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (s_fail) break;
+    // ---- the next chunk's products 1 run while this chunk's outputs go out ----
+    if (c + 1 < NC) {
+      if (tid == 0 && !issue_p1(c + 1)) s_fail = 1;
+      factors(c + 1);
+    }
+    {
+      const float *gam = sGam + par * kChunk;
+      uint16_t *o = p.out + ((size_t(b) * L + t0 + tc0) * H_v + h) * D + j;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (tc0 + k < n) o[size_t(k) * H_v * D] = f2bf(fmaf(gam[tc0 + k], qs[k], eo[k]));
+    }
+    __syncthreads();  // the next chunk's factors (and any failure) are visible
   }
   if (!s_fail) {
     float v[32];
@@ -962,7 +1200,10 @@ __global__ void prefill_ring_kernel(const PrefillParams p) {
 template <int D>
 static cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream) {
   cudaError_t e;
-  e = launch_pdl(prefill_conv_kernel<D>, dim3(p.NCp, 2 * p.H_k + p.H_v, p.B), dim3(D), stream, p);
+  if constexpr (state_pass_tc(D))
+    e = launch_pdl(prefill_conv128_kernel, dim3(p.NCp, 2 * p.H_k + p.H_v, p.B), dim3(128), stream, p);
+  else
+    e = launch_pdl(prefill_conv_kernel<D>, dim3(p.NCp, 2 * p.H_k + p.H_v, p.B), dim3(D), stream, p);
   if (e != cudaSuccess) return e;
   // the ring update must follow the conv (which reads the old window) and
   // precede the state pass (which advances offsets)
@@ -1038,7 +1279,6 @@ cudaError_t launch_prefill(const uint16_t *x, const uint16_t *w, const float *g,
   p.Gc = reinterpret_cast<float *>(base + l.Gc);
   p.Pm = reinterpret_cast<float *>(base + l.Pm);
   p.qn_hi = reinterpret_cast<uint16_t *>(base + l.qn_hi);
-  p.qn_lo = reinterpret_cast<uint16_t *>(base + l.qn_lo);
   p.kn_hi = reinterpret_cast<uint16_t *>(base + l.kn_hi);
   p.kn_lo = reinterpret_cast<uint16_t *>(base + l.kn_lo);
   p.kt_hi = reinterpret_cast<uint16_t *>(base + l.kt_hi);
