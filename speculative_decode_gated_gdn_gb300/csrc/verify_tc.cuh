@@ -75,16 +75,17 @@ struct VtScalars {
 };
 
 // Shared memory.  S is the fp32 state tile as the swizzled copies leave it.
-// B holds the product's B operand (tf32, K-major, no swizzle: 8-row x
-// 16-byte core matrices of 4 elements, 128 bytes apart along K, 8-row groups
-// 4 KiB apart).  Rows 2T..15 are never read back, so for 2T <= 8 B holds
-// only the first 8-row group and the descriptor's second group falls on the
-// arrays after it.
+// B holds the first 8-row group of the product's B operand (tf32, K-major, no
+// swizzle: 8-row x 16-byte core matrices of 4 elements, 128 bytes apart along
+// K, 8-row groups 4 KiB apart).  The descriptor's second group (rows 8..15)
+// is the 4 KiB after B, the DEFERRED capture arrays: for 2T <= 8 its rows
+// are never read back, and for 2T > 8 rows 8..2T-1 are written there once
+// the captures are dead (applied, or waited for and unused).  That keeps
+// T = 5 at three CTAs per SM.
 template <int T>
 struct VtSmem {
-  static constexpr bool kTwoGroups = 2 * T > 8;
   alignas(1024) float S[kVtD * kVtD];
-  alignas(1024) uint32_t B[(kTwoGroups ? 16 : 8) * kVtD];
+  alignas(1024) uint32_t B[8 * kVtD];
   float ce[T][kVtD];  // DEFERRED: e_t of the verify whose commit is pending
   float ck[T][kVtD];  // DEFERRED: its normalised k_t
   VtScalars<T> sc;
@@ -93,6 +94,9 @@ struct VtSmem {
 // every bulk-copy destination is 16-byte aligned, the tile 1024-byte aligned
 template <int T>
 constexpr bool vt_layout_ok() {
+  // the second 8-row group of B overlays ce, ck: contiguous, and whole when used
+  static_assert(offsetof(VtSmem<T>, ce) == offsetof(VtSmem<T>, B) + 8 * kVtD * 4, "B's second group");
+  static_assert(2 * T <= 8 || 2 * T * kVtD * 4 >= 8 * kVtD * 4, "ce, ck cover B's second group");
   return offsetof(VtSmem<T>, S) % 1024 == 0 && offsetof(VtSmem<T>, B) % 1024 == 0 &&
          offsetof(VtSmem<T>, ce) % 16 == 0 &&
          offsetof(VtSmem<T>, ck) % 16 == 0 && (offsetof(VtSmem<T>, sc) + offsetof(VtScalars<T>, cG)) % 16 == 0 &&
@@ -236,7 +240,7 @@ __device__ __forceinline__ void vt_head_partials(const float (&yq)[T], const flo
 }
 
 template <int T, int MODE>
-__global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
+__global__ void __launch_bounds__(kVtThreads, T <= 5 ? 3 : 2)
     verify_tc_kernel(const __grid_constant__ VerifyParams p) {
   constexpr int D = kVtD, NROW = kVtRowThreads;
   constexpr int NKK = T * (T - 1) / 2, NV = VtScalars<T>::NV;
@@ -577,7 +581,14 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
   vt_conv<T>(tq, xq, p.act, yq);
   vt_conv<T>(tk, xk, p.act, yk);
   vt_conv<T>(tv, xv, p.act, yv);
-  unsigned char *bsm = reinterpret_cast<unsigned char *>(sm.B);
+  // B rows 8..2T-1 overlay the capture arrays: when captures were staged
+  // but no commit applied them (level 2 with nothing pending), their copies
+  // must have landed before these writes
+  bool cap_late = false;
+  if constexpr (2 * T > 8) {
+    if (cap_staged && !applied) cap_late = !mbar_wait_limit(&sc.cbar, 0, wl);
+  }
+  unsigned char *bsm = reinterpret_cast<unsigned char *>(&sm) + offsetof(VtSmem<T>, B);
 #pragma unroll
   for (int t = 0; t < T; ++t) {
     *reinterpret_cast<uint32_t *>(bsm + vt_canon32(t, i)) = f2tf32(yk[t]);
@@ -703,7 +714,7 @@ __global__ void __launch_bounds__(kVtThreads, T <= 2 ? 3 : 2)
       }
     }
   }
-  if (late) give_up();  // (thread 0 flags it and drains the copies)
+  if (late || cap_late) give_up();  // (thread 0 flags it and drains the copies)
   else if (applied && tid == 0) bulk_wait_read_all();
 }
 
