@@ -82,8 +82,12 @@
  * cores in tf32 (the state read truncated to tf32, q and k rounded to it:
  * about 2^-11 of each term's magnitude); these products only enter e_t and
  * o_t through per-head coefficients, and the state itself, every state
- * update, conv, norm, gate and recurrence step stays in fp32.  Its results differ from the CUDA-core path's (d = 32, 64, SNAPSHOT)
- * only by rounding.  The d = 128 tensor-core verify addresses the state as
+ * update, conv, norm, gate and recurrence step stays in fp32.  Its results
+ * differ from the CUDA-core path's (d = 32, 64, SNAPSHOT) only by rounding.
+ * The chunked prefill takes its products on the tensor cores in bf16: three
+ * passes (x = x_hi + x_lo, about 16 bits of each fp32 operand) for every
+ * product that reaches the state, one pass for those that only reach the
+ * bf16 outputs.  The d = 128 tensor-core verify addresses the state as
  * B * H_v * d_v rows of a tensor map, so it needs B * H_v * 128 < 2^31.
  */
 #ifndef GDN_GB300_H
