@@ -26,6 +26,8 @@
 //   prefill_state_kernel  per (value head, 32-row d_v slice): the chunk loop
 //   prefill_ring_kernel   last three raw inputs into the ring
 // The state kernel also advances offsets by L.
+#include <mutex>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -62,6 +64,9 @@ struct PrefillParams {
   uint16_t *pm_hi;          // [B][H_v][NCp] tiles of Pm as [t][s] (K dim = 64)
   uint32_t *status;         // sticky device status word
   int B, L, NC, NCp, H_k, H_v, C, R, act;
+  // the launch covers chunks [seg0, seg1) (seg0 even: whole pairs); the
+  // state pass advances offsets only in the launch with `last` set
+  int seg0, seg1, last;
 };
 
 struct PrefillWs {
@@ -139,7 +144,7 @@ __device__ __forceinline__ void store_tiles(const float (&y)[kChunk], int ch, ui
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(D) prefill_conv_kernel(const PrefillParams p) {
-  const int chunk = blockIdx.x, head = blockIdx.y, b = blockIdx.z;  // head in [0, 2 H_k + H_v)
+  const int chunk = p.seg0 + blockIdx.x, head = blockIdx.y, b = blockIdx.z;  // head in [0, 2 H_k + H_v)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = D / 32;
   __shared__ float s_part[kChunk][NW];
@@ -296,7 +301,7 @@ __device__ __forceinline__ void flush_stage(const ConvStage &st, uint16_t *hi, u
 
 __global__ void __launch_bounds__(128, 4) prefill_conv128_kernel(const PrefillParams p) {
   constexpr int D = 128;
-  const int chunk = blockIdx.x, head = blockIdx.y, b = blockIdx.z;  // head in [0, 2 H_k + H_v)
+  const int chunk = p.seg0 + blockIdx.x, head = blockIdx.y, b = blockIdx.z;  // head in [0, 2 H_k + H_v)
   const int tid = threadIdx.x, o = tid & 15, g = tid >> 4;
   pdl_wait();
   pdl_trigger();
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   float *sBeta = sG + kPairRows;
   float *sColW = sBeta + kPairRows;  // beta_s gamma_s of column s of the pair
 
-  const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int pair = p.seg0 / 2 + blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H_v = p.H_v, H_k = p.H_k, L = p.L;
   const int hk = h / (H_v / H_k);
@@ -957,13 +962,19 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
                    reinterpret_cast<uint16_t *>(smem + Lay::S_lo + o));
     }
   };
+  // this launch's chunks [c_beg, c_end); c_beg is even, so a chunk's parity
+  // (buffers, barrier phases) is the same counted from here or from 0
+  const int c_beg = p.seg0, c_end = p.seg1;
   int pend_wq = -1, pend_kp = -1;  // (thread 0) chunk whose operand copies are in flight
-  if (tid == 0 && NC > 0) {
-    load_wq(0);
-    load_kp(0);
-    pend_wq = pend_kp = 0;
+  if (tid == 0 && c_end > c_beg) {
+    load_wq(c_beg);
+    load_kp(c_beg);
+    pend_wq = pend_kp = c_beg;
   }
-  if (tid < kChunk) sG[tid] = tid < L ? p.Gc[bh * Lp + tid] : 0.f;
+  if (tid < kChunk) {
+    const int t = c_beg * kChunk + tid;
+    sG[tid] = t < L ? p.Gc[bh * Lp + t] : 0.f;
+  }
   tc_fence_before();
   __syncthreads();  // barriers, TMEM address, first gates
   tc_fence_after();
@@ -982,8 +993,8 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     put_row(v);
     // the TMEM state is kept pre-multiplied by the decay of the chunk about
     // to be accumulated onto it (S <- gamma_n S + E~^T K)
-    if (NC > 0) {
-      const float g0 = expf(sG[min(kChunk, L) - 1]);
+    if (c_end > c_beg) {
+      const float g0 = expf(sG[min(kChunk, L - c_beg * kChunk) - 1]);
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] *= g0;
     }
@@ -1034,13 +1045,13 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       sGam[(c & 1) * kChunk + tid] = expf(Gs[tid]);
     }
   };
-  if (NC > 0) {
-    if (tid == 0 && !issue_p1(0)) s_fail = 1;
-    factors(0);
+  if (c_end > c_beg) {
+    if (tid == 0 && !issue_p1(c_beg)) s_fail = 1;
+    factors(c_beg);
   }
-  __syncthreads();  // factors of chunk 0
+  __syncthreads();  // factors of the first chunk
 
-  for (int c = 0; c < NC; ++c) {
+  for (int c = c_beg; c < c_end; ++c) {
     const int t0 = c * kChunk, n = min(kChunk, L - t0);
     const uint32_t ph = uint32_t(c) & 1u;
     const int par = c & 1;
@@ -1049,7 +1060,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     // the next chunk's gates (threads < 64, into the buffer of its parity)
     // and this thread's U of the chunk, in flight while products 1 finish
     // (that buffer was last read by the factors of chunk c-1)
-    if (tid < kChunk && c + 1 < NC) {
+    if (tid < kChunk && c + 1 < c_end) {
       const int t = (c + 1) * kChunk + tid;
       sG[((c + 1) & 1) * kChunk + tid] = t < L ? p.Gc[bh * Lp + t] : 0.f;
     }
@@ -1062,7 +1073,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     const bool ok1 = mbar_wait_bounded(&bars[2], ph);
     tc_fence_after();
     if (!ok1) s_fail = 1;
-    if (tid == 0 && ok1 && c + 1 < NC) {  // W and Q tiles are free
+    if (tid == 0 && ok1 && c + 1 < c_end) {  // W and Q tiles are free
       load_wq(c + 1);
       pend_wq = c + 1;
     }
@@ -1118,7 +1129,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     ok2 = mbar_wait_bounded(&bars[3], ph) && ok2;
     tc_fence_after();
     if (!ok2) s_fail = 1;
-    if (tid == 0 && ok2 && c + 1 < NC) {  // K^T and Pm tiles are free
+    if (tid == 0 && ok2 && c + 1 < c_end) {  // K^T and Pm tiles are free
       load_kp(c + 1);
       pend_kp = c + 1;
     }
@@ -1130,7 +1141,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       float v[32];
       tmem_ld32(trow + kColS + ic0, v);
       put_row(v);
-      if (c + 1 < NC) {  // the TMEM state, decayed for the next chunk
+      if (c + 1 < c_end) {  // the TMEM state, decayed for the next chunk
         const float gn = expf(sG[((c + 1) & 1) * kChunk + min(kChunk, L - (c + 1) * kChunk) - 1]);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gn;
@@ -1143,7 +1154,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     tc_fence_after();
     if (s_fail) break;
     // ---- the next chunk's products 1 run while this chunk's outputs go out ----
-    if (c + 1 < NC) {
+    if (c + 1 < c_end) {
       if (tid == 0 && !issue_p1(c + 1)) s_fail = 1;
       factors(c + 1);
     }
@@ -1167,7 +1178,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     if (pend_wq >= 0) mbar_wait_bounded(&bars[0], uint32_t(pend_wq) & 1u);
     if (pend_kp >= 0) mbar_wait_bounded(&bars[1], uint32_t(pend_kp) & 1u);
   }
-  if (h == 0 && tid == 0) p.offsets[b] += L;
+  if (p.last && h == 0 && tid == 0) p.offsets[b] += L;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1197,68 +1208,147 @@ __global__ void prefill_ring_kernel(const PrefillParams p) {
   for (int i = 0; i < kHist; ++i) ring[size_t(kWinSlot + i) * p.C] = w[i];
 }
 
+// Launch with or without programmatic stream serialization.
+template <typename K>
+static cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                             const PrefillParams &p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <int D>
-static cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream) {
-  cudaError_t e;
-  if constexpr (state_pass_tc(D))
-    e = launch_pdl(prefill_conv128_kernel, dim3(p.NCp, 2 * p.H_k + p.H_v, p.B), dim3(128), stream, p);
-  else
-    e = launch_pdl(prefill_conv_kernel<D>, dim3(p.NCp, 2 * p.H_k + p.H_v, p.B), dim3(D), stream, p);
-  if (e != cudaSuccess) return e;
-  // the ring update must follow the conv (which reads the old window) and
-  // precede the state pass (which advances offsets)
-  e = launch_pdl(prefill_ring_kernel, dim3((p.C + 255) / 256, p.B), dim3(256), stream, p);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefill_chunk_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(TcLayout<D>::total));
-  if (e != cudaSuccess) return e;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.NCp / 2, p.H_v, p.B);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = TcLayout<D>::total;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_chunk_tc_kernel<D>, p);
-    if (e != cudaSuccess) return e;
-  }
-  if constexpr (state_pass_tc(D)) {
+static cudaError_t set_prefill_smem() {
+  cudaError_t e = cudaFuncSetAttribute(prefill_chunk_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(TcLayout<D>::total));
+  if (e == cudaSuccess && state_pass_tc(D))
     e = cudaFuncSetAttribute(prefill_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(StLayout::total));
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.H_v, p.B);
-    cfg.blockDim = dim3(kStThreads);
-    cfg.dynamicSmemBytes = StLayout::total;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_state_tc_kernel, p);
-  }
-  const size_t state_smem = sizeof(StateSmem<D>);
-  e = cudaFuncSetAttribute(prefill_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(state_smem));
-  if (e != cudaSuccess) return e;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(D / kSlice, p.H_v, p.B);
-    cfg.blockDim = dim3(kStateThreads);
-    cfg.dynamicSmemBytes = state_smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_state_kernel<D>, p);
-  }
+  if (e == cudaSuccess && !state_pass_tc(D))
+    e = cudaFuncSetAttribute(prefill_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(StateSmem<D>)));
   return e;
+}
+
+// conv and chunk products of chunks [p.seg0, p.seg1) on `stream`
+template <int D>
+static cudaError_t launch_chunk_stage(const PrefillParams &p, cudaStream_t stream, bool pdl) {
+  const int nchunks = ((p.seg1 + 1) & ~1) - p.seg0;  // whole pairs (the padding chunk past an odd NC)
+  cudaError_t e;
+  if constexpr (state_pass_tc(D))
+    e = launch_ex(prefill_conv128_kernel, dim3(nchunks, 2 * p.H_k + p.H_v, p.B), dim3(128), 0, stream, pdl, p);
+  else
+    e = launch_ex(prefill_conv_kernel<D>, dim3(nchunks, 2 * p.H_k + p.H_v, p.B), dim3(D), 0, stream, pdl, p);
+  if (e != cudaSuccess) return e;
+  // the ring update follows the conv of the first chunks, the only one that
+  // reads the old window
+  if (p.seg0 == 0) {
+    e = launch_ex(prefill_ring_kernel, dim3((p.C + 255) / 256, p.B), dim3(256), 0, stream, pdl, p);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_ex(prefill_chunk_tc_kernel<D>, dim3(nchunks / 2, p.H_v, p.B), dim3(kTcThreads), TcLayout<D>::total,
+                   stream, pdl, p);
+}
+
+template <int D>
+static cudaError_t launch_state_stage(const PrefillParams &p, cudaStream_t stream, bool pdl) {
+  if constexpr (state_pass_tc(D))
+    return launch_ex(prefill_state_tc_kernel, dim3(p.H_v, p.B), dim3(kStThreads), StLayout::total, stream, pdl, p);
+  else
+    return launch_ex(prefill_state_kernel<D>, dim3(D / kSlice, p.H_v, p.B), dim3(kStateThreads),
+                     sizeof(StateSmem<D>), stream, pdl, p);
+}
+
+// The segmented schedule: the sequential state pass of one range of chunks
+// (one CTA per (row, value head): B * H_v SMs) runs on a high-priority side
+// stream while the conv and chunk products of the next range run on the
+// caller's stream on the remaining SMs.  Stream order and events carry every
+// dependency (no kernel waits on another's flag); the segmented launches skip
+// programmatic serialization, so a kernel of the next range never occupies
+// an SM before the state pass it follows has taken its own.
+constexpr int kMaxSegments = 8;
+struct PrefillSide {
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev[kMaxSegments + 1] = {};
+  bool ready = false, failed = false;
+};
+
+static std::mutex &prefill_side_mutex() {
+  static std::mutex m;
+  return m;
+}
+
+// (with prefill_side_mutex held) the current device's side stream and events
+static PrefillSide *prefill_side() {
+  static PrefillSide sides[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  PrefillSide &s = sides[dev];
+  if (!s.ready && !s.failed) {
+    int least = 0, greatest = 0;
+    bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+              cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, greatest) == cudaSuccess;
+    for (int i = 0; ok && i <= kMaxSegments; ++i)
+      ok = cudaEventCreateWithFlags(&s.ev[i], cudaEventDisableTiming) == cudaSuccess;
+    s.ready = ok;
+    s.failed = !ok;
+  }
+  return s.ready ? &s : nullptr;
+}
+
+// Chunk ranges: a short first range (so the state pass starts early), then
+// the rest in up to kMaxSegments - 1 even-sized ranges of whole pairs.
+static int prefill_segments(int NC, int (&bound)[kMaxSegments + 1]) {
+  constexpr int kFirst = 8, kMinRest = 16;
+  if (NC < kFirst + kMinRest) return 0;
+  const int rest = NC - kFirst;
+  int n = (rest + kMinRest - 1) / kMinRest;
+  n = n < kMaxSegments - 1 ? n : kMaxSegments - 1;
+  bound[0] = 0;
+  bound[1] = kFirst;
+  for (int i = 1; i <= n; ++i) {
+    int c = kFirst + int((long(rest) * i) / n);
+    c = i == n ? NC : (c & ~1);
+    bound[i + 1] = c;
+  }
+  return n + 1;
+}
+
+template <int D>
+static cudaError_t launch_prefill_d(const PrefillParams &p0, cudaStream_t stream) {
+  cudaError_t e = set_prefill_smem<D>();
+  if (e != cudaSuccess) return e;
+  int bound[kMaxSegments + 1];
+  const int nseg = state_pass_tc(D) ? prefill_segments(p0.NC, bound) : 0;
+  if (nseg > 1) {
+    std::lock_guard<std::mutex> lock(prefill_side_mutex());
+    PrefillSide *side = prefill_side();
+    if (side) {
+      for (int sgi = 0; sgi < nseg; ++sgi) {
+        PrefillParams p = p0;
+        p.seg0 = bound[sgi], p.seg1 = bound[sgi + 1], p.last = sgi == nseg - 1;
+        if ((e = launch_chunk_stage<D>(p, stream, false)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(side->ev[sgi], stream)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(side->side, side->ev[sgi], 0)) != cudaSuccess) return e;
+        if ((e = launch_state_stage<D>(p, side->side, false)) != cudaSuccess) return e;
+      }
+      if ((e = cudaEventRecord(side->ev[kMaxSegments], side->side)) != cudaSuccess) return e;
+      return cudaStreamWaitEvent(stream, side->ev[kMaxSegments], 0);
+    }
+  }
+  // one range: every kernel on the caller's stream, chained by PDL
+  PrefillParams p = p0;
+  p.seg0 = 0, p.seg1 = p.NC, p.last = 1;
+  if ((e = launch_chunk_stage<D>(p, stream, true)) != cudaSuccess) return e;
+  return launch_state_stage<D>(p, stream, true);
 }
 
 size_t prefill_workspace_bytes(int B, int L, int H_k, int H_v, int D) {

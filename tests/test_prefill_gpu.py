@@ -42,6 +42,9 @@ def fresh_state(geom, seed):
 SHAPES = [  # (B, L, H_k, H_v, d)
     (2, 1, 1, 2, 32), (2, 2, 2, 4, 64), (1, 5, 2, 4, 128), (2, 64, 2, 4, 64), (2, 150, 2, 4, 128),
     (1, 200, 1, 1, 32), (3, 129, 2, 6, 64),
+    # d = 128 prompts of 24+ chunks run as chunk ranges whose state pass
+    # overlaps the next range's products: two ranges, and three with an odd tail
+    (1, 1536, 1, 2, 128), (2, 1600, 2, 4, 128),
 ]
 
 
