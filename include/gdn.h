@@ -330,6 +330,13 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L);
  *  inputs of window ++ prompt; offsets[b] += L; out [B][L][H_v][d_v] bf16.
  * A layer run in DEFERRED mode must be flushed (gdn_flush) first.
  * dims->T and T_max describe the ring the state is primed for (R = 3 + T_max).
+ * At d = 128, for prompts of 24 or more chunks with B * H_v at most half the
+ * SMs, the sequential state pass of each chunk range runs on an internal
+ * high-priority stream of the current device (created on first use) while
+ * the next range's products run on `stream`; events order the two and join
+ * the internal stream back into `stream`, so all work is complete in
+ * `stream` order as for any other call (and a call captured into a CUDA
+ * graph captures both streams).
  * Errors: as gdn_conv_verify; GDN_ERR_WORKSPACE if ws_bytes is too small.
  */
 int gdn_prefill_chunked(const gdn_dims *dims, int L, const gdn_bf16 *x, const gdn_bf16 *conv_w,
