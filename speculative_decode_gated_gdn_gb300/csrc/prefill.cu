@@ -26,6 +26,7 @@
 //   prefill_state_kernel  per (value head, 32-row d_v slice): the chunk loop
 //   prefill_ring_kernel   last three raw inputs into the ring
 // The state kernel also advances offsets by L.
+#include <atomic>
 #include <mutex>
 
 #include "gdn_common.cuh"
@@ -1225,16 +1226,23 @@ static cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaS
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// Raise the kernels' dynamic shared-memory limits, once per device.
 template <int D>
 static cudaError_t set_prefill_smem() {
-  cudaError_t e = cudaFuncSetAttribute(prefill_chunk_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(TcLayout<D>::total));
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(prefill_chunk_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(TcLayout<D>::total));
   if (e == cudaSuccess && state_pass_tc(D))
     e = cudaFuncSetAttribute(prefill_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(StLayout::total));
   if (e == cudaSuccess && !state_pass_tc(D))
     e = cudaFuncSetAttribute(prefill_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(sizeof(StateSmem<D>)));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   return e;
 }
 

@@ -155,3 +155,32 @@ def test_prefill_rejects_bad_arguments(gdn):
                               out, small)
     assert ei.value.code == L.GDN_ERR_WORKSPACE
     assert gpu.offsets[0].item() == 0
+
+
+def test_ranged_prefill_in_a_cuda_graph_is_bit_identical(gdn):
+    """A d = 128 prompt long enough for the ranged schedule (its state pass on
+    the library's internal stream) captured into a CUDA graph and replayed
+    gives the same bits as the direct call: the internal stream joins the
+    capture and is joined back."""
+    geom = synth.Geometry(B=1, T=2, H_k=2, H_v=4, d=128)
+    Lp = 1600
+    st = synth.layer_state(geom, 81, 1)
+    pr = synth.prompt_inputs(geom, 81, Lp)
+    direct = GpuStack(geom, st, synth.active_mask(1), L.GDN_COMMIT_RECOMPUTE, 1)
+    out_direct = gpu_prefill(direct, 0, pr, Lp)
+    torch.cuda.synchronize()
+
+    cap = GpuStack(geom, st, synth.active_mask(1), L.GDN_COMMIT_RECOMPUTE, 1)
+    d = cap.dims
+    ws = torch.empty(L.gdn_prefill_workspace_bytes(d, Lp), dtype=torch.uint8, device="cuda")
+    out = torch.empty((geom.B, Lp, geom.H_v, geom.d), dtype=torch.bfloat16, device="cuda")
+    x, g, beta = dev_bf16(pr["x"]), torch.from_numpy(pr["g"]).cuda(), torch.from_numpy(pr["beta"]).cuda()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        L.gdn_prefill_chunked(d, Lp, x, cap.w[0], g, beta, cap.state[0], cap.ring[0], cap.offsets, out, ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out_direct.view(torch.int16)), "prompt outputs"
+    assert torch.equal(cap.state, direct.state), "primed state"
+    assert np.array_equal(host_bits(cap.ring), host_bits(direct.ring)), "primed window"
+    assert torch.equal(cap.offsets, direct.offsets)
