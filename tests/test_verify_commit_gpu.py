@@ -75,7 +75,7 @@ def test_cohort_b8_t2(gdn, mode):
 SWEEP = [  # (B, T, T_max, H_k, H_v, d)
     (3, 1, 1, 2, 4, 32), (2, 3, 4, 1, 3, 32), (4, 4, 4, 2, 2, 64), (3, 5, 8, 2, 6, 64),
     (2, 6, 6, 1, 2, 128), (2, 7, 8, 2, 4, 128), (3, 8, 8, 2, 4, 128), (5, 2, 3, 3, 6, 128),
-    (2, 8, 8, 4, 4, 32), (3, 4, 4, 2, 4, 128), (2, 5, 8, 1, 4, 128),
+    (2, 8, 8, 4, 4, 32), (3, 4, 4, 2, 4, 128), (2, 5, 8, 1, 4, 128), (2, 1, 2, 2, 2, 128),
 ]
 
 
