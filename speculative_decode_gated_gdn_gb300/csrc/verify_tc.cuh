@@ -78,27 +78,38 @@ struct VtScalars {
 // B holds the first 8-row group of the product's B operand (tf32, K-major, no
 // swizzle: 8-row x 16-byte core matrices of 4 elements, 128 bytes apart along
 // K, 8-row groups 4 KiB apart).  The descriptor's second group (rows 8..15)
-// is the 4 KiB after B, the DEFERRED capture arrays: for 2T <= 8 its rows
-// are never read back, and for 2T > 8 rows 8..2T-1 are written there once
-// the captures are dead (applied, or waited for and unused).  That keeps
-// T = 5 at three CTAs per SM.
+// is the memory after B, the DEFERRED k captures (padded to 8 rows when
+// 2T > 8): for 2T <= 8 its rows are never read back, and for 2T > 8 rows
+// 8..2T-1 are written there once the captures are dead (applied, or waited
+// for and unused).  The e captures, which each thread reads only for its own
+// row, are staged with the k captures for T <= 4 and come straight from
+// global memory above that.  That keeps every T at three CTAs per SM.
+template <int T, bool kStaged>
+struct VtCe {
+  float ce[T][kVtD];  // DEFERRED: e_t of the verify whose commit is pending
+};
+template <int T>
+struct VtCe<T, false> {};
+
 template <int T>
 struct VtSmem {
+  static constexpr int kCkRows = 2 * T > 8 ? 8 : T;
+  static constexpr bool kCeStaged = T <= 4;
   alignas(1024) float S[kVtD * kVtD];
   alignas(1024) uint32_t B[8 * kVtD];
-  float ce[T][kVtD];  // DEFERRED: e_t of the verify whose commit is pending
-  float ck[T][kVtD];  // DEFERRED: its normalised k_t
+  float ck[kCkRows][kVtD];  // DEFERRED: normalised k_t of the verify whose commit is pending
+  VtCe<T, kCeStaged> cep;
   VtScalars<T> sc;
 };
 
 // every bulk-copy destination is 16-byte aligned, the tile 1024-byte aligned
 template <int T>
 constexpr bool vt_layout_ok() {
-  // the second 8-row group of B overlays ce, ck: contiguous, and whole when used
-  static_assert(offsetof(VtSmem<T>, ce) == offsetof(VtSmem<T>, B) + 8 * kVtD * 4, "B's second group");
-  static_assert(2 * T <= 8 || 2 * T * kVtD * 4 >= 8 * kVtD * 4, "ce, ck cover B's second group");
+  // the second 8-row group of B overlays the captures: contiguous, and whole when used
+  static_assert(offsetof(VtSmem<T>, ck) == offsetof(VtSmem<T>, B) + 8 * kVtD * 4, "B's second group");
+  static_assert(2 * T <= 8 || sizeof(VtSmem<T>::ck) >= 8 * kVtD * 4, "ck covers B's second group");
+  static_assert(!VtSmem<T>::kCeStaged || offsetof(VtSmem<T>, cep) % 16 == 0, "ce copy alignment");
   return offsetof(VtSmem<T>, S) % 1024 == 0 && offsetof(VtSmem<T>, B) % 1024 == 0 &&
-         offsetof(VtSmem<T>, ce) % 16 == 0 &&
          offsetof(VtSmem<T>, ck) % 16 == 0 && (offsetof(VtSmem<T>, sc) + offsetof(VtScalars<T>, cG)) % 16 == 0 &&
          (offsetof(VtSmem<T>, sc) + offsetof(VtScalars<T>, bar)) % 8 == 0;
 }
@@ -240,7 +251,7 @@ __device__ __forceinline__ void vt_head_partials(const float (&yq)[T], const flo
 }
 
 template <int T, int MODE>
-__global__ void __launch_bounds__(kVtThreads, T <= 5 ? 3 : 2)
+__global__ void __launch_bounds__(kVtThreads, 3)
     verify_tc_kernel(const __grid_constant__ VerifyParams p) {
   constexpr int D = kVtD, NROW = kVtRowThreads;
   constexpr int NKK = T * (T - 1) / 2, NV = VtScalars<T>::NV;
@@ -330,8 +341,9 @@ __global__ void __launch_bounds__(kVtThreads, T <= 5 ? 3 : 2)
       }
       if (captures) {
         constexpr uint32_t kCap = T * D * sizeof(float);
-        mbar_arrive_expect_tx(&sc.cbar, 2 * kCap + kMaxT * sizeof(float));
-        bulk_g2s(&sm.ce[0][0], p.ws_e + bh * T * D, kCap, &sc.cbar);
+        constexpr bool kCe = VtSmem<T>::kCeStaged;
+        mbar_arrive_expect_tx(&sc.cbar, (kCe ? 2 : 1) * kCap + kMaxT * sizeof(float));
+        if constexpr (kCe) bulk_g2s(&sm.cep.ce[0][0], p.ws_e + bh * T * D, kCap, &sc.cbar);
         bulk_g2s(&sm.ck[0][0], p.ws_k + bh * T * D, kCap, &sc.cbar);
         bulk_g2s(sc.cG, p.ws_G + bh * kMaxT, kMaxT * sizeof(float), &sc.cbar);
       }
@@ -357,14 +369,25 @@ __global__ void __launch_bounds__(kVtThreads, T <= 5 ? 3 : 2)
   auto apply_and_write = [&]() -> bool {
     bool ok = true;
     if (row) {
+      // this row's e_t: staged with the k captures, or (T > 4) straight from
+      // the workspace, in flight while the k captures land
+      const int j = tid;
+      float ej[T];
+      if constexpr (!VtSmem<T>::kCeStaged) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) ej[t] = t < K ? p.ws_e[(bh * T + t) * D + j] : 0.f;
+      }
       ok = mbar_wait_limit(&sc.cbar, 0, wl);
+      if constexpr (VtSmem<T>::kCeStaged) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) ej[t] = sm.cep.ce[t][j];
+      }
       if (ok) {
-        const int j = tid;
         const float GK = sc.cG[K - 1];
         const float gam = expf(GK);
         float f[T];
 #pragma unroll
-        for (int t = 0; t < T; ++t) f[t] = t < K ? expf(GK - sc.cG[t]) * sm.ce[t][j] : 0.f;
+        for (int t = 0; t < T; ++t) f[t] = t < K ? expf(GK - sc.cG[t]) * ej[t] : 0.f;
 #pragma unroll
         for (int c = 0; c < kVtBoxes; ++c) {
           if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
