@@ -645,13 +645,24 @@ def run_e2e(args, sk, world):
     geom, n_layers = sk.geom, sk.n_layers
     K, W = args.steps, args.warmup
     dev = sk.dev
-    pin = lambda t: t.cpu().pin_memory()
-    hx = [pin(x.view(torch.int16)) for x in sk.xs]
-    hg = [pin(g) for g in sk.gs]
-    hb = [pin(b) for b in sk.bs]
-    hk = torch.from_numpy(np.ascontiguousarray(sk.keeps_np)).pin_memory()
-    hout = [torch.empty(sk.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    hoff = [torch.empty(sk.offsets.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
+    # every host buffer is a view of one pinned block (one allocation, 256-byte
+    # aligned views): the copy engines see a few large translations instead of
+    # many small pinned allocations scattered over host memory
+    keeps_t = torch.from_numpy(np.ascontiguousarray(sk.keeps_np))
+    srcs = ([x.view(torch.int16) for x in sk.xs] + list(sk.gs) + list(sk.bs) + [keeps_t]
+            + [torch.empty(sk.out.shape, dtype=torch.bfloat16)] * 2 + [torch.empty(sk.offsets.shape, dtype=torch.int32)] * 2)
+    sizes = [(t.numel() * t.element_size() + 255) // 256 * 256 for t in srcs]
+    block = torch.empty(sum(sizes), dtype=torch.uint8, pin_memory=True)
+    views, off = [], 0
+    for t, n in zip(srcs, sizes):
+        v = block[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)  # the inputs' values (device tensors are copied to the host once here)
+        views.append(v)
+        off += n
+    P = len(sk.xs)
+    hx, hg, hb = views[:P], views[P:2 * P], views[2 * P:3 * P]
+    hk = views[3 * P]
+    hout, hoff = views[3 * P + 1:3 * P + 3], views[3 * P + 3:3 * P + 5]
     dx = [torch.empty(hx[0].shape, dtype=torch.int16, device=dev) for _ in range(2)]
     dg = [torch.empty(hg[0].shape, dtype=torch.float32, device=dev) for _ in range(2)]
     db = [torch.empty(hb[0].shape, dtype=torch.float32, device=dev) for _ in range(2)]
