@@ -421,13 +421,17 @@ __global__ void __launch_bounds__(kVtThreads, 3)
         float f[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) f[t] = t < K ? expf(GK - sc.cG[t]) * ej[t] : 0.f;
-#pragma unroll
+        // deep drafts roll the box and chunk loops (the token loop stays
+        // unrolled, so the arithmetic and its order are unchanged): the fully
+        // unrolled body grows with T and costs instruction fetch
+        constexpr int kApplyUnroll = T >= 5 ? 1 : kVtBoxCols / 4, kApplyUnrollBoxes = T >= 5 ? 1 : kVtBoxes;
+#pragma unroll kApplyUnrollBoxes
         for (int c = 0; c < kVtBoxes; ++c) {
           if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
             ok = false;
             break;
           }
-#pragma unroll
+#pragma unroll kApplyUnroll
           for (int u = 0; u < kVtBoxCols / 4; ++u) {
             float4 *sp = reinterpret_cast<float4 *>(&sm.S[vt_s_idx(c, j, u)]);
             float4 s4 = *sp;
@@ -659,7 +663,7 @@ __global__ void __launch_bounds__(kVtThreads, 3)
   // completed B tile
   if constexpr (kDirectSums) {
     asm volatile("bar.sync 1, %0;" ::"n"(NROW) : "memory");  // every B column is written
-    if (tid < VtScalars<T>::NV) sc.hpart[0][tid] = vt_head_sum_direct<T>(bsm, tid);
+    if (tid < NV) sc.hpart[0][tid] = vt_head_sum_direct<T>(bsm, tid);
   } else {
     vt_head_partials<T>(yq, yk, lane, sc.hpart[warp]);
   }
