@@ -421,10 +421,10 @@ __global__ void __launch_bounds__(kVtThreads, 3)
         float f[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) f[t] = t < K ? expf(GK - sc.cG[t]) * ej[t] : 0.f;
-        // deep drafts roll the box and chunk loops (the token loop stays
+        // drafts past T = 2 roll the box and chunk loops (the token loop stays
         // unrolled, so the arithmetic and its order are unchanged): the fully
         // unrolled body grows with T and costs instruction fetch
-        constexpr int kApplyUnroll = T >= 5 ? 1 : kVtBoxCols / 4, kApplyUnrollBoxes = T >= 5 ? 1 : kVtBoxes;
+        constexpr int kApplyUnroll = T >= 3 ? 1 : kVtBoxCols / 4, kApplyUnrollBoxes = T >= 3 ? 1 : kVtBoxes;
 #pragma unroll kApplyUnrollBoxes
         for (int c = 0; c < kVtBoxes; ++c) {
           if (!mbar_wait_limit(&sc.bar[c], 0, wl)) {
