@@ -250,43 +250,11 @@ __device__ __forceinline__ void vt_head_partials(const float (&yq)[T], const flo
   }
 }
 
-// T >= 7: per-head sum n (the enumeration of vt_head_round) computed whole
-// by one thread from the B tile, which then holds k_t (row t) and q_t (row
-// T + t) in fp32: a short loop of 16-byte shared loads instead of a
-// T(T+1)-term butterfly, so the code no longer grows with T.
-template <int T>
-__device__ __forceinline__ float vt_head_sum_direct(const unsigned char *bsm, int n) {
-  int ra, rb;  // B rows of the two vectors
-  if (n < 2 * T) {
-    const int t = n >> 1;
-    ra = rb = (n & 1) ? t : T + t;  // |q_t|^2, |k_t|^2
-  } else if (n < 2 * T + T * (T - 1) / 2) {
-    int m = n - 2 * T, t = 1;  // k_s . k_t, s < t
-    while (m >= t) m -= t, ++t;
-    ra = m, rb = t;
-  } else {
-    int m = n - 2 * T - T * (T - 1) / 2, t = 0;  // k_s . q_t, s <= t
-    while (m > t) m -= t + 1, ++t;
-    ra = m, rb = T + t;
-  }
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int i4 = 0; i4 < kVtD / 4; ++i4) {
-    const float4 a = *reinterpret_cast<const float4 *>(bsm + vt_canon32(ra, 4 * i4));
-    const float4 c = *reinterpret_cast<const float4 *>(bsm + vt_canon32(rb, 4 * i4));
-    acc[0] = fmaf(a.x, c.x, acc[0]);
-    acc[1] = fmaf(a.y, c.y, acc[1]);
-    acc[2] = fmaf(a.z, c.z, acc[2]);
-    acc[3] = fmaf(a.w, c.w, acc[3]);
-  }
-  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
-}
-
 template <int T, int MODE>
 __global__ void __launch_bounds__(kVtThreads, 3)
     verify_tc_kernel(const __grid_constant__ VerifyParams p) {
   constexpr int D = kVtD, NROW = kVtRowThreads;
-  constexpr int NKK = T * (T - 1) / 2, NV = VtScalars<T>::NV;
+  constexpr int NKK = T * (T - 1) / 2;
   constexpr bool kDef = MODE == GDN_COMMIT_DEFERRED;
   static_assert(2 * T <= kVtN, "the product holds 2T <= 16 vectors");
   static_assert(NROW == D, "one row thread per state row");
@@ -304,7 +272,6 @@ __global__ void __launch_bounds__(kVtThreads, 3)
   const int row0 = int(bh) * D;  // first row of this tile in the state map
   const uint32_t wl = p.wait_limit;
   const bool gated = p.gz != nullptr;
-  constexpr bool kDirectSums = T >= 7;  // per-head sums from the B tile (vt_head_sum_direct)
 
   // With GDN_VERIFY_OVERLAP (level 1) the next kernel may start at once and
   // this one stages its state (and reads its taps, window and pending keep)
@@ -641,6 +608,19 @@ __global__ void __launch_bounds__(kVtThreads, 3)
   vt_conv<T>(tq, xq, p.act, yq);
   vt_conv<T>(tk, xk, p.act, yk);
   vt_conv<T>(tv, xv, p.act, yv);
+  // new raw inputs into ring slots 3..2+T: q/k channels by one CTA of the key
+  // head.  Past T = 2 they go out at once, so that the raw inputs are dead
+  // before the per-head sums (whose butterfly then fits the register budget);
+  // at T <= 2 after the sums, which measured slightly faster there.
+  constexpr bool kRingEarly = T >= 3;
+  auto store_ring = [&]() {
+    if (h % (H_v / H_k) == 0) {
+      vt_store_ring<T>(p, b, cq, xq);
+      vt_store_ring<T>(p, b, ck, xk);
+    }
+    vt_store_ring<T>(p, b, cv, xv);
+  };
+  if constexpr (kRingEarly) store_ring();
   // B rows 8..2T-1 overlay the capture arrays: when captures were staged
   // but no commit applied them (level 2 with nothing pending), their copies
   // must have landed before these writes
@@ -651,38 +631,21 @@ __global__ void __launch_bounds__(kVtThreads, 3)
   unsigned char *bsm = reinterpret_cast<unsigned char *>(&sm) + offsetof(VtSmem<T>, B);
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    // T >= 7 keeps the fp32 values (the tf32 product reads their upper 19
-    // bits) so that the per-head sums below can use them exactly
-    *reinterpret_cast<uint32_t *>(bsm + vt_canon32(t, i)) = kDirectSums ? __float_as_uint(yk[t]) : f2tf32(yk[t]);
-    *reinterpret_cast<uint32_t *>(bsm + vt_canon32(T + t, i)) = kDirectSums ? __float_as_uint(yq[t]) : f2tf32(yq[t]);
+    *reinterpret_cast<uint32_t *>(bsm + vt_canon32(t, i)) = f2tf32(yk[t]);
+    *reinterpret_cast<uint32_t *>(bsm + vt_canon32(T + t, i)) = f2tf32(yq[t]);
   }
   fence_async_smem();  // B is read by the tensor cores
   mbar_arrive(&sc.bready);
-  // the per-head dot products: T <= 6 as each warp's partial sums, T >= 7
-  // (where the butterfly's code is largest) whole, one per thread, from the
-  // completed B tile
-  if constexpr (kDirectSums) {
-    asm volatile("bar.sync 1, %0;" ::"n"(NROW) : "memory");  // every B column is written
-    if (tid < NV) sc.hpart[0][tid] = vt_head_sum_direct<T>(bsm, tid);
-  } else {
-    vt_head_partials<T>(yq, yk, lane, sc.hpart[warp]);
-  }
-  // new raw inputs into ring slots 3..2+T: q/k channels by one CTA of the key head
-  if (h % (H_v / H_k) == 0) {
-    vt_store_ring<T>(p, b, cq, xq);
-    vt_store_ring<T>(p, b, ck, xk);
-  }
-  vt_store_ring<T>(p, b, cv, xv);
+  // the per-head dot products as each warp's partial sums
+  vt_head_partials<T>(yq, yk, lane, sc.hpart[warp]);
+  if constexpr (!kRingEarly) store_ring();
   asm volatile("bar.sync 1, %0;" ::"n"(NROW) : "memory");  // the partial sums are visible
 
   // ---- coefficients of the recurrence, one thread each --------------------------
   {
     // the head sums (the four warps' partials, in warp order) and the
     // cumulative log-decays G_t = g_0 + ... + g_t (in order)
-    auto H = [&](int n) {
-      if constexpr (kDirectSums) return sc.hpart[0][n];
-      else return ((sc.hpart[0][n] + sc.hpart[1][n]) + sc.hpart[2][n]) + sc.hpart[3][n];
-    };
+    auto H = [&](int n) { return ((sc.hpart[0][n] + sc.hpart[1][n]) + sc.hpart[2][n]) + sc.hpart[3][n]; };
     auto Gcum = [&](int t) {
       float a = 0.f;
 #pragma unroll
