@@ -380,6 +380,55 @@ __device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const float (&v)
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// An M = 64 accumulator (cta_group::1) holds row r in lane 32 (r / 16) + r % 16:
+// the first 16 lanes of each warp's quarter.  The 16x32bx2 shape reads those
+// 16 lanes with the whole warp: threads 0-15 get their lane's columns
+// [c, c + N), threads 16-31 the same lanes' columns [c + OFF, c + OFF + N).
+// Two such 8-column loads (any two base columns), then one wait.
+template <int OFF>
+__device__ __forceinline__ void tmem_ld_h8x2(uint32_t ta, uint32_t tb, float (&va)[8], float (&vb)[8]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16], %18;\n\t"
+      "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17], %18;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(ta), "r"(tb), "n"(OFF)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) va[i] = __uint_as_float(r[i]), vb[i] = __uint_as_float(r[8 + i]);
+}
+
+// As tmem_ld_h8x2, one load of 16 columns per half.
+template <int OFF>
+__device__ __forceinline__ void tmem_ld_h16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr), "n"(OFF)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The mirror store of tmem_ld_h16, without waiting for it (tmem_wait_st()).
+template <int OFF>
+__device__ __forceinline__ void tmem_st_h16_async(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %17, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+      "n"(OFF)
+      : "memory");
+}
+
 // Warp-collective store of 32 consecutive fp32 columns of the warp's 32 TMEM
 // lanes (the mirror of tmem_ld32), then wait until the store is done.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {

@@ -856,11 +856,14 @@ __global__ void __launch_bounds__(kStateThreads) prefill_state_kernel(const Pref
 }
 
 // ---------------------------------------------------------------------------
-// 3b. the sequential pass over chunks on the tensor cores (d = 128).  One CTA
-//     per (row, value head); state row j <-> TMEM lane j.  The fp32 state
-//     stays in TMEM for the whole prompt; per chunk of n tokens (t, s index
-//     tokens, i, j state columns and rows):
-//       E'^T = S W^T,   QS^T = S Q^T       M = 128 rows j, N = 64 tokens each, K = d
+// 3b. the sequential pass over chunks on the tensor cores (d = 128).  The
+//     value rows j of the state evolve independently (the delta rule mixes
+//     only its key columns i), so two CTAs per (row, value head) each carry
+//     64 of them, M = 64 in every product (row r of a half in TMEM lane
+//     32 (r / 16) + r % 16).  The fp32 state stays in TMEM for the whole
+//     prompt; per chunk of n tokens (t, s index tokens, i, j state columns
+//     and rows):
+//       E'^T = S W^T,   QS^T = S Q^T       M = 64 rows j, N = 64 tokens each, K = d
 //       E = U - E',  E~_t = exp(G_n - G_t) E_t,  S <- gamma_n S   (epilogue)
 //       O^T = E^T Pm^T                     N = 64 tokens, K = 64 tokens
 //       S += E~^T K                        N = d columns, K = 64 tokens
@@ -877,8 +880,9 @@ __global__ void __launch_bounds__(kStateThreads) prefill_state_kernel(const Pref
 //     new state (all the next products wait for) are written.  Operand tiles
 //     of the next chunk are fetched as soon as the products of this chunk
 //     that read them are done.  The epilogues are spread over 16 warps: warp
-//     w reads TMEM lane quarter w % 4 and takes column group w / 4 (16 tokens
-//     or 32 state columns); the per-token decay factors are computed once per
+//     w reads the 16 rows of TMEM lane quarter w % 4 and takes column group
+//     w / 4, its two half-warps one half of it each (8 tokens or 16 state
+//     columns a thread); the per-token decay factors are computed once per
 //     chunk.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kStCols = 512;
@@ -887,15 +891,16 @@ constexpr uint32_t kStCols = 512;
 constexpr uint32_t kColE = 0, kColE1 = 192, kColS = 384;
 constexpr int kStThreads = 512;
 
+constexpr int kStRows = 64;  // value rows j of the state per CTA
 struct StLayout {  // d = 128, byte offsets in dynamic shared memory
-  static constexpr uint32_t S_hi = 0, S_lo = 32768;          // S [j][i], K = 128: A operand
-  static constexpr uint32_t W_hi = 65536, Q_hi = 81920;      // W, Q [t][i], K = 128: B operands;
-  static constexpr uint32_t W_lo = 98304;                    // [W_hi; Q_hi; W_lo] is one 192-row one
-  static constexpr uint32_t Kt_hi = 114688, Kt_lo = 131072;  // K^T [i][t], K = 64: B operand
-  static constexpr uint32_t Pm_hi = 147456;                  // Pm [t][s], K = 64: B operand
-  static constexpr uint32_t E_hi = 155648;                   // E^T [j][s], K = 64: A operand (bf16)
-  static constexpr uint32_t Et_hi = 188416, Et_lo = 204800;  // decayed E^T [j][t], K = 64: A operand
-  static constexpr uint32_t G = 221184;                      // [2][64] within-chunk G, by chunk parity
+  static constexpr uint32_t S_hi = 0, S_lo = 16384;         // S [j][i] of the half, K = 128: A operand
+  static constexpr uint32_t W_hi = 32768, Q_hi = 49152;     // W, Q [t][i], K = 128: B operands;
+  static constexpr uint32_t W_lo = 65536;                   // [W_hi; Q_hi; W_lo] is one 192-row one
+  static constexpr uint32_t Kt_hi = 81920, Kt_lo = 98304;   // K^T [i][t], K = 64: B operand
+  static constexpr uint32_t Pm_hi = 114688;                 // Pm [t][s], K = 64: B operand
+  static constexpr uint32_t E_hi = 122880;                  // E^T [j][s], K = 64: A operand (bf16)
+  static constexpr uint32_t Et_hi = 131072, Et_lo = 139264;  // decayed E^T [j][t], K = 64: A operand
+  static constexpr uint32_t G = 147456;                     // [2][64] within-chunk G, by chunk parity
   static constexpr uint32_t Dec = G + 2 * kChunk * 4;        // [2][64] exp(G_n - G_t), 0 past n
   static constexpr uint32_t Gam = Dec + 2 * kChunk * 4;      // [2][64] exp(G_t)
   static constexpr uint32_t total = Gam + 2 * kChunk * 4;
@@ -911,10 +916,12 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
   float *sG = reinterpret_cast<float *>(smem + Lay::G);
   float *sDec = reinterpret_cast<float *>(smem + Lay::Dec);
   float *sGam = reinterpret_cast<float *>(smem + Lay::Gam);
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int h = blockIdx.x >> 1, half = blockIdx.x & 1, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group
-  const int j = 32 * quarter + lane;             // this thread's state row
+  const int hl = lane >> 4;                      // half of the column group
+  const int jr = 16 * quarter + (lane & 15);     // this thread's row of the CTA's 64
+  const int j = kStRows * half + jr;             // ... and of the state
   const int H_v = p.H_v, H_k = p.H_k, L = p.L, NC = p.NC;
   const int hk = h / (H_v / H_k);
   const size_t Lp = size_t(NC) * kChunk;
@@ -922,8 +929,8 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
   const uint32_t sbase = smem_u32(smem);
   constexpr uint32_t kT128 = kChunk * D * sizeof(uint16_t);     // a 64 x 128 bf16 tile
   constexpr uint32_t kT64 = kChunk * kChunk * sizeof(uint16_t);  // a 64 x 64 bf16 tile
-  const int tc0 = 16 * cg;  // this thread's 16 tokens of a chunk
-  const int ic0 = 32 * cg;  // this thread's 32 state columns
+  const int tc0 = 16 * cg + 8 * hl;   // this thread's 8 tokens of a chunk
+  const int ic0 = 32 * cg + 16 * hl;  // this thread's 16 state columns
 
   if (tid == 0) {
 #pragma unroll
@@ -954,11 +961,11 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     bulk_g2s(smem + Lay::Kt_lo, p.kt_lo + kq, kT128, &bars[1]);
     bulk_g2s(smem + Lay::Pm_hi, p.pm_hi + pq, kT64, &bars[1]);
   };
-  // bf16 hi/lo of this thread's 32 state columns of row j into the A tiles of S
-  auto put_row = [&](const float (&v)[32]) {
+  // bf16 hi/lo of this thread's 16 state columns of row j into the A tiles of S
+  auto put_row = [&](const float (&v)[16]) {
 #pragma unroll
-    for (int i8 = 0; i8 < 32; i8 += 8) {
-      const uint32_t o = canon_off(j, ic0 + i8, D);
+    for (int i8 = 0; i8 < 16; i8 += 8) {
+      const uint32_t o = canon_off(jr, ic0 + i8, D);
       store8_split(v + i8, reinterpret_cast<uint16_t *>(smem + Lay::S_hi + o),
                    reinterpret_cast<uint16_t *>(smem + Lay::S_lo + o));
     }
@@ -981,13 +988,15 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
   tc_fence_after();
   const uint32_t tm = s_tmem;
   const uint32_t trow = tm + (uint32_t(32 * quarter) << 16);
+  // 16x32bx2 loads and stores: the second half-warp 8 tokens or 16 columns on
+  const uint32_t ttok = trow + 16 * cg, tcol = trow + kColS + 32 * cg;
 
   // the initial state: this thread's columns of row j into TMEM and the A tiles
   float *Sg = p.state + (bh * D + j) * D + ic0;
   {
-    float v[32];
+    float v[16];
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
+    for (int i = 0; i < 16; i += 4) {
       const float4 f = *reinterpret_cast<const float4 *>(Sg + i);
       v[i] = f.x, v[i + 1] = f.y, v[i + 2] = f.z, v[i + 3] = f.w;
     }
@@ -997,9 +1006,10 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     if (c_end > c_beg) {
       const float g0 = expf(sG[min(kChunk, L - c_beg * kChunk) - 1]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= g0;
+      for (int i = 0; i < 16; ++i) v[i] *= g0;
     }
-    tmem_st32(trow + kColS + ic0, v);
+    tmem_st_h16_async<16>(tcol, v);
+    tmem_wait_st();
   }
   fence_async_smem();
   tc_fence_before();
@@ -1008,8 +1018,8 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
 
   constexpr int pa[3] = {0, 0, 1}, pb[3] = {0, 1, 0};  // (hi,hi), (hi,lo), (lo,hi)
   constexpr uint32_t sbo128 = (D / 8) * 128, sbo64 = (kChunk / 8) * 128;
-  constexpr uint32_t idesc64 = umma_idesc_bf16(128, kChunk), idesc128 = umma_idesc_bf16(128, D);
-  constexpr uint32_t idesc192 = umma_idesc_bf16(128, 192);
+  constexpr uint32_t idesc64 = umma_idesc_bf16(kStRows, kChunk), idesc128 = umma_idesc_bf16(kStRows, D);
+  constexpr uint32_t idesc192 = umma_idesc_bf16(kStRows, 192);
   // [E'a | QS | E'c] of chunk c lives in the columns of its parity, so that
   // chunk c+1's products 1 can run while chunk c's outputs are read out
   auto col_e = [](int c) -> uint32_t { return (c & 1) ? kColE1 : kColE; };
@@ -1065,11 +1075,11 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       const int t = (c + 1) * kChunk + tid;
       sG[((c + 1) & 1) * kChunk + tid] = t < L ? p.Gc[bh * Lp + t] : 0.f;
     }
-    float u[16];
+    float u[8];
     {
       const float *Ug = p.U + (bh * Lp + t0 + tc0) * D + j;
 #pragma unroll
-      for (int t = 0; t < 16; ++t) u[t] = Ug[size_t(t) * D];
+      for (int t = 0; t < 8; ++t) u[t] = Ug[size_t(t) * D];
     }
     const bool ok1 = mbar_wait_bounded(&bars[2], ph);
     tc_fence_after();
@@ -1081,19 +1091,18 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     // ---- epilogue 1: E^T and decayed E^T tiles ----
     {
       const float *dec = sDec + par * kChunk;
-      float ea[16], ec[16], ev[16], et[16];
-      tmem_ld16x2(trow + ce + tc0, trow + ce + 2 * kChunk + tc0, ea, ec);
+      float ea[8], ec[8], ev[8], et[8];
+      tmem_ld_h8x2<8>(ttok + ce, ttok + ce + 2 * kChunk, ea, ec);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < 8; ++k) {
         const int t = tc0 + k;
         ev[k] = t < n ? u[k] - (ea[k] + ec[k]) : 0.f;
         et[k] = ev[k] * dec[t];
       }
-#pragma unroll
-      for (int t8 = 0; t8 < 16; t8 += 8) {
-        const uint32_t o = canon_off(j, tc0 + t8, kChunk);
-        store8_split(ev + t8, reinterpret_cast<uint16_t *>(smem + Lay::E_hi + o), nullptr);
-        store8_split(et + t8, reinterpret_cast<uint16_t *>(smem + Lay::Et_hi + o),
+      {
+        const uint32_t o = canon_off(jr, tc0, kChunk);
+        store8_split(ev, reinterpret_cast<uint16_t *>(smem + Lay::E_hi + o), nullptr);
+        store8_split(et, reinterpret_cast<uint16_t *>(smem + Lay::Et_hi + o),
                      reinterpret_cast<uint16_t *>(smem + Lay::Et_lo + o));
       }
       tmem_wait_st();  // the previous epilogue's decayed state is in place
@@ -1136,17 +1145,17 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
     }
     // ---- epilogue 2: the A tiles of the updated state (the next chunk's
     // products 1 wait for them); this chunk's QS^T and O^T into registers ----
-    float qs[16], eo[16];
-    tmem_ld16x2(trow + ce + kChunk + tc0, trow + ce + 2 * kChunk + tc0, qs, eo);
+    float qs[8], eo[8];
+    tmem_ld_h8x2<8>(ttok + ce + kChunk, ttok + ce + 2 * kChunk, qs, eo);
     {
-      float v[32];
-      tmem_ld32(trow + kColS + ic0, v);
+      float v[16];
+      tmem_ld_h16<16>(tcol, v);
       put_row(v);
       if (c + 1 < c_end) {  // the TMEM state, decayed for the next chunk
         const float gn = expf(sG[((c + 1) & 1) * kChunk + min(kChunk, L - (c + 1) * kChunk) - 1]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gn;
-        tmem_st32_async(trow + kColS + ic0, v);
+        for (int i = 0; i < 16; ++i) v[i] *= gn;
+        tmem_st_h16_async<16>(tcol, v);
       }
     }
     fence_async_smem();
@@ -1163,23 +1172,23 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_state_tc_kernel(const P
       const float *gam = sGam + par * kChunk;
       uint16_t *o = p.out + ((size_t(b) * L + t0 + tc0) * H_v + h) * D + j;
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
+      for (int k = 0; k < 8; ++k)
         if (tc0 + k < n) o[size_t(k) * H_v * D] = f2bf(fmaf(gam[tc0 + k], qs[k], eo[k]));
     }
     __syncthreads();  // the next chunk's factors (and any failure) are visible
   }
   if (!s_fail) {
-    float v[32];
-    tmem_ld32(trow + kColS + ic0, v);
+    float v[16];
+    tmem_ld_h16<16>(tcol, v);
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) st_f4(Sg + i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+    for (int i = 0; i < 16; i += 4) st_f4(Sg + i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
   } else if (tid == 0) {
     atomicOr(p.status, GDN_STATUS_TIMEOUT);
     // copies still in flight must land before the CTA leaves
     if (pend_wq >= 0) mbar_wait_bounded(&bars[0], uint32_t(pend_wq) & 1u);
     if (pend_kp >= 0) mbar_wait_bounded(&bars[1], uint32_t(pend_kp) & 1u);
   }
-  if (p.last && h == 0 && tid == 0) p.offsets[b] += L;
+  if (p.last && h == 0 && half == 0 && tid == 0) p.offsets[b] += L;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1269,7 +1278,7 @@ static cudaError_t launch_chunk_stage(const PrefillParams &p, cudaStream_t strea
 template <int D>
 static cudaError_t launch_state_stage(const PrefillParams &p, cudaStream_t stream, bool pdl) {
   if constexpr (state_pass_tc(D))
-    return launch_ex(prefill_state_tc_kernel, dim3(p.H_v, p.B), dim3(kStThreads), StLayout::total, stream, pdl, p);
+    return launch_ex(prefill_state_tc_kernel, dim3(2 * p.H_v, p.B), dim3(kStThreads), StLayout::total, stream, pdl, p);
   else
     return launch_ex(prefill_state_kernel<D>, dim3(D / kSlice, p.H_v, p.B), dim3(kStateThreads),
                      sizeof(StateSmem<D>), stream, pdl, p);
