@@ -401,10 +401,13 @@ __global__ void __launch_bounds__(128, 4) prefill_conv128_kernel(const PrefillPa
 //    tolerance once the decay is weak enough for the state to carry over many
 //    chunks).  QK only forms Pm, which only enters the bf16 outputs: one pass.
 //    The UT transform itself is a forward substitution on the CUDA cores:
-//    each thread solves one column of one chunk's Tm, without block barriers.
+//    each thread of the first warpgroup solves one column of one chunk's Tm,
+//    without block barriers.  Two warpgroups read the accumulators: thread t
+//    and thread t + 128 share TMEM lane t (token t of the pair) and take one
+//    half of each epilogue's columns.
 // ---------------------------------------------------------------------------
 constexpr int kPairRows = 2 * kChunk;  // M of every product
-constexpr int kTcThreads = 128;        // thread t <-> TMEM lane t <-> token t of the pair
+constexpr int kTcThreads = 256;        // thread t <-> TMEM lane t % 128 <-> token t % 128 of the pair
 constexpr uint32_t kTmemCols = 256;    // [0,128): KK then W; [128,256): QK then U
 
 template <int D>
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[6];
   __shared__ uint32_t s_tmem;
-  __shared__ float s_wsum[4];
+  __shared__ float s_wsum[kTcThreads / 32];
   float(*At)[kChunk][kChunk] = reinterpret_cast<float(*)[kChunk][kChunk]>(smem + Lay::R3);
   float *sG = reinterpret_cast<float *>(smem + Lay::misc);
   float *sBeta = sG + kPairRows;
@@ -440,12 +443,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
 
   const int pair = p.seg0 / 2 + blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & (kPairRows - 1), wg = tid / kPairRows;  // token of the pair, warpgroup
   const int H_v = p.H_v, H_k = p.H_k, L = p.L;
   const int hk = h / (H_v / H_k);
   const int c0 = 2 * pair;
   const size_t Lp = size_t(p.NC) * kChunk;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t lane_base = uint32_t(warp * 32) << 16;  // this warp's TMEM lanes
+  const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
   if (tid == 0) {
 #pragma unroll
@@ -471,8 +475,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
     bulk_g2s(smem + Lay::R2 + 2 * Lay::tr_tile, p.kt_lo + kq, 2 * Lay::tr_tile, &bars[1]);
   }
 
-  // within-chunk cumulative log-decay: threads 0-63 scan chunk c0, 64-127 chunk c0+1
-  const int tok = c0 * kChunk + tid;
+  // within-chunk cumulative log-decay: rows 0-63 scan chunk c0, 64-127 chunk
+  // c0+1 (both warpgroups, the first one stores it)
+  const int tok = c0 * kChunk + row;
   float gt = 0.f, bt = 0.f;
   if (tok < L) {
     gt = p.g[(size_t(b) * L + tok) * H_v + h];
@@ -489,8 +494,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   __syncthreads();  // barriers, TMEM address, warp sums
   tc_fence_after();
   if (warp & 1) incl += s_wsum[warp - 1];
-  sG[tid] = incl;
-  sBeta[tid] = bt;
+  if (wg == 0) {
+    sG[row] = incl;
+    sBeta[row] = bt;
+  }
   const uint32_t tmem = s_tmem;
   bool ok = true;
 
@@ -524,15 +531,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   __syncthreads();  // sG / sBeta of every token are visible
 
   // ---- epilogue 1: A (strictly lower, beta- and decay-weighted KK) and Pm ---
-  const int q = tid >> 6, tl = tid & (kChunk - 1);  // chunk in the pair, row in the chunk
+  const int q = row >> 6, tl = row & (kChunk - 1);  // chunk in the pair, row in the chunk
   const int chunk = c0 + q;
   if (ok) {
-    const float Gt = sG[tid], bq = sBeta[tid];
+    const float Gt = sG[row], bq = sBeta[row];
     const int cb = q * kChunk;
     float *Pg = p.Pm + (((size_t(b) * H_v + h) * p.NC + chunk) * kChunk + tl) * kChunk;
     uint16_t *Pt = p.pm_hi + ((size_t(b) * H_v + h) * p.NCp + chunk) * kChunk * kChunk;
-#pragma unroll
-    for (int cc = 0; cc < kChunk; cc += 32) {
+    {  // this warpgroup's 32 of the chunk's 64 columns
+      const int cc = 32 * wg;
       float kk[32], qk[32], pm[32];
       tmem_ld32(tmem + lane_base + cb + cc, kk);
       tmem_ld32(tmem + lane_base + 128 + cb + cc, qk);
@@ -570,7 +577,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   const int s = tl;
   float *xq = reinterpret_cast<float *>(smem + Lay::R1 + Lay::xs_off) + q * kChunk * kChunk;
   auto xsw = [](int u, int col) { return u * kChunk + (col ^ ((u & 7) << 3)); };
-  if (ok) {
+  if (ok && wg == 0) {
     for (int ib = 0; ib < kChunk / kBlk; ++ib) {
       const int r0 = ib * kBlk;
       float y[kBlk];
@@ -603,9 +610,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   // by rows: item (chunk, row t, columns 8 c8 .. 8 c8 + 7) is one 16-byte row
   // of a core matrix, and eight consecutive threads (rows t .. t+7) fill a
   // whole 128-byte core matrix.
-  if (ok) sColW[tid] = sBeta[tid] * expf(sG[tid]);  // column tid of the pair
+  if (ok && wg == 0) sColW[row] = sBeta[row] * expf(sG[row]);  // column `row` of the pair
   __syncthreads();  // every column is solved (and the U lo tile may reuse its space below)
-  constexpr int kItems = kPairRows * kChunk / 8 / kTcThreads;  // 8 per thread
+  constexpr int kItems = kPairRows * kChunk / 8 / kTcThreads;  // 4 per thread
   float rv[kItems][8];
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
@@ -698,13 +705,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   }
 
   // ---- epilogue 2: W and U rows (fp32) for the state pass; decay -----------
+  // (columns per warpgroup: half of d, or all of it in the first one when d < 64)
+  constexpr int kEpCols = D >= 64 ? D / 2 : D;
+  const int ep0 = wg * kEpCols;
   const bool okw = mbar_wait_bounded(&bars[3], 0) && ok;
   tc_fence_after();
   if (okw && chunk < p.NC) {
     float *Wg = p.W + ((size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl) * D;
     const size_t wt = ((size_t(b) * H_v + h) * p.NCp + chunk) * tile_el;
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = ep0; cc < ep0 + kEpCols && cc < D; cc += 32) {  // this warpgroup's columns
       float v[32];
       tmem_ld32(tmem + lane_base + cc, v);
       if constexpr (state_pass_tc(D)) {
@@ -718,14 +728,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
         for (int j = 0; j < 32; j += 4) st_f4(Wg + cc + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
       }
     }
-    p.Gc[(size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl] = sG[tid];
+    if (wg == 0) p.Gc[(size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl] = sG[row];
   }
   const bool oku = mbar_wait_bounded(&bars[5], 0) && okw;
   tc_fence_after();
   if (oku && chunk < p.NC) {
     float *Ug = p.U + ((size_t(b) * H_v + h) * Lp + size_t(chunk) * kChunk + tl) * D;
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = ep0; cc < ep0 + kEpCols && cc < D; cc += 32) {  // this warpgroup's columns
       float v[32];
       tmem_ld32(tmem + lane_base + 128 + cc, v);
 #pragma unroll
