@@ -402,12 +402,13 @@ __global__ void __launch_bounds__(128, 4) prefill_conv128_kernel(const PrefillPa
 //    chunks).  QK only forms Pm, which only enters the bf16 outputs: one pass.
 //    The UT transform itself is a forward substitution on the CUDA cores:
 //    each thread of the first warpgroup solves one column of one chunk's Tm,
-//    without block barriers.  Two warpgroups read the accumulators: thread t
-//    and thread t + 128 share TMEM lane t (token t of the pair) and take one
-//    half of each epilogue's columns.
+//    without block barriers.  Four warpgroups read the accumulators: threads
+//    t, t + 128, t + 256 and t + 384 share TMEM lane t (token t of the pair)
+//    and take one quarter of each epilogue's columns.
 // ---------------------------------------------------------------------------
 constexpr int kPairRows = 2 * kChunk;  // M of every product
-constexpr int kTcThreads = 256;        // thread t <-> TMEM lane t % 128 <-> token t % 128 of the pair
+constexpr int kTcThreads = 512;        // thread t <-> TMEM lane t % 128 <-> token t % 128 of the pair
+constexpr int kTcGroups = kTcThreads / kPairRows;  // warpgroups
 constexpr uint32_t kTmemCols = 256;    // [0,128): KK then W; [128,256): QK then U
 
 template <int D>
@@ -476,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   }
 
   // within-chunk cumulative log-decay: rows 0-63 scan chunk c0, 64-127 chunk
-  // c0+1 (both warpgroups, the first one stores it)
+  // c0+1 (every warpgroup, the first one stores it)
   const int tok = c0 * kChunk + row;
   float gt = 0.f, bt = 0.f;
   if (tok < L) {
@@ -538,13 +539,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
     const int cb = q * kChunk;
     float *Pg = p.Pm + (((size_t(b) * H_v + h) * p.NC + chunk) * kChunk + tl) * kChunk;
     uint16_t *Pt = p.pm_hi + ((size_t(b) * H_v + h) * p.NCp + chunk) * kChunk * kChunk;
-    {  // this warpgroup's 32 of the chunk's 64 columns
-      const int cc = 32 * wg;
-      float kk[32], qk[32], pm[32];
-      tmem_ld32(tmem + lane_base + cb + cc, kk);
-      tmem_ld32(tmem + lane_base + 128 + cb + cc, qk);
+    {  // this warpgroup's 16 of the chunk's 64 columns
+      constexpr int kE1 = kChunk / kTcGroups;
+      const int cc = kE1 * wg;
+      float kk[kE1], qk[kE1], pm[kE1];
+      tmem_ld16x2(tmem + lane_base + cb + cc, tmem + lane_base + 128 + cb + cc, kk, qk);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < kE1; ++j) {
         const int sl = cc + j;
         const float decay = sl <= tl ? expf(Gt - sG[cb + sl]) : 0.f;
         At[q][sl][tl] = sl < tl ? bq * decay * kk[j] : 0.f;
@@ -553,11 +554,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
       if (chunk < p.NC) {
         if constexpr (state_pass_tc(D)) {
 #pragma unroll
-          for (int s8 = 0; s8 < 32; s8 += 8)
+          for (int s8 = 0; s8 < kE1; s8 += 8)
             store8_split(pm + s8, Pt + canon_off(tl, cc + s8, kChunk) / 2, nullptr);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) Pg[cc + j] = pm[j];
+          for (int j = 0; j < kE1; ++j) Pg[cc + j] = pm[j];
         }
       }
     }
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   // whole 128-byte core matrix.
   if (ok && wg == 0) sColW[row] = sBeta[row] * expf(sG[row]);  // column `row` of the pair
   __syncthreads();  // every column is solved (and the U lo tile may reuse its space below)
-  constexpr int kItems = kPairRows * kChunk / 8 / kTcThreads;  // 4 per thread
+  constexpr int kItems = kPairRows * kChunk / 8 / kTcThreads;  // 2 per thread
   float rv[kItems][8];
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
@@ -705,8 +706,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   }
 
   // ---- epilogue 2: W and U rows (fp32) for the state pass; decay -----------
-  // (columns per warpgroup: half of d, or all of it in the first one when d < 64)
-  constexpr int kEpCols = D >= 64 ? D / 2 : D;
+  // (columns per warpgroup: a quarter of d, at least 32, the last warpgroups
+  // idle when d < 128)
+  constexpr int kEpCols = D / kTcGroups >= 32 ? D / kTcGroups : 32;
   const int ep0 = wg * kEpCols;
   const bool okw = mbar_wait_bounded(&bars[3], 0) && ok;
   tc_fence_after();
