@@ -579,11 +579,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_chunk_tc_kernel(const P
   float *xq = reinterpret_cast<float *>(smem + Lay::R1 + Lay::xs_off) + q * kChunk * kChunk;
   auto xsw = [](int u, int col) { return u * kChunk + (col ^ ((u & 7) << 3)); };
   if (ok && wg == 0) {
+#pragma unroll
     for (int ib = 0; ib < kChunk / kBlk; ++ib) {
       const int r0 = ib * kBlk;
       float y[kBlk];
 #pragma unroll
       for (int rr = 0; rr < kBlk; ++rr) y[rr] = r0 + rr == s ? 1.f : 0.f;
+#pragma unroll 4  // the loads of four solved rows in flight together
       for (int u = 0; u < r0; ++u) {
         const float xu = xq[xsw(u, s)];
         const float4 *ac = reinterpret_cast<const float4 *>(&At[q][u][r0]);
