@@ -300,7 +300,7 @@ __device__ __forceinline__ void flush_stage(const ConvStage &st, uint16_t *hi, u
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(128, 4) prefill_conv128_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(128, 5) prefill_conv128_kernel(const PrefillParams p) {
   constexpr int D = 128;
   const int chunk = p.seg0 + blockIdx.x, head = blockIdx.y, b = blockIdx.z;  // head in [0, 2 H_k + H_v)
   const int tid = threadIdx.x, o = tid & 15, g = tid >> 4;
