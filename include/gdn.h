@@ -330,8 +330,8 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L);
  *  inputs of window ++ prompt; offsets[b] += L; out [B][L][H_v][d_v] bf16.
  * A layer run in DEFERRED mode must be flushed (gdn_flush) first.
  * dims->T and T_max describe the ring the state is primed for (R = 3 + T_max).
- * At d = 128, for prompts of 24 or more chunks with B * H_v at most half the
- * SMs, the sequential state pass of each chunk range runs on an internal
+ * At d = 128, for prompts of 24 or more chunks with 2 * B * H_v at most the
+ * SM count, the sequential state pass of each chunk range runs on an internal
  * high-priority stream of the current device (created on first use) while
  * the next range's products run on `stream`; events order the two and join
  * the internal stream back into `stream`, so all work is complete in

@@ -1335,6 +1335,19 @@ static PrefillSide *prefill_side() {
   return s.ready ? &s : nullptr;
 }
 
+// SMs of the current device (cached per device; 0 if unknown).
+static int prefill_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (!n) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 0) n = 0;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 // Chunk ranges: a short first range (so the state pass starts early), then
 // the rest in up to kMaxSegments - 1 even-sized ranges of whole pairs.
 static int prefill_segments(int NC, int (&bound)[kMaxSegments + 1]) {
@@ -1358,7 +1371,10 @@ static cudaError_t launch_prefill_d(const PrefillParams &p0, cudaStream_t stream
   cudaError_t e = set_prefill_smem<D>();
   if (e != cudaSuccess) return e;
   int bound[kMaxSegments + 1];
-  const int nseg = state_pass_tc(D) ? prefill_segments(p0.NC, bound) : 0;
+  // ranges only when a range's state pass (2 B H_v CTAs, one per SM) fits in
+  // one wave beside the products of the next range
+  const bool fits = 2 * p0.B * p0.H_v <= prefill_sm_count();
+  const int nseg = state_pass_tc(D) && fits ? prefill_segments(p0.NC, bound) : 0;
   if (nseg > 1) {
     std::lock_guard<std::mutex> lock(prefill_side_mutex());
     PrefillSide *side = prefill_side();
