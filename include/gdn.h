@@ -331,12 +331,13 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int L);
  * A layer run in DEFERRED mode must be flushed (gdn_flush) first.
  * dims->T and T_max describe the ring the state is primed for (R = 3 + T_max).
  * At d = 128, for prompts of 24 or more chunks with 2 * B * H_v at most the
- * SM count, the sequential state pass of each chunk range runs on an internal
- * high-priority stream of the current device (created on first use) while
- * the next range's products run on `stream`; events order the two and join
- * the internal stream back into `stream`, so all work is complete in
- * `stream` order as for any other call (and a call captured into a CUDA
- * graph captures both streams).
+ * SM count, the sequential state pass of each chunk range runs on `stream`
+ * at the device's highest launch priority while the products of the later
+ * ranges run on an internal stream of the current device (created on first
+ * use), forked from `stream` after the first range's products; events order
+ * the two and `stream` ends behind the last state pass, so all work is
+ * complete in `stream` order as for any other call (and a call captured into
+ * a CUDA graph captures both streams).
  * Errors: as gdn_conv_verify; GDN_ERR_WORKSPACE if ws_bytes is too small.
  */
 int gdn_prefill_chunked(const gdn_dims *dims, int L, const gdn_bf16 *x, const gdn_bf16 *conv_w,

@@ -1232,20 +1232,28 @@ __global__ void prefill_ring_kernel(const PrefillParams p) {
   for (int i = 0; i < kHist; ++i) ring[size_t(kWinSlot + i) * p.C] = w[i];
 }
 
-// Launch with or without programmatic stream serialization.
+// Launch with or without programmatic stream serialization, at the stream's
+// priority or (priority != 0) at that launch priority.
 template <typename K>
 static cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
-                             const PrefillParams &p) {
+                             const PrefillParams &p, int priority = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n++].val.programmaticStreamSerializationAllowed = 1;
+  }
+  if (priority != 0) {
+    attr[n].id = cudaLaunchAttributePriority;
+    attr[n++].val.priority = priority;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
@@ -1290,25 +1298,28 @@ static cudaError_t launch_chunk_stage(const PrefillParams &p, cudaStream_t strea
 }
 
 template <int D>
-static cudaError_t launch_state_stage(const PrefillParams &p, cudaStream_t stream, bool pdl) {
+static cudaError_t launch_state_stage(const PrefillParams &p, cudaStream_t stream, bool pdl, int priority = 0) {
   if constexpr (state_pass_tc(D))
-    return launch_ex(prefill_state_tc_kernel, dim3(2 * p.H_v, p.B), dim3(kStThreads), StLayout::total, stream, pdl, p);
+    return launch_ex(prefill_state_tc_kernel, dim3(2 * p.H_v, p.B), dim3(kStThreads), StLayout::total, stream, pdl, p,
+                     priority);
   else
     return launch_ex(prefill_state_kernel<D>, dim3(D / kSlice, p.H_v, p.B), dim3(kStateThreads),
                      sizeof(StateSmem<D>), stream, pdl, p);
 }
 
-// The segmented schedule: the sequential state pass of one range of chunks
-// (one CTA per (row, value head): B * H_v SMs) runs on a high-priority side
-// stream while the conv and chunk products of the next range run on the
-// caller's stream on the remaining SMs.  Stream order and events carry every
-// dependency (no kernel waits on another's flag); the segmented launches skip
-// programmatic serialization, so a kernel of the next range never occupies
-// an SM before the state pass it follows has taken its own.
+// The segmented schedule: the sequential state pass of each range of chunks
+// (two CTAs per (row, value head): 2 B H_v SMs) runs on the caller's stream
+// at the highest launch priority, the first one chained to the first range's
+// products by programmatic serialization; the conv and chunk products of the
+// later ranges run on a side stream on the remaining SMs, forked once the
+// first range's products are done.  Stream order and events carry every
+// dependency (no kernel waits on another's flag), and the caller's stream
+// ends behind the last state pass, which waited for the last products.
 constexpr int kMaxSegments = 8;
 struct PrefillSide {
   cudaStream_t side = nullptr;
   cudaEvent_t ev[kMaxSegments + 1] = {};
+  int high = 0;  // the device's greatest stream priority
   bool ready = false, failed = false;
 };
 
@@ -1326,7 +1337,8 @@ static PrefillSide *prefill_side() {
   if (!s.ready && !s.failed) {
     int least = 0, greatest = 0;
     bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
-              cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, greatest) == cudaSuccess;
+              cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, least) == cudaSuccess;
+    s.high = greatest;
     for (int i = 0; ok && i <= kMaxSegments; ++i)
       ok = cudaEventCreateWithFlags(&s.ev[i], cudaEventDisableTiming) == cudaSuccess;
     s.ready = ok;
@@ -1382,13 +1394,19 @@ static cudaError_t launch_prefill_d(const PrefillParams &p0, cudaStream_t stream
       for (int sgi = 0; sgi < nseg; ++sgi) {
         PrefillParams p = p0;
         p.seg0 = bound[sgi], p.seg1 = bound[sgi + 1], p.last = sgi == nseg - 1;
-        if ((e = launch_chunk_stage<D>(p, stream, false)) != cudaSuccess) return e;
-        if ((e = cudaEventRecord(side->ev[sgi], stream)) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(side->side, side->ev[sgi], 0)) != cudaSuccess) return e;
-        if ((e = launch_state_stage<D>(p, side->side, false)) != cudaSuccess) return e;
+        if (sgi == 0) {  // products on the caller's stream, the side stream forked behind them
+          if ((e = launch_chunk_stage<D>(p, stream, false)) != cudaSuccess) return e;
+          if ((e = cudaEventRecord(side->ev[0], stream)) != cudaSuccess) return e;
+          if ((e = cudaStreamWaitEvent(side->side, side->ev[0], 0)) != cudaSuccess) return e;
+          if ((e = launch_state_stage<D>(p, stream, true, side->high)) != cudaSuccess) return e;
+        } else {  // products on the side stream, the state pass behind them on the caller's
+          if ((e = launch_chunk_stage<D>(p, side->side, false)) != cudaSuccess) return e;
+          if ((e = cudaEventRecord(side->ev[sgi], side->side)) != cudaSuccess) return e;
+          if ((e = cudaStreamWaitEvent(stream, side->ev[sgi], 0)) != cudaSuccess) return e;
+          if ((e = launch_state_stage<D>(p, stream, false, side->high)) != cudaSuccess) return e;
+        }
       }
-      if ((e = cudaEventRecord(side->ev[kMaxSegments], side->side)) != cudaSuccess) return e;
-      return cudaStreamWaitEvent(stream, side->ev[kMaxSegments], 0);
+      return cudaSuccess;
     }
   }
   // one range: every kernel on the caller's stream, chained by PDL
