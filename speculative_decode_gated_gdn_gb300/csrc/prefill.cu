@@ -17,15 +17,20 @@
 // The first two lines and W, U, Pm depend only on the chunk's inputs and run
 // in parallel over chunks; the last three run sequentially over chunks.
 //
-// Kernels (one stream, in order):
-//   prefill_conv_kernel   conv + SiLU + L2 norm of every token  -> Q, K, V (fp32;
-//                         at d = 128 prefill_conv128_kernel, straight into the
-//                         operand tiles)
+// Kernels, in order (at d = 128 and 24 or more chunks once per chunk range,
+// the state passes and the later ranges' products on two streams; see the
+// segmented schedule below):
+//   prefill_conv_kernel      conv + SiLU + L2 norm of every token -> Q, K, V
+//                            (fp32; at d = 128 prefill_conv128_kernel,
+//                            straight into the operand tiles)
+//   prefill_ring_kernel      last three raw inputs into the ring
 //   prefill_chunk_tc_kernel  per (chunk pair, value head): G, A, Tm, W, U, Pm
-//                         (the products on tcgen05)
-//   prefill_state_kernel  per (value head, 32-row d_v slice): the chunk loop
-//   prefill_ring_kernel   last three raw inputs into the ring
-// The state kernel also advances offsets by L.
+//                            (the products on tcgen05)
+//   prefill_state_tc_kernel  d = 128: per (row, value head, 64 value rows):
+//                            the chunk loop on tcgen05
+//   prefill_state_kernel     d < 128: per (value head, 32-row d_v slice): the
+//                            chunk loop on the CUDA cores
+// The (last) state pass also advances offsets by L.
 #include <atomic>
 #include <mutex>
 

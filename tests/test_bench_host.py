@@ -99,3 +99,29 @@ def test_byte_accounting():
         step = 30 * bench.verify_bytes(g, 6, mode) + bench.commit_bytes(g, 4, 30, mode)
         assert step > mn
     assert 30 * bench.verify_bytes(g, 6, "deferred", 4) + bench.commit_bytes(g, 4, 30, "deferred") == mn
+
+
+def test_source_hash_follows_code_not_comments():
+    src = ('int a = 1;  // a note\n/* a block\n   comment */ const char *s = "// kept";\n'
+           "char q = '\"';\n\n  x = y; /* inline */ z;\n")
+    code = bench.code_only(src)
+    assert "note" not in code and "block" not in code and "inline" not in code
+    assert '"// kept"' in code and "'\"'" in code and "x = y;" in code and "z;" in code
+    # comments, trailing blanks and empty lines do not move the hash; code does
+    assert bench.code_only(src.replace("a note", "another note") + "\n\n// tail\n") == code
+    assert bench.code_only(src.replace("x = y;", "x = w;")) != code
+
+
+def test_profiled_figures_need_a_matching_code_hash(monkeypatch):
+    # a committed ncu figure is reported only while the code it was taken on
+    # is the current code
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    key = next(iter(rec["verify"]))
+    monkeypatch.setattr(bench, "source_hash", lambda kind: rec[kind]["source_hash"] if kind == "prefill"
+                        else rec[kind][key]["source_hash"])
+    assert bench.profiled_traffic("verify", key) == rec["verify"][key]["dram_bytes_per_launch"]
+    assert bench.profiled_tensor_pipe() == rec["prefill"]["tensor_pipe"]
+    monkeypatch.setattr(bench, "source_hash", lambda kind: "0" * 16)
+    assert bench.profiled_traffic("verify", key) is None
+    assert bench.profiled_tensor_pipe() is None
